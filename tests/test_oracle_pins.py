@@ -1,0 +1,378 @@
+"""Pins for the CPU oracle: each test checks it against something other than
+itself (library routines, closed forms, brute force, invariants the pages
+state). CPU only."""
+
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from speculative_drafting_pe_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+# A tiny drafter for whole-pass pins: several heads, GQA group 2, 3 pages.
+TINY = synth.DrafterShape("oracle-pin", hidden=32, n_q_heads=4, n_kv_heads=2, head_dim=8,
+                          ffn=64, vocab=97, dtype="fp32")
+
+
+def _tiny_case(K, B=2, seed=5, prefix=(20, 41)):
+    wl = synth.Workload("pin", TINY, B, K, prefix, (0.7, 0.7), seed)
+    W = synth.make_weights(TINY, seed)
+    inp = synth.make_step_inputs(wl, K=K)
+    return W, inp
+
+
+def _run_oracle(W, inp, K, **kw):
+    Wn = synth.weights_to_numpy(W)
+    return oracle.draft_pass(
+        TINY, Wn, inp.last_token.numpy(), inp.target_hidden.double().numpy(),
+        inp.positions.numpy(), inp.seq_lens.numpy(), inp.page_table.numpy(),
+        inp.k_cache.double().numpy(), inp.v_cache.double().numpy(), K, **kw)
+
+
+# --------------------------------------------------------------- building blocks
+
+def test_rms_norm_matches_torch_library():
+    rng = np.random.default_rng(0)
+    x = rng.normal(size=(5, 7, 33)) * 3.0
+    g = 1.0 + 0.1 * rng.normal(size=33)
+    ref = F.rms_norm(torch.tensor(x), (33,), weight=torch.tensor(g), eps=1e-6).numpy()
+    np.testing.assert_allclose(oracle.rms_norm(x, g, 1e-6), ref, rtol=1e-13, atol=1e-13)
+
+
+def test_silu_matches_torch_library():
+    x = np.linspace(-30, 30, 1001)
+    np.testing.assert_allclose(oracle.silu(x), F.silu(torch.tensor(x)).numpy(), rtol=1e-13, atol=1e-15)
+
+
+def test_rope_equals_complex_rotation():
+    # Rotate-half RoPE is multiplication of z = x1 + i x2 by exp(i * pos * inv_freq).
+    rng = np.random.default_rng(1)
+    hd, theta = 16, 1e4
+    x = rng.normal(size=(6, hd))
+    pos = np.array([0, 1, 7, 100, 2047, 8191])
+    half = hd // 2
+    inv = theta ** (-(np.arange(half) * 2.0) / hd)
+    z = (x[:, :half] + 1j * x[:, half:]) * np.exp(1j * pos[:, None] * inv[None, :])
+    ref = np.concatenate([z.real, z.imag], axis=1)
+    np.testing.assert_allclose(oracle.rope_neox(x, pos, theta), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_rope_special_cases():
+    # position 0 is the identity; hd=2 rotates by exactly `pos` radians.
+    x = np.random.default_rng(2).normal(size=(3, 8))
+    np.testing.assert_array_equal(oracle.rope_neox(x, np.zeros(3), 1e4), x)
+    out = oracle.rope_neox(np.array([[1.0, 0.0]]), np.array([0.5]), 1e4)
+    np.testing.assert_allclose(out, [[np.cos(0.5), np.sin(0.5)]], rtol=1e-15)
+
+
+def test_rope_relative_position_property():
+    # <rope(q, p1), rope(k, p2)> depends only on p1 - p2.
+    rng = np.random.default_rng(3)
+    q, k = rng.normal(size=64), rng.normal(size=64)
+    d1 = oracle.rope_neox(q, np.array(10), 1e4) @ oracle.rope_neox(k, np.array(3), 1e4)
+    d2 = oracle.rope_neox(q, np.array(1007), 1e4) @ oracle.rope_neox(k, np.array(1000), 1e4)
+    assert abs(d1 - d2) < 1e-9
+
+
+def test_attention_matches_torch_sdpa():
+    rng = np.random.default_rng(4)
+    K, nq, nkv, hd, S = 5, 8, 2, 16, 37
+    q = rng.normal(size=(K, nq, hd))
+    k_all = rng.normal(size=(S + K, nkv, hd))
+    v_all = rng.normal(size=(S + K, nkv, hd))
+    out = oracle.causal_paged_attention(q, k_all, v_all, S)
+    G = nq // nkv
+    qt = torch.tensor(q).permute(1, 0, 2)[None]                       # [1, nq, K, hd]
+    kt = torch.tensor(k_all).permute(1, 0, 2).repeat_interleave(G, 0)[None]
+    vt = torch.tensor(v_all).permute(1, 0, 2).repeat_interleave(G, 0)[None]
+    mask = torch.arange(S + K)[None, :] <= (S + torch.arange(K))[:, None]
+    ref = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask)[0].permute(1, 0, 2)
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_gather_prefix_kv_follows_page_table():
+    # Encode (page, head, slot, dim) in the value and read entries back.
+    P, npg, nkv, hd = 16, 9, 2, 3
+    cache = np.zeros((npg, nkv, P, hd))
+    for p, h, s, d in itertools.product(range(npg), range(nkv), range(P), range(hd)):
+        cache[p, h, s, d] = p * 1000 + h * 100 + s + d / 10
+    pt = np.array([7, 2, 5, 0])
+    out = oracle.gather_prefix_kv(cache, pt, 50, P)
+    for e in range(50):
+        page = pt[e // P]
+        for h in range(nkv):
+            assert out[e, h, 0] == page * 1000 + h * 100 + e % P
+
+
+def test_linear_is_x_times_w_transposed():
+    rng = np.random.default_rng(6)
+    x = rng.normal(size=(3, 11))
+    w = rng.normal(size=(40000, 11)).astype(np.float32)
+    ref = F.linear(torch.tensor(x), torch.tensor(w, dtype=torch.float64)).numpy()
+    np.testing.assert_allclose(oracle.linear(x, w), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_argmax_ties_go_to_lowest_index_and_gap():
+    logits = np.array([[1.0, 3.0, 3.0, 2.0], [5.0, 5.0, 5.0, 5.0], [0.0, -1.0, 2.5, 2.0]])
+    np.testing.assert_array_equal(oracle.argmax_lowest(logits), [1, 0, 2])
+    np.testing.assert_allclose(oracle.top2_gap(logits), [0.0, 0.0, 0.5])
+
+
+def test_build_rows_row0_real_rest_placeholders():
+    W, inp = _tiny_case(K=4)
+    Wn = synth.weights_to_numpy(W)
+    h = np.random.default_rng(7).normal(size=(2, TINY.hidden))
+    u, resid = oracle.build_rows(TINY, Wn, inp.last_token.numpy(), h, 4)
+    H = TINY.hidden
+    for b in range(2):
+        e0 = Wn["embed"][inp.last_token[b]]
+        np.testing.assert_allclose(u[b, 0, :H], e0 / np.sqrt(np.mean(e0 ** 2) + 1e-6) * Wn["layers"][0]["norm_e"])
+        np.testing.assert_allclose(resid[b, 0], h[b])
+        for j in range(1, 4):
+            m = Wn["emb_mask"]
+            np.testing.assert_allclose(u[b, j, :H], m / np.sqrt(np.mean(m ** 2) + 1e-6) * Wn["layers"][0]["norm_e"])
+            np.testing.assert_allclose(resid[b, j], Wn["h_shared"])
+
+
+# --------------------------------------------------------------- whole draft pass
+
+def _torch_reference_pass(W, inp, K):
+    """Independent float64 restatement with torch library routines
+    (F.linear, F.rms_norm, F.silu, SDPA, complex-number RoPE) and an explicit
+    per-entry walk of the page table."""
+    cfg = TINY
+    d = torch.float64
+    t = lambda a: a.to(d)
+    B = inp.last_token.shape[0]
+    H, nq, nkv, hd = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    eps = cfg.rms_eps
+
+    def norm(x, g):
+        return F.rms_norm(x, (x.shape[-1],), weight=t(g), eps=eps)
+
+    def rope(x, pos):
+        half = hd // 2
+        inv = cfg.rope_theta ** (-(torch.arange(half, dtype=d) * 2.0) / hd)
+        ang = pos.to(d)[..., None] * inv
+        z = torch.complex(x[..., :half], x[..., half:]) * torch.polar(torch.ones_like(ang), ang)
+        return torch.cat([z.real, z.imag], dim=-1)
+
+    h = F.linear(t(inp.target_hidden), t(W["fc"]))
+    emb = torch.stack([t(W["embed"][int(tok)]) for tok in inp.last_token])
+    L0 = W["layers"][0]
+    logits = torch.empty(B, K, cfg.vocab, dtype=d)
+    for b in range(B):
+        rows_e = [emb[b]] + [t(W["emb_mask"])] * (K - 1)
+        rows_h = [h[b]] + [t(W["h_shared"])] * (K - 1)
+        x = torch.cat([norm(torch.stack(rows_e), L0["norm_e"]), norm(torch.stack(rows_h), L0["norm_h"])], -1)
+        r = torch.stack(rows_h).clone()
+        S = int(inp.seq_lens[b])
+        pos = int(inp.positions[b]) + torch.arange(K)
+        for li, Lw in enumerate(W["layers"]):
+            if li > 0:
+                x = norm(r, Lw["attn_norm"])
+            qkv = F.linear(x, t(Lw["w_qkv"]))
+            q = rope(qkv[:, : nq * hd].reshape(K, nq, hd), pos[:, None])
+            k = rope(qkv[:, nq * hd:(nq + nkv) * hd].reshape(K, nkv, hd), pos[:, None])
+            v = qkv[:, (nq + nkv) * hd:].reshape(K, nkv, hd)
+            ks, vs = [], []
+            for e in range(S):
+                page = int(inp.page_table[b, e // cfg.page_size])
+                ks.append(t(inp.k_cache[li, page, :, e % cfg.page_size, :]))
+                vs.append(t(inp.v_cache[li, page, :, e % cfg.page_size, :]))
+            k_all = torch.cat([torch.stack(ks), k]) if S else k
+            v_all = torch.cat([torch.stack(vs), v]) if S else v
+            G = nq // nkv
+            mask = torch.arange(S + K)[None, :] <= (S + torch.arange(K))[:, None]
+            a = F.scaled_dot_product_attention(
+                q.permute(1, 0, 2)[None],
+                k_all.permute(1, 0, 2).repeat_interleave(G, 0)[None],
+                v_all.permute(1, 0, 2).repeat_interleave(G, 0)[None], attn_mask=mask)
+            r = r + F.linear(a[0].permute(1, 0, 2).reshape(K, nq * hd), t(Lw["w_o"]))
+            x = norm(r, Lw["mlp_norm"])
+            r = r + F.linear(F.silu(F.linear(x, t(Lw["w_gate"]))) * F.linear(x, t(Lw["w_up"])), t(Lw["w_down"]))
+        logits[b] = F.linear(norm(r, W["final_norm"]), t(W["lm_head"]))
+    return logits.numpy()
+
+
+@pytest.mark.parametrize("K", [1, 4])
+def test_draft_pass_matches_independent_torch_restatement(K):
+    # K=1 is one ordinary (sequential) EAGLE step: row 0 only.
+    W, inp = _tiny_case(K)
+    out = _run_oracle(W, inp, K)
+    ref = _torch_reference_pass(W, inp, K)
+    np.testing.assert_allclose(out["logits"], ref, rtol=1e-10, atol=1e-10)
+    ok = out["gap"] > 1e-9
+    np.testing.assert_array_equal(out["drafts"][ok], ref.argmax(-1)[ok])
+
+
+def test_prefix_consistency_and_row0_independent_of_K():
+    # Rows are causal: drafts for K' < K equal the first K' drafts for K.
+    W, inp = _tiny_case(K=6)
+    full = _run_oracle(W, inp, 6)
+    for Kp in (1, 2, 5):
+        part = _run_oracle(W, inp, Kp)
+        np.testing.assert_allclose(part["logits"], full["logits"][:, :Kp], rtol=1e-10, atol=1e-11)
+        ok = part["gap"] > 1e-9
+        np.testing.assert_array_equal(part["drafts"][ok], full["drafts"][:, :Kp][ok])
+
+
+def test_perturbing_later_rows_leaves_earlier_rows_unchanged():
+    W, inp = _tiny_case(K=5)
+    base = _run_oracle(W, inp, 5)
+
+    def hook(u):
+        u = u.copy()
+        u[:, 3:, :] += 0.5
+        return u
+
+    pert = _run_oracle(W, inp, 5, perturb_rows=hook)
+    np.testing.assert_array_equal(pert["logits"][:, :3], base["logits"][:, :3])
+    assert np.abs(pert["logits"][:, 3:] - base["logits"][:, 3:]).max() > 1e-5
+
+
+def test_draft_argmax_exhaustive_on_tiny_vocab():
+    W, inp = _tiny_case(K=3)
+    out = _run_oracle(W, inp, 3)
+    V = TINY.vocab
+    for b, j in itertools.product(range(2), range(3)):
+        row = out["logits"][b, j]
+        best = 0
+        for v in range(V):
+            if row[v] > row[best]:
+                best = v
+        assert out["drafts"][b, j] == best
+
+
+def test_new_kv_rows_are_rotated_with_row_positions():
+    # The k row written for row j equals RoPE(W_k x_j) at position Q_b + j:
+    # un-rotating by the same angle restores an unrotated projection whose
+    # norm equals the rotated one per pair.
+    W, inp = _tiny_case(K=3)
+    out = _run_oracle(W, inp, 3)
+    kn = out["k_new"]
+    assert kn.shape == (4, 2, 3, TINY.n_kv_heads, TINY.head_dim)
+    assert np.isfinite(kn).all() and np.isfinite(out["v_new"]).all()
+
+
+# --------------------------------------------------------------- verify / rebuild
+
+def _brute_accept(d, g):
+    K = len(d)
+    return max(n for n in range(K + 1) if all(d[i] == g[i] for i in range(n)))
+
+
+def test_verify_brute_force_tiny_vocab():
+    V, K = 3, 3
+    ds = np.array(list(itertools.product(range(V), repeat=K)))
+    gs = np.array(list(itertools.product(range(V), repeat=K + 1)))
+    D = np.repeat(ds, len(gs), axis=0)
+    G = np.tile(gs, (len(ds), 1))
+    a, bonus = oracle.verify(D, G)
+    for i in range(len(D)):
+        ai = _brute_accept(D[i], G[i])
+        assert a[i] == ai and bonus[i] == G[i, ai]
+        assert 0 <= a[i] <= K
+
+
+def test_full_acceptance_gives_bonus_and_k_plus_1_tokens():
+    d = np.array([[4, 8, 15, 16]])
+    g = np.array([[4, 8, 15, 16, 23]])
+    a, bonus = oracle.verify(d, g)
+    assert a[0] == 4 and bonus[0] == 23
+    em = oracle.emitted_tokens(d, a, bonus)
+    np.testing.assert_array_equal(em[0], [4, 8, 15, 16, 23])
+    a0, b0 = oracle.verify(d, np.array([[5, 8, 15, 16, 23]]))
+    assert a0[0] == 0 and b0[0] == 5
+    np.testing.assert_array_equal(oracle.emitted_tokens(d, a0, b0)[0], [5, -1, -1, -1, -1])
+
+
+def test_rebuild_against_explicit_slot_lists():
+    rng = np.random.default_rng(8)
+    P = 16
+    for trial in range(200):
+        B, K = 4, int(rng.integers(1, 12))
+        S = rng.integers(0, 100, size=B)
+        Q = S + rng.integers(0, 30, size=B)
+        max_pages = int(np.ceil((S.max() + 2 * K) / P)) + int(rng.integers(0, 2))
+        num_pages = B * max_pages + 3
+        pt = rng.permutation(num_pages)[: B * max_pages].reshape(B, max_pages)
+        a = rng.integers(0, K + 1, size=B)
+        out = oracle.rebuild_metadata(a, K, S, Q, pt, num_pages, P)
+        for b in range(B):
+            slots = np.concatenate([p * P + np.arange(P) for p in pt[b]])   # entry -> slot
+            kept = min(a[b], K - 1) + 1
+            assert out["status"][b] == oracle.REQ_OK
+            assert S[b] + 1 <= out["seq_lens"][b] == S[b] + kept <= S[b] + K
+            assert out["positions"][b] - Q[b] == a[b] + 1
+            np.testing.assert_array_equal(out["slot_mapping"][b], slots[out["seq_lens"][b]: out["seq_lens"][b] + K])
+            rb = out["rollback_slots"][b]
+            n_rb = K - kept
+            np.testing.assert_array_equal(rb[:n_rb], slots[S[b] + kept: S[b] + K])
+            assert (rb[n_rb:] == -1).all()
+            assert set(rb[:n_rb]) <= set(out["slot_mapping"][b])
+
+
+def test_rebuild_capacity_and_bad_page_status():
+    P, K = 16, 4
+    pt = np.array([[0, 1], [2, 3], [4, -1]])
+    S = np.array([27, 28, 10])
+    Q = np.array([30, 30, 12])
+    a = np.array([1, 1, 3])           # kept 2, 2, 4 -> S' = 29, 30, 14
+    out = oracle.rebuild_metadata(a, K, S, Q, pt, num_pages=5, page_size=P)
+    # request 0: S'+K = 33 > 32 -> capacity; request 1 likewise; request 2: entries 14..17
+    # need page index 1 of its table, which is -1 -> bad page.
+    np.testing.assert_array_equal(out["status"], [oracle.REQ_CAPACITY, oracle.REQ_CAPACITY, oracle.REQ_BAD_PAGE])
+    np.testing.assert_array_equal(out["seq_lens"], S)
+    np.testing.assert_array_equal(out["positions"], Q)
+    assert (out["slot_mapping"] == -1).all() and (out["rollback_slots"] == -1).all()
+    out2 = oracle.rebuild_metadata(np.array([0, 0, 0]), K, np.array([27, 0, 0]), Q, pt, 5, P)
+    assert out2["status"][0] == oracle.REQ_OK            # 28 + 4 = 32 fits exactly
+    np.testing.assert_array_equal(out2["slot_mapping"][0], [1 * P + 12, 1 * P + 13, 1 * P + 14, 1 * P + 15])
+
+
+# --------------------------------------------------------------- acceptance statistics
+
+@pytest.mark.parametrize("alpha,K", [(0.7, 3), (0.55, 7), (0.3, 11), (0.8, 11), (0.6, 1)])
+def test_planted_alpha_mean_tokens_matches_closed_form(alpha, K):
+    n, V = 200_000, 1000
+    rng = np.random.default_rng(9)
+    d = rng.integers(0, V, size=(n, K))
+    g = synth.plant_targets(d, np.full(n, alpha), V, seed=int(alpha * 100) + K)
+    a, _ = oracle.verify(d, g)
+    tokens = a + 1
+    mean, sem = tokens.mean(), tokens.std(ddof=1) / np.sqrt(n)
+    exact = oracle.expected_tokens_iid(alpha, K)
+    assert abs(mean - exact) < 4 * sem
+    # the lesson page's 1 + K*alpha bounds it from above, with equality at K = 1
+    assert exact <= oracle.tokens_per_pass_linear(alpha, K) + 1e-12
+    if K == 1:
+        assert abs(exact - oracle.tokens_per_pass_linear(alpha, K)) < 1e-12
+
+
+def test_expected_tokens_closed_form_by_enumeration():
+    # E[a+1] = sum_a (a+1) P(a) with P(a) = alpha^a (1-alpha) for a<K, alpha^K for a=K.
+    for alpha in (0.0, 0.3, 0.55, 0.8, 1.0):
+        for K in range(1, 13):
+            e = sum((a + 1) * alpha ** a * (1 - alpha) for a in range(K)) + (K + 1) * alpha ** K
+            assert abs(oracle.expected_tokens_iid(alpha, K) - e) < 1e-12
+
+
+def test_lesson_page_worked_example():
+    with open(os.path.join(GOLDEN, "lesson_worked_example.json")) as f:
+        gold = json.load(f)
+    ex = gold["speedup_example"]
+    assert abs(oracle.tokens_per_pass_linear(ex["alpha"], ex["K"]) - ex["tokens_per_pass"]) < 1e-12
+    s = oracle.speedup_linear(ex["alpha"], ex["K"], ex["overhead"])
+    assert abs(s - ex["speedup_fraction"][0] / ex["speedup_fraction"][1]) < 1e-12
+    assert round(s, 1) == ex["speedup_printed"]
+    be = gold["breakeven_example"]
+    assert abs(oracle.breakeven_alpha(be["overhead"], be["K"]) - be["alpha_breakeven"]) < 1e-12
+    assert abs(oracle.speedup_linear(be["alpha_breakeven"], be["K"], be["overhead"]) - 1.0) < 1e-12
