@@ -1,0 +1,192 @@
+/*
+ * pe.h — C ABI of libpe.so: P-EAGLE parallel drafting and greedy
+ * verify / batch-metadata rebuild on one GB300 (sm_103a).
+ *
+ * The method (cited by page title and section):
+ *  - "在 Amazon SageMaker AI 上使用 P-EAGLE 并行化推测解码" (Chinese translation
+ *    of the AWS post), section "解决方案概述" (Solution overview):
+ *    "P-EAGLE 如何打破这个链" — learned placeholders emb_mask and h_shared;
+ *    "逐步草稿过程" — Step 1: target hidden states of layers 2, L/2, L-1
+ *    concatenated to 3d; Step 2: position 1 = real token embedding + target
+ *    hidden, positions 2..K = emb_mask + h_shared, all K positions through
+ *    the 4 drafter layers and the LM head in one pass, K drafts at once; the
+ *    target then verifies all K in one pass with the standard acceptance rule.
+ *  - "Amazon SageMaker AIにおけるP-EAGLEによる推論高速化": a fused kernel
+ *    rebuilds the batch metadata after verification.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller unless stated
+ *    otherwise; the library never frees them. Matrices are row-major,
+ *    weight matrices are stored [out, in].
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *    asynchronous on that stream; outputs are valid once it reaches them.
+ *  - The return value is PE_OK or a negative PE_ERR_* code; on error
+ *    pe_last_error() (thread-local) describes it and nothing was enqueued.
+ *  - Problems found on the device for one request (bad page index, cache
+ *    capacity) are reported per request in `status[b]` (PE_REQ_*); other
+ *    requests are unaffected. No kernel traps; every device-side wait is
+ *    bounded and a wait that gives up sets a flag read by pe_device_errors().
+ */
+#ifndef PE_H
+#define PE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PE_ABI_VERSION 1
+
+/* return codes */
+#define PE_OK               0
+#define PE_ERR_ARG         -1   /* null pointer, size out of range, misaligned pointer */
+#define PE_ERR_UNSUPPORTED -2   /* shape the kernels do not implement */
+#define PE_ERR_CUDA        -3   /* a CUDA runtime / driver call failed */
+#define PE_ERR_NOMEM       -4   /* workspace allocation failed */
+
+/* per-request status written by pe_draft and pe_verify_rebuild */
+#define PE_REQ_OK          0
+#define PE_REQ_CAPACITY    1    /* entries needed exceed max_pages * page_size */
+#define PE_REQ_BAD_PAGE    2    /* a needed page-table entry is outside [0, num_pages) */
+#define PE_REQ_BAD_INPUT   3    /* token id outside [0, V), negative length */
+
+/* bits of the device error word (pe_device_errors) */
+#define PE_DEVERR_GEMM_TIMEOUT  1u
+#define PE_DEVERR_ATTN_TIMEOUT  2u
+
+#define PE_DTYPE_BF16 0         /* bf16 weights/activations/KV, fp32 accumulate */
+#define PE_DTYPE_FP32 1         /* fp32 everything; GEMMs run as tf32 */
+
+/* Drafter shape. n_layers must be 4, page_size 16, head_dim 64 or 128,
+ * n_kv_heads must divide n_q_heads, n_q_heads*head_dim and
+ * n_kv_heads*head_dim must be multiples of 128, hidden and ffn multiples
+ * of 64. k_max (1..16) is the largest K any call will pass. */
+typedef struct pe_config {
+    int32_t hidden;       /* H */
+    int32_t n_layers;     /* 4 */
+    int32_t n_q_heads;    /* nq */
+    int32_t n_kv_heads;   /* nkv */
+    int32_t head_dim;     /* hd */
+    int32_t ffn;          /* F (SwiGLU width) */
+    int32_t vocab;        /* V */
+    float   rms_eps;      /* RMSNorm epsilon */
+    float   rope_theta;   /* RoPE base */
+    int32_t page_size;    /* 16 */
+    int32_t k_max;        /* largest K a call may pass */
+    int32_t dtype;        /* PE_DTYPE_* for weights, activations and KV cache */
+} pe_config;
+
+/* Per-layer weights, all of the config dtype, device pointers, 16-byte aligned. */
+typedef struct pe_layer_weights {
+    const void* norm_e;     /* [H]  layer 0 only: gain of RMSNorm on the token embedding half */
+    const void* norm_h;     /* [H]  layer 0 only: gain of RMSNorm on the hidden half */
+    const void* attn_norm;  /* [H]  layers 1..3: pre-attention RMSNorm gain (NULL for layer 0) */
+    const void* w_qkv;      /* [(nq+2nkv)*hd, in], in = 2H for layer 0, H otherwise; rows q | k | v */
+    const void* w_o;        /* [H, nq*hd] */
+    const void* mlp_norm;   /* [H]  pre-MLP RMSNorm gain */
+    const void* w_gate;     /* [F, H] */
+    const void* w_up;       /* [F, H] */
+    const void* w_down;     /* [H, F] */
+} pe_layer_weights;
+
+typedef struct pe_weights {
+    const void* fc;          /* [H, 3H]: fuses [h_lo; h_mid; h_hi] into H */
+    const void* embed;       /* [V, H] token embedding */
+    const void* emb_mask;    /* [H] learned mask-token embedding (positions 2..K) */
+    const void* h_shared;    /* [H] learned shared hidden state (positions 2..K) */
+    const void* final_norm;  /* [H] */
+    const void* lm_head;     /* [V, H] (not tied to embed) */
+    pe_layer_weights layer[4];
+} pe_weights;
+
+typedef struct pe_handle pe_handle;
+
+/* Create a drafter on `device` (the device must be current or will be made
+ * current). Records the weight pointers (caller keeps them alive until
+ * pe_destroy), allocates the workspaces for up to max_batch requests of up to
+ * cfg->k_max rows and builds TMA descriptors for the weights. Synchronous. */
+int pe_init_drafter(const pe_config* cfg, const pe_weights* weights,
+                    int32_t max_batch, int32_t device, pe_handle** out);
+
+/* One parallel draft pass (pages' Step 2) for B requests, K drafts each.
+ *
+ *  last_token    [B] int32     last accepted token of each request (row 0 input)
+ *  target_hidden [B, 3H]       config dtype; [h_lo | h_mid | h_hi] of that token
+ *  positions     [B] int32     Q_b: RoPE position of row 0; row j uses Q_b + j
+ *  seq_lens      [B] int32     S_b: committed drafter-cache entries; row j is
+ *                              written to and attends through entry S_b + j
+ *  page_table    [B, max_pages] int32  physical page of each 16-entry block
+ *  num_pages     pages in each layer of the caches
+ *  k_cache, v_cache  [4][num_pages][nkv][16][hd] config dtype; read for
+ *                entries < S_b, written at entries S_b..S_b+K-1
+ *  drafts        [B, K] int32  OUT: argmax of the LM head per row
+ *  logits_dbg    [B, K, V] fp32 OUT or NULL: full logits (testing only)
+ *  status        [B] int32     OUT: PE_REQ_*; a request that is not OK gets
+ *                drafts -1 and no cache writes
+ * Requires 1 <= B <= max_batch, 1 <= K <= k_max, target_hidden 16-byte aligned. */
+int pe_draft(pe_handle* h, int32_t B, int32_t K,
+             const int32_t* last_token, const void* target_hidden,
+             const int32_t* positions, const int32_t* seq_lens,
+             const int32_t* page_table, int32_t max_pages, int32_t num_pages,
+             void* k_cache, void* v_cache,
+             int32_t* drafts, float* logits_dbg, int32_t* status, void* stream);
+
+/* Greedy verification + batch-metadata rebuild + KV rollback (one kernel).
+ * h may be NULL (the kernel needs no drafter state).
+ *
+ *  drafts        [B, K] int32     the step's drafts d
+ *  target_tokens [B, K+1] int32   target argmax tokens g for the K+1 positions
+ *  page_table    [B, max_pages] int32, num_pages as for pe_draft
+ *  positions, seq_lens  [B] int32 in: Q_b, S_b of the step just drafted
+ *  positions_out, seq_lens_out [B] int32 OUT (may alias the inputs):
+ *                 Q_b' = Q_b + a_b + 1, S_b' = S_b + min(a_b, K-1) + 1
+ *  accepted      [B] int32 OUT  a_b = longest prefix with d == g, 0..K
+ *  bonus         [B] int32 OUT  g[b, a_b]
+ *  emitted       [B, K+1] int32 OUT or NULL: d[b, :a_b], bonus, then -1
+ *  slot_mapping  [B, K] int32 OUT  physical slot (page*16 + offset) of entries
+ *                 S_b' .. S_b'+K-1 (where the next draft pass writes)
+ *  rollback_slots [B, K] int32 OUT  slots of rejected entries S_b' .. S_b+K-1,
+ *                 then -1 padding
+ *  status        [B] int32 OUT  PE_REQ_*; when not OK, positions/seq_lens are
+ *                 passed through unchanged and slot/rollback rows are -1.
+ * Requires 1 <= K <= 31. */
+int pe_verify_rebuild(pe_handle* h, int32_t B, int32_t K,
+                      const int32_t* drafts, const int32_t* target_tokens,
+                      const int32_t* page_table, int32_t max_pages, int32_t num_pages,
+                      const int32_t* positions, const int32_t* seq_lens,
+                      int32_t* positions_out, int32_t* seq_lens_out,
+                      int32_t* accepted, int32_t* bonus, int32_t* emitted,
+                      int32_t* slot_mapping, int32_t* rollback_slots,
+                      int32_t* status, void* stream);
+
+/* The draft pass's tcgen05 GEMM engine on its own (plain store epilogue):
+ *   y[n, m] = sum_k w[m, k] * x[n, k]
+ *  w  [M, Kd] config-dtype weights, x [N, Kd] activations (same dtype),
+ *  y  [N, M] fp32 OUT. w and x 16-byte aligned, Kd a multiple of 8.
+ *  ws       fp32 split-K scratch of at least *ws_floats elements (may be NULL
+ *           when *ws_floats is 0), tickets int32 [*n_tickets] that must be
+ *           zero before the first call; the kernel leaves them zero again.
+ * pe_linear_scratch reports the sizes for a shape on the current device. */
+int pe_linear_scratch(int32_t dtype, int32_t M, int32_t N, int32_t Kd, int64_t* ws_floats, int32_t* n_tickets);
+int pe_linear(int32_t dtype, int32_t M, int32_t N, int32_t Kd, const void* w, const void* x, float* y,
+              float* ws, int32_t* tickets, void* stream);
+
+/* Synchronise `stream` and return (then clear) the device error word of h
+ * (PE_DEVERR_* bits; 0 = no device-side wait gave up). */
+int pe_device_errors(pe_handle* h, void* stream, uint32_t* out_bits);
+
+/* Number of kernels the last pe_draft call enqueued (for launch accounting). */
+int pe_last_launch_count(const pe_handle* h);
+
+void pe_destroy(pe_handle* h);
+
+/* Thread-local description of the last error (never NULL). */
+const char* pe_last_error(void);
+
+int pe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PE_H */

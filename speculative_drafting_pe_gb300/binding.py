@@ -1,0 +1,244 @@
+"""Thin ctypes binding of libpe.so (C ABI in include/pe.h).
+
+Argument marshalling only: every step of the draft pass and of the
+verify/rebuild runs in the library's CUDA kernels. PyTorch supplies device
+memory and the current stream. ``load()`` raises if the library is missing;
+there is no fallback path.
+"""
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+PE_OK = 0
+PE_REQ_OK, PE_REQ_CAPACITY, PE_REQ_BAD_PAGE, PE_REQ_BAD_INPUT = 0, 1, 2, 3
+PE_DTYPE_BF16, PE_DTYPE_FP32 = 0, 1
+
+EXPORTS = (
+    "pe_init_drafter", "pe_draft", "pe_verify_rebuild", "pe_device_errors",
+    "pe_last_launch_count", "pe_destroy", "pe_last_error", "pe_abi_version", "pe_linear_scratch", "pe_linear",
+)
+
+_i32 = ctypes.c_int32
+_vp = ctypes.c_void_p
+
+
+class PeConfig(ctypes.Structure):
+    _fields_ = [("hidden", _i32), ("n_layers", _i32), ("n_q_heads", _i32), ("n_kv_heads", _i32),
+                ("head_dim", _i32), ("ffn", _i32), ("vocab", _i32), ("rms_eps", ctypes.c_float),
+                ("rope_theta", ctypes.c_float), ("page_size", _i32), ("k_max", _i32), ("dtype", _i32)]
+
+
+_LAYER_FIELDS = ("norm_e", "norm_h", "attn_norm", "w_qkv", "w_o", "mlp_norm", "w_gate", "w_up", "w_down")
+
+
+class PeLayerWeights(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in _LAYER_FIELDS]
+
+
+_TOP_FIELDS = ("fc", "embed", "emb_mask", "h_shared", "final_norm", "lm_head")
+
+
+class PeWeights(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in _TOP_FIELDS] + [("layer", PeLayerWeights * 4)]
+
+
+class PeError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"libpe error {code}: {msg}")
+        self.code = code
+
+
+_LIB = None
+
+
+def library_path():
+    return _build.LIB
+
+
+def load():
+    """Load libpe.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libpe.so not found at {path}; build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    lib.pe_abi_version.restype = ctypes.c_int
+    lib.pe_last_error.restype = ctypes.c_char_p
+    lib.pe_init_drafter.argtypes = [ctypes.POINTER(PeConfig), ctypes.POINTER(PeWeights), _i32, _i32,
+                                    ctypes.POINTER(_vp)]
+    lib.pe_init_drafter.restype = ctypes.c_int
+    lib.pe_draft.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.pe_draft.restype = ctypes.c_int
+    lib.pe_verify_rebuild.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
+                                      _vp, _vp, _vp, _vp, _vp]
+    lib.pe_verify_rebuild.restype = ctypes.c_int
+    lib.pe_device_errors.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.pe_device_errors.restype = ctypes.c_int
+    lib.pe_last_launch_count.argtypes = [_vp]
+    lib.pe_last_launch_count.restype = ctypes.c_int
+    lib.pe_destroy.argtypes = [_vp]
+    lib.pe_destroy.restype = None
+    lib.pe_linear_scratch.argtypes = [_i32, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(_i32)]
+    lib.pe_linear_scratch.restype = ctypes.c_int
+    lib.pe_linear.argtypes = [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.pe_linear.restype = ctypes.c_int
+    _LIB = lib
+    return lib
+
+
+def _check(rc):
+    if rc != PE_OK:
+        raise PeError(rc, _LIB.pe_last_error().decode())
+
+
+def _p(t):
+    return None if t is None else _vp(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return _vp(s.cuda_stream)
+
+
+def _need(t, dtype, device, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+class Drafter:
+    """A drafter handle over caller-owned device weights.
+
+    shape: object with hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab,
+    rms_eps, rope_theta, page_size, dtype ("bf16" | "fp32").
+    weights: dict as produced by ``synth.make_weights`` with tensors on the
+    device; the Drafter keeps references so they outlive the handle.
+    """
+
+    def __init__(self, shape, weights, max_batch, k_max, device=None):
+        lib = load()
+        self.shape = shape
+        self.dtype = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        self.k_max = k_max
+        self.max_batch = max_batch
+        self._weights = weights
+        cfg = PeConfig(shape.hidden, 4, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn,
+                       shape.vocab, shape.rms_eps, shape.rope_theta, shape.page_size, k_max,
+                       PE_DTYPE_BF16 if shape.dtype == "bf16" else PE_DTYPE_FP32)
+        w = PeWeights()
+        for n in _TOP_FIELDS:
+            t = weights[n]
+            _need(t, self.dtype, self.device, n)
+            setattr(w, n, t.data_ptr())
+        for li, L in enumerate(weights["layers"]):
+            for n in _LAYER_FIELDS:
+                t = L.get(n)
+                if t is not None:
+                    _need(t, self.dtype, self.device, f"layers[{li}].{n}")
+                    setattr(w.layer[li], n, t.data_ptr())
+        self._cfg, self._w = cfg, w
+        h = _vp()
+        _check(lib.pe_init_drafter(ctypes.byref(cfg), ctypes.byref(w), max_batch, self.device.index or 0,
+                                   ctypes.byref(h)))
+        self._h = h
+
+    def draft(self, last_token, target_hidden, positions, seq_lens, page_table, num_pages, k_cache, v_cache,
+              K, drafts=None, status=None, logits=None, stream=None):
+        """Enqueue one draft pass; returns (drafts [B, K] int32, status [B] int32)."""
+        B = last_token.shape[0]
+        dev = self.device
+        for name, t in (("last_token", last_token), ("positions", positions), ("seq_lens", seq_lens),
+                        ("page_table", page_table)):
+            _need(t, torch.int32, dev, name)
+        _need(target_hidden, self.dtype, dev, "target_hidden")
+        _need(k_cache, self.dtype, dev, "k_cache")
+        _need(v_cache, self.dtype, dev, "v_cache")
+        if drafts is None:
+            drafts = torch.empty(B, K, dtype=torch.int32, device=dev)
+        if status is None:
+            status = torch.empty(B, dtype=torch.int32, device=dev)
+        if logits is not None:
+            _need(logits, torch.float32, dev, "logits")
+        _check(load().pe_draft(self._h, B, K, _p(last_token), _p(target_hidden), _p(positions), _p(seq_lens),
+                               _p(page_table), page_table.shape[1], num_pages, _p(k_cache), _p(v_cache),
+                               _p(drafts), _p(logits), _p(status), _stream_ptr(stream)))
+        return drafts, status
+
+    def launch_count(self):
+        return load().pe_last_launch_count(self._h)
+
+    def device_errors(self, stream=None):
+        bits = ctypes.c_uint32(0)
+        _check(load().pe_device_errors(self._h, _stream_ptr(stream), ctypes.byref(bits)))
+        return bits.value
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            load().pe_destroy(self._h)
+            self._h = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def linear(w, x, stream=None):
+    """y = x @ w.T in fp32 on the tcgen05 GEMM engine (bf16 or fp32/tf32 inputs)."""
+    lib = load()
+    M, Kd = w.shape
+    N = x.shape[0]
+    dtype = PE_DTYPE_BF16 if w.dtype == torch.bfloat16 else PE_DTYPE_FP32
+    _need(x, w.dtype, w.device, "x")
+    _need(w, w.dtype, w.device, "w")
+    wsf, nt = ctypes.c_int64(0), _i32(0)
+    _check(lib.pe_linear_scratch(dtype, M, N, Kd, ctypes.byref(wsf), ctypes.byref(nt)))
+    ws = torch.empty(max(wsf.value, 1), dtype=torch.float32, device=w.device)
+    tickets = torch.zeros(max(nt.value, 1), dtype=torch.int32, device=w.device)
+    y = torch.empty(N, M, dtype=torch.float32, device=w.device)
+    _check(lib.pe_linear(dtype, M, N, Kd, _p(w), _p(x), _p(y), _p(ws), _p(tickets), _stream_ptr(stream)))
+    return y
+
+
+def verify_rebuild(drafts, target_tokens, page_table, num_pages, positions, seq_lens, positions_out=None,
+                   seq_lens_out=None, emitted=True, stream=None, out=None):
+    """Greedy verify + metadata rebuild + rollback on the device.
+
+    Returns a dict of int32 device tensors: accepted, bonus, emitted (or None),
+    slot_mapping, rollback_slots, status, positions, seq_lens.
+    """
+    lib = load()
+    B, K = drafts.shape
+    dev = drafts.device
+    for name, t in (("drafts", drafts), ("target_tokens", target_tokens), ("page_table", page_table),
+                    ("positions", positions), ("seq_lens", seq_lens)):
+        _need(t, torch.int32, dev, name)
+    o = out if out is not None else {}
+
+    def buf(name, *size):
+        if name not in o or o[name] is None:
+            o[name] = torch.empty(*size, dtype=torch.int32, device=dev)
+        return o[name]
+
+    pos_o = positions_out if positions_out is not None else buf("positions", B)
+    sl_o = seq_lens_out if seq_lens_out is not None else buf("seq_lens", B)
+    o["positions"], o["seq_lens"] = pos_o, sl_o
+    em = buf("emitted", B, K + 1) if emitted else None
+    _check(lib.pe_verify_rebuild(None, B, K, _p(drafts), _p(target_tokens), _p(page_table), page_table.shape[1],
+                                 num_pages, _p(positions), _p(seq_lens), _p(pos_o), _p(sl_o),
+                                 _p(buf("accepted", B)), _p(buf("bonus", B)), _p(em),
+                                 _p(buf("slot_mapping", B, K)), _p(buf("rollback_slots", B, K)),
+                                 _p(buf("status", B)), _stream_ptr(stream)))
+    o["emitted"] = em
+    return o

@@ -1,0 +1,412 @@
+// tcgen05 weight-streaming GEMM with fused epilogues.
+//
+// D[m, n] = sum_k W[m, k] * X[n, k] with the weight rows on the 128-row M
+// side of the MMA and the B*K token rows on the N side (16..256 per tile), so
+// that at small batch the kernel streams each weight byte from HBM once.
+//
+// Roles (192 threads, one work unit per CTA):
+//   warp 0      TMA producer: weight tile [128 x 128 B] + token tile
+//               [bn x 128 B] per stage, 128-byte swizzle, into a smem ring.
+//   warp 1      TMEM allocation; lane 0 issues tcgen05.mma (M=128, N=bn)
+//               into an fp32 TMEM accumulator and commits stages back.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane per
+//               thread), optional split-K reduction, fused epilogue.
+//
+// Split-K: every split writes its fp32 partial tile to scratch; the last
+// split to arrive at the tile's ticket sums the partials in split order
+// (0, 1, ..., S-1), so the result does not depend on arrival order, then
+// applies the epilogue and resets the ticket for the next launch.
+#include "common.cuh"
+#include "internal.h"
+
+namespace pe {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;
+constexpr int kRowBytes = 128;               // one 128-byte swizzle row per tile row
+constexpr int kABytes = kBM * kRowBytes;     // 16 KB weight tile per stage
+constexpr int kChunk = 16;                   // accumulator columns per tcgen05.ld
+constexpr int kPitch = kBM + 4;              // epilogue staging row pitch (floats)
+
+__host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn) {
+    size_t off = static_cast<size_t>(stages) * (kABytes + static_cast<size_t>(bn) * kRowBytes);
+    off += static_cast<size_t>(2 * stages + 1) * 8;   // mbarriers
+    off += 16;                                        // TMEM base + flags
+    off = (off + 15) & ~static_cast<size_t>(15);
+    off += static_cast<size_t>(kChunk) * kPitch * 4;  // epilogue staging tile
+    return off + 1024;                                // base alignment slack
+}
+
+__host__ __device__ inline uint32_t tmem_cols_for(int bn) {
+    return bn <= 32 ? 32u : (bn <= 64 ? 64u : (bn <= 128 ? 128u : 256u));
+}
+
+// ------------------------------------------------------------ epilogues
+
+template <typename T, int EPI>
+__device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v)[kChunk], int ml, int m_tile,
+                                            int n0, float* stile) {
+    if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
+        const int m = m_tile * kBM + ml;
+        if (m < p.M) {
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                const int n = n0 + i;
+                if (n < p.N) {
+                    float* dst = p.out_f32 + static_cast<size_t>(n) * p.ld_out + m;
+                    if constexpr (EPI == EPI_RESID) *dst += v[i];
+                    else *dst = v[i];
+                }
+            }
+        }
+    } else if constexpr (EPI == EPI_ARGMAX) {
+        const int m = m_tile * kBM + ml;
+        const bool valid = m < p.M;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const int n = n0 + i;
+            if (p.logits != nullptr && valid && n < p.N) p.logits[static_cast<size_t>(n) * p.ld_logits + m] = v[i];
+            unsigned long long key = valid ? argmax_key(v[i], static_cast<uint32_t>(m)) : 0ull;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
+                key = o > key ? o : key;
+            }
+            if ((ml & 31) == 0 && n < p.N && key != 0ull) atomicMax(p.amax + n, key);
+        }
+    } else if constexpr (EPI == EPI_SWIGLU) {
+        // rows 0..63 of the tile are gate rows, 64..127 the matching up rows
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) stile[i * kPitch + ml] = v[i];
+        named_bar_sync(1, 128);
+        const int fl = ml & 63;
+        const int f = m_tile * 64 + fl;
+        const int ibeg = (ml >> 6) * (kChunk / 2);
+        if (f < p.M) {
+            T* out = static_cast<T*>(p.out_act);
+#pragma unroll
+            for (int i = ibeg; i < ibeg + kChunk / 2; ++i) {
+                const int n = n0 + i;
+                if (n < p.N) {
+                    const float g = stile[i * kPitch + fl];
+                    const float u = stile[i * kPitch + fl + 64];
+                    out[static_cast<size_t>(n) * p.ld_act + f] = Elem<T>::from_f(silu_f(g) * u);
+                }
+            }
+        }
+    } else if constexpr (EPI == EPI_QKV) {
+        // A 128-row tile holds whole heads of exactly one of q, k, v.
+        const int m0 = m_tile * kBM;
+        const int m = m0 + ml;
+        const int hd = p.hd;
+        const int half = hd >> 1;
+        const int region = m0 < p.nq_hd ? 0 : (m0 < p.nq_hd + p.nkv * hd ? 1 : 2);
+        float outv[kChunk];
+        if (region < 2) {
+            named_bar_sync(1, 128);
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) stile[i * kPitch + ml] = v[i];
+            named_bar_sync(1, 128);
+            const int d = ml % hd;
+            const bool lo = d < half;
+            const int partner = lo ? ml + half : ml - half;
+            const int fi = lo ? d : d - half;
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                const int n = n0 + i;
+                outv[i] = 0.f;
+                if (n < p.N) {
+                    const float2 cs = p.rope_cs[static_cast<size_t>(n) * half + fi];
+                    const float y = stile[i * kPitch + partner];
+                    outv[i] = lo ? (v[i] * cs.x - y * cs.y) : (v[i] * cs.x + y * cs.y);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) outv[i] = v[i];
+        }
+        if (m < p.M) {
+            if (region == 0) {
+                T* q = static_cast<T*>(p.out_act);
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i) {
+                    const int n = n0 + i;
+                    if (n < p.N) q[static_cast<size_t>(n) * p.ld_act + m] = Elem<T>::from_f(outv[i]);
+                }
+            } else {
+                const int r = m - p.nq_hd - (region == 2 ? p.nkv * hd : 0);
+                const int kvh = r / hd;
+                const int d = r - kvh * hd;
+                T* cache = static_cast<T*>(region == 1 ? p.k_cache : p.v_cache);
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i) {
+                    const int n = n0 + i;
+                    if (n < p.N) {
+                        const int slot = p.row_slot[n];
+                        if (slot >= 0) {
+                            const size_t page = static_cast<size_t>(slot >> 4);
+                            const int off = slot & 15;
+                            cache[((page * p.nkv + kvh) * 16 + off) * hd + d] = Elem<T>::from_f(outv[i]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <typename T, int EPI>
+__device__ __forceinline__ void epilogue(const GemmParams& p, uint32_t tmem_acc, uint64_t* tfull, float* stile,
+                                         int* sflag, int m_tile, int n_tile, int split, int warp, int lane) {
+    const int quad = warp & 3;               // TMEM lane quadrant this warp may read
+    const int ml = quad * 32 + lane;         // tile row = TMEM lane
+    const uint32_t t_row = tmem_acc + (static_cast<uint32_t>(quad * 32) << 16);
+    const bool ok = mbar_wait(tfull, 0, p.err, PE_DEVERR_GEMM_TIMEOUT);
+    tc_fence_after_sync();
+    if (!ok) sflag[0] = 1;
+    named_bar_sync(1, 128);
+    if (sflag[0]) return;
+
+    const int bn = p.bn;
+    const int n_base = n_tile * bn;
+    if (p.splits > 1) {
+        const int tile = m_tile * p.n_tiles + n_tile;
+        float* mine = p.ws + (static_cast<size_t>(tile) * p.splits + split) * bn * kBM;
+        for (int c0 = 0; c0 < bn; c0 += kChunk) {
+            float v[kChunk];
+            tmem_ld16(t_row + c0, v);
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) __stcg(mine + static_cast<size_t>(c0 + i) * kBM + ml, v[i]);
+        }
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (ml == 0) {
+            const int old = atomicAdd(p.tickets + tile, 1);
+            const int last = (old == p.splits - 1) ? 1 : 0;
+            if (last) atomicExch(p.tickets + tile, 0);
+            sflag[1] = last;
+        }
+        named_bar_sync(1, 128);
+        if (!sflag[1]) return;
+        __threadfence();
+        const float* base = p.ws + static_cast<size_t>(tile) * p.splits * bn * kBM;
+        for (int c0 = 0; c0 < bn; c0 += kChunk) {
+            float v[kChunk];
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) v[i] = 0.f;
+            for (int s = 0; s < p.splits; ++s) {
+                const float* src = base + (static_cast<size_t>(s) * bn + c0) * kBM + ml;
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i) v[i] += __ldcg(src + static_cast<size_t>(i) * kBM);
+            }
+            apply_chunk<T, EPI>(p, v, ml, m_tile, n_base + c0, stile);
+        }
+    } else {
+        for (int c0 = 0; c0 < bn; c0 += kChunk) {
+            float v[kChunk];
+            tmem_ld16(t_row + c0, v);
+            apply_chunk<T, EPI>(p, v, ml, m_tile, n_base + c0, stile);
+        }
+    }
+}
+
+// ------------------------------------------------------------ kernel
+
+template <typename T, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+           const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int stages = p.stages;
+    const int bn = p.bn;
+    const uint32_t b_bytes = static_cast<uint32_t>(bn) * kRowBytes;
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + static_cast<size_t>(stages) * kABytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + static_cast<size_t>(stages) * b_bytes);
+    uint64_t* empty = full + stages;
+    uint64_t* tfull = empty + stages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+    int* sflag = reinterpret_cast<int*>(tmem_slot + 1);
+    float* stile = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(sflag + 3) + 15) & ~uintptr_t(15));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int unit = blockIdx.x;
+    const int n_tile = unit % p.n_tiles;
+    const int rest = unit / p.n_tiles;
+    const int split = rest % p.splits;
+    const int m_tile = rest / p.splits;
+    const int kb0 = split * p.kb_per_split;
+    const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+    const uint32_t tmem_cols = tmem_cols_for(bn);
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        if constexpr (EPI == EPI_SWIGLU) tma_prefetch_desc(&tmA2);
+        tma_prefetch_desc(&tmB);
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tfull, 1);
+        sflag[0] = 0;
+        sflag[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_acc = *tmem_slot;
+
+    pdl_launch_dependents();
+    pdl_wait();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_x = l2_policy_evict_last();
+            constexpr int kBK = kRowBytes / static_cast<int>(sizeof(T));
+            int s = 0;
+            uint32_t ph = 0;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait(&empty[s], ph ^ 1u, p.err, PE_DEVERR_GEMM_TIMEOUT)) break;
+                mbar_arrive_expect_tx(&full[s], kABytes + b_bytes);
+                const int kx = kb * kBK;
+                uint8_t* a_dst = sA + static_cast<size_t>(s) * kABytes;
+                if constexpr (EPI == EPI_SWIGLU) {
+                    tma_load_2d(a_dst, &tmA, &full[s], kx, m_tile * 64, pol_w);
+                    tma_load_2d(a_dst + kABytes / 2, &tmA2, &full[s], kx, m_tile * 64, pol_w);
+                } else {
+                    tma_load_2d(a_dst, &tmA, &full[s], kx, m_tile * kBM, pol_w);
+                }
+                tma_load_2d(sB + static_cast<size_t>(s) * b_bytes, &tmB, &full[s], kx, n_tile * bn, pol_x);
+                if (++s == stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = umma_idesc(UmmaKind<T>::kFmt, kBM, bn);
+            int s = 0;
+            uint32_t ph = 0;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait(&full[s], ph, p.err, PE_DEVERR_GEMM_TIMEOUT)) break;
+                tc_fence_after_sync();
+                const uint32_t a_addr = smem_u32(sA + static_cast<size_t>(s) * kABytes);
+                const uint32_t b_addr = smem_u32(sB + static_cast<size_t>(s) * b_bytes);
+#pragma unroll
+                for (int kk = 0; kk < kRowBytes / 32; ++kk) {
+                    UmmaKind<T>::mma(tmem_acc, umma_desc_sw128(a_addr + kk * 32), umma_desc_sw128(b_addr + kk * 32),
+                                     idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(&empty[s]);
+                if (++s == stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            umma_commit(tfull);
+        }
+        __syncwarp();
+    } else {
+        epilogue<T, EPI>(p, tmem_acc, tfull, stile, sflag, m_tile, n_tile, split, warp, lane);
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x == 0 && p.err != nullptr && (*reinterpret_cast<volatile unsigned*>(p.err) & PE_DEVERR_GEMM_TIMEOUT)) {
+        // A wait gave up: let any bulk copy still in flight land before this
+        // CTA's shared memory is released.
+        __nanosleep(100000);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_acc, tmem_cols);
+    }
+}
+
+template <typename T, int EPI>
+int launch_typed(const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B, const GemmPlan& plan,
+                 const GemmParams& p, cudaStream_t stream, bool pdl) {
+    auto kern = k_gemm<T, EPI>;
+    PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(plan.smem_bytes)));
+    PE_CUDA_TRY(launch_ex(kern, dim3(plan.units), dim3(kThreads), plan.smem_bytes, stream, pdl, A, A2, B, p));
+    return PE_OK;
+}
+
+template <typename T>
+int launch_dispatch(int epi, const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B,
+                    const GemmPlan& plan, const GemmParams& p, cudaStream_t stream, bool pdl) {
+    switch (epi) {
+        case EPI_STORE: return launch_typed<T, EPI_STORE>(A, A2, B, plan, p, stream, pdl);
+        case EPI_QKV: return launch_typed<T, EPI_QKV>(A, A2, B, plan, p, stream, pdl);
+        case EPI_RESID: return launch_typed<T, EPI_RESID>(A, A2, B, plan, p, stream, pdl);
+        case EPI_SWIGLU: return launch_typed<T, EPI_SWIGLU>(A, A2, B, plan, p, stream, pdl);
+        case EPI_ARGMAX: return launch_typed<T, EPI_ARGMAX>(A, A2, B, plan, p, stream, pdl);
+        default: set_error("unknown GEMM epilogue"); return PE_ERR_ARG;
+    }
+}
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+inline int round_up(int a, int b) { return ceil_div(a, b) * b; }
+
+}  // namespace
+
+GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms) {
+    GemmPlan g{};
+    const int bk = kRowBytes / elem_bytes;
+    g.kb_total = ceil_div(Kd, bk);
+    if (N <= 256) {
+        g.n_tiles = 1;
+        g.bn = round_up(N < 1 ? 1 : N, 16);
+    } else {
+        g.n_tiles = ceil_div(N, 256);
+        g.bn = round_up(ceil_div(N, g.n_tiles), 16);
+    }
+    const int rows_per_tile = epi == EPI_SWIGLU ? 64 : kBM;
+    g.m_tiles = ceil_div(M, rows_per_tile);
+    g.tiles = g.m_tiles * g.n_tiles;
+    int splits = 1;
+    const int target = 2 * num_sms;
+    if (g.tiles < target && epi != EPI_ARGMAX) {
+        splits = ceil_div(target, g.tiles);
+        const int cap = g.kb_total / 4 > 1 ? g.kb_total / 4 : 1;   // >= 4 k-blocks per split
+        splits = splits < cap ? splits : cap;
+    }
+    g.kb_per_split = ceil_div(g.kb_total, splits);
+    g.splits = ceil_div(g.kb_total, g.kb_per_split);
+    g.units = g.tiles * g.splits;
+    const size_t stage = kABytes + static_cast<size_t>(g.bn) * kRowBytes;
+    const size_t budget = g.bn <= 64 ? 100 * 1024 : 190 * 1024;
+    int st = static_cast<int>(budget / stage);
+    g.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
+    g.smem_bytes = gemm_smem_bytes(g.stages, g.bn);
+    g.ws_floats = g.splits > 1 ? static_cast<size_t>(g.tiles) * g.splits * g.bn * kBM : 0;
+    return g;
+}
+
+int launch_gemm(int dtype, int epi, const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B,
+                const GemmPlan& plan, GemmParams p, cudaStream_t stream, bool pdl) {
+    p.m_tiles = plan.m_tiles;
+    p.n_tiles = plan.n_tiles;
+    p.splits = plan.splits;
+    p.kb_total = plan.kb_total;
+    p.kb_per_split = plan.kb_per_split;
+    p.bn = plan.bn;
+    p.stages = plan.stages;
+    if (dtype == PE_DTYPE_BF16) return launch_dispatch<__nv_bfloat16>(epi, A, A2, B, plan, p, stream, pdl);
+    return launch_dispatch<float>(epi, A, A2, B, plan, p, stream, pdl);
+}
+
+}  // namespace pe

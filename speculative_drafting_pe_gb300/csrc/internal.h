@@ -1,0 +1,158 @@
+// Internal declarations shared by the libpe.so translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <utility>
+
+#include "pe.h"
+
+namespace pe {
+
+// ---------------------------------------------------------------- errors
+
+void set_error(const std::string& msg);
+#define PE_CUDA_TRY(expr)                                                                   \
+    do {                                                                                    \
+        cudaError_t e_ = (expr);                                                            \
+        if (e_ != cudaSuccess) {                                                            \
+            ::pe::set_error(std::string(#expr) + ": " + cudaGetErrorString(e_));            \
+            return PE_ERR_CUDA;                                                             \
+        }                                                                                   \
+    } while (0)
+
+int encode_tmap_2d(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t rows,
+                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
+
+// ---------------------------------------------------------------- GEMM
+
+enum Epi : int { EPI_STORE = 0, EPI_QKV = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_ARGMAX = 4 };
+
+// One tcgen05 GEMM  D[m, n] = sum_k W[m, k] * X[n, k]  (weights W fill the
+// 128-row M side, token rows X the N side), followed by a fused epilogue.
+struct GemmParams {
+    int M;              // output features (for SWIGLU: F, each tile = 64 gate + 64 up rows)
+    int N;              // token rows
+    int Kd;             // reduction length
+    int m_tiles, n_tiles, splits, kb_total, kb_per_split, bn, stages;
+    // STORE / RESID: fp32 [N, ld_out]
+    float* out_f32;
+    int ld_out;
+    // QKV: q out (T) [N, ld_act]; SWIGLU: act out (T) [N, ld_act]
+    void* out_act;
+    int ld_act;
+    // QKV extras
+    void* k_cache;      // this layer's [num_pages][nkv][16][hd]
+    void* v_cache;
+    int nq_hd, nkv, hd;
+    const int* row_slot;        // [N] physical cache slot of row n, -1 = skip
+    const float2* rope_cs;      // [N][hd/2] (cos, sin)
+    // ARGMAX
+    unsigned long long* amax;   // [N]
+    float* logits;              // [N, ld_logits] or null
+    int ld_logits;
+    // split-K scratch
+    float* ws;
+    int* tickets;
+    unsigned* err;
+};
+
+struct GemmPlan {
+    int bn, n_tiles, m_tiles, splits, kb_total, kb_per_split, stages;
+    int units;
+    size_t smem_bytes;
+    size_t ws_floats;   // split-K scratch needed (0 if splits == 1)
+    int tiles;          // tickets needed
+};
+
+GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms);
+int launch_gemm(int dtype, int epi, const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B,
+                const GemmPlan& plan, GemmParams p, cudaStream_t stream, bool pdl);
+
+// ---------------------------------------------------------------- small kernels
+
+struct RowBuildParams {
+    int B, K, H, V, hd, max_pages, num_pages, page_size;
+    const int32_t* last_token;
+    const int32_t* positions;
+    const int32_t* seq_lens;
+    const int32_t* page_table;
+    const float* h;            // [B, H] FC output
+    const void* embed;         // [V, H]
+    const void* emb_mask;      // [H]
+    const void* h_shared;      // [H]
+    const void* norm_e;        // [H]
+    const void* norm_h;        // [H]
+    float eps;
+    void* u;                   // OUT [R, 2H] T
+    float* resid;              // OUT [R, H]
+    int* row_slot;             // OUT [R]
+    float2* rope_cs;           // OUT [R, hd/2]
+    const double* inv_freq;    // [hd/2]
+    unsigned long long* amax;  // OUT [R] zeroed
+    int32_t* status;           // OUT [B]
+};
+int launch_row_build(int dtype, const RowBuildParams& p, cudaStream_t s, bool pdl);
+
+int launch_rmsnorm(int dtype, const float* x, const void* gain, void* out, int rows, int H, float eps,
+                   cudaStream_t s, bool pdl);
+
+int launch_argmax_finalize(const unsigned long long* amax, const int32_t* status, int B, int K, int32_t* drafts,
+                           cudaStream_t s, bool pdl);
+
+// ---------------------------------------------------------------- attention
+
+struct AttnParams {
+    int B, K, nq, nkv, hd, max_pages, num_pages, page_size;
+    int chunk;        // cache entries per split
+    int max_splits;   // grid.z
+    const void* q;            // [R, nq*hd] T (rotated)
+    const void* k_cache;      // this layer
+    const void* v_cache;
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    const int32_t* status;
+    void* out;                // [R, nq*hd] T
+    float* ws;                // split partials
+    int* tickets;             // [B*nkv]
+    unsigned* err;
+};
+struct AttnPlan {
+    int chunk, max_splits;
+    size_t ws_floats;
+    int tickets;
+};
+AttnPlan plan_attention(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms);
+int launch_attention(int dtype, const AttnParams& p, cudaStream_t s, bool pdl);
+
+// ---------------------------------------------------------------- verify
+
+int launch_verify_rebuild(int B, int K, const int32_t* drafts, const int32_t* target, const int32_t* page_table,
+                          int max_pages, int num_pages, int page_size, const int32_t* positions,
+                          const int32_t* seq_lens, int32_t* positions_out, int32_t* seq_lens_out,
+                          int32_t* accepted, int32_t* bonus, int32_t* emitted, int32_t* slot_mapping,
+                          int32_t* rollback, int32_t* status, cudaStream_t s);
+
+// Launch helper: every kernel goes through cudaLaunchKernelEx so that the
+// programmatic-dependent-launch attribute can be set uniformly.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                      Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace pe

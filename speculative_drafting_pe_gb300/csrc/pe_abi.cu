@@ -1,0 +1,520 @@
+// C ABI of libpe.so: drafter handle, workspaces, TMA descriptors and the
+// per-step orchestration of the draft pass (see include/pe.h).
+//
+// One draft pass enqueues, on the caller's stream:
+//   FC GEMM (3H -> H, rows = B)                          [a1]
+//   row build (rows, slots, RoPE table, status)          [a2]
+//   4 x { [RMSNorm] QKV GEMM + RoPE + paged KV write,    [a3]
+//         paged attention,                               [a4]
+//         O GEMM + residual,                             [a5]
+//         RMSNorm, gate/up GEMM + SwiGLU,                [a6]
+//         down GEMM + residual }
+//   final RMSNorm, LM-head GEMM + fused argmax,          [a7]
+//   argmax finalisation -> drafts.
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+struct pe_handle {
+    pe_config cfg;
+    pe_weights w;
+    int device = 0;
+    int max_batch = 0;
+    int max_rows = 0;
+    int num_sms = 0;
+    size_t elem = 2;
+    bool pdl = false;
+    // workspaces (device)
+    float* h = nullptr;           // [max_batch, H]
+    float* resid = nullptr;       // [max_rows, H]
+    void* u = nullptr;            // [max_rows, 2H]
+    void* xn = nullptr;           // [max_rows, H]
+    void* q = nullptr;            // [max_rows, nq*hd]
+    void* attn = nullptr;         // [max_rows, nq*hd]
+    void* act = nullptr;          // [max_rows, F]
+    unsigned long long* amax = nullptr;
+    int* row_slot = nullptr;
+    float2* rope_cs = nullptr;
+    double* inv_freq = nullptr;
+    float* gemm_ws = nullptr;
+    size_t gemm_ws_floats = 0;
+    int* gemm_tickets = nullptr;
+    int gemm_tickets_n = 0;
+    float* attn_ws = nullptr;
+    size_t attn_ws_floats = 0;
+    int* attn_tickets = nullptr;
+    int attn_tickets_n = 0;
+    unsigned* err = nullptr;
+    // weight tensor maps
+    CUtensorMap tm_fc, tm_lm;
+    CUtensorMap tm_qkv[4], tm_o[4], tm_gate[4], tm_up[4], tm_down[4];
+    int last_launches = 0;
+};
+
+namespace pe {
+
+static thread_local std::string g_last_error = "no error";
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (fn == nullptr) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+int encode_tmap_2d(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t rows,
+                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (fn == nullptr) {
+        set_error("cuTensorMapEncodeTiled entry point not available");
+        return PE_ERR_CUDA;
+    }
+    if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || (row_stride_bytes & 15u) != 0) {
+        set_error("TMA operand must be 16-byte aligned with a 16-byte multiple row stride");
+        return PE_ERR_ARG;
+    }
+    cuuint64_t dims[2] = {inner, rows < 1 ? 1 : rows};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt =
+        dtype == PE_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed with code " + std::to_string(static_cast<int>(r)));
+        return PE_ERR_CUDA;
+    }
+    return PE_OK;
+}
+
+}  // namespace pe
+
+using namespace pe;
+
+namespace {
+
+constexpr int kBoxBytes = 128;   // inner TMA box = one 128-byte swizzle row
+
+int box_inner(const pe_handle* h) { return kBoxBytes / static_cast<int>(h->elem); }
+
+// weight [rows, cols] row-major; box rows 128 (64 for gate/up halves)
+int weight_map(pe_handle* h, CUtensorMap* m, const void* w, int rows, int cols, int box_rows) {
+    return encode_tmap_2d(m, w, h->cfg.dtype, cols, rows, static_cast<uint64_t>(cols) * h->elem, box_inner(h),
+                          box_rows);
+}
+
+// activation [rows, cols]; box rows = bn of the GEMM consuming it
+int act_map(const pe_handle* h, CUtensorMap* m, const void* x, int rows, int cols, int bn) {
+    return encode_tmap_2d(m, x, h->cfg.dtype, cols, rows, static_cast<uint64_t>(cols) * h->elem,
+                          kBoxBytes / static_cast<int>(h->elem), bn);
+}
+
+void free_handle(pe_handle* h) {
+    if (h == nullptr) return;
+    void* ptrs[] = {h->h,    h->resid,    h->u,        h->xn,         h->q,       h->attn,         h->act,
+                    h->amax, h->row_slot, h->rope_cs, h->inv_freq, h->gemm_ws, h->gemm_tickets, h->attn_ws,
+                    h->attn_tickets, h->err};
+    for (void* p : ptrs)
+        if (p) cudaFree(p);
+    delete h;
+}
+
+int check_config(const pe_config& c) {
+    if (c.n_layers != 4) { set_error("n_layers must be 4"); return PE_ERR_UNSUPPORTED; }
+    if (c.page_size != 16) { set_error("page_size must be 16"); return PE_ERR_UNSUPPORTED; }
+    if (c.head_dim != 64 && c.head_dim != 128) { set_error("head_dim must be 64 or 128"); return PE_ERR_UNSUPPORTED; }
+    if (c.n_kv_heads <= 0 || c.n_q_heads % c.n_kv_heads != 0) {
+        set_error("n_kv_heads must divide n_q_heads");
+        return PE_ERR_UNSUPPORTED;
+    }
+    if ((c.n_q_heads * c.head_dim) % 128 != 0 || (c.n_kv_heads * c.head_dim) % 128 != 0) {
+        set_error("n_q_heads*head_dim and n_kv_heads*head_dim must be multiples of 128");
+        return PE_ERR_UNSUPPORTED;
+    }
+    if (c.hidden % 64 != 0 || c.ffn % 64 != 0 || c.hidden <= 0 || c.ffn <= 0) {
+        set_error("hidden and ffn must be positive multiples of 64");
+        return PE_ERR_UNSUPPORTED;
+    }
+    if (c.vocab <= 0) { set_error("vocab must be positive"); return PE_ERR_ARG; }
+    if (c.k_max < 1 || c.k_max > 16) { set_error("k_max must be in 1..16"); return PE_ERR_UNSUPPORTED; }
+    if (c.k_max * (c.n_q_heads / c.n_kv_heads) > 128) {
+        set_error("k_max * (n_q_heads / n_kv_heads) must be <= 128");
+        return PE_ERR_UNSUPPORTED;
+    }
+    if (c.dtype != PE_DTYPE_BF16 && c.dtype != PE_DTYPE_FP32) { set_error("unknown dtype"); return PE_ERR_ARG; }
+    if (!(c.rms_eps > 0.f) || !(c.rope_theta > 0.f)) { set_error("rms_eps and rope_theta must be > 0"); return PE_ERR_ARG; }
+    return PE_OK;
+}
+
+template <typename P>
+int dev_alloc(P** p, size_t bytes) {
+    if (bytes == 0) bytes = 16;
+    if (cudaMalloc(reinterpret_cast<void**>(p), bytes) != cudaSuccess) {
+        set_error("cudaMalloc of " + std::to_string(bytes) + " bytes failed");
+        return PE_ERR_NOMEM;
+    }
+    return PE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pe_abi_version(void) { return PE_ABI_VERSION; }
+
+const char* pe_last_error(void) { return g_last_error.c_str(); }
+
+int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max_batch, int32_t device,
+                    pe_handle** out) {
+    if (cfg == nullptr || weights == nullptr || out == nullptr) { set_error("null argument"); return PE_ERR_ARG; }
+    *out = nullptr;
+    int rc = check_config(*cfg);
+    if (rc != PE_OK) return rc;
+    if (max_batch < 1) { set_error("max_batch must be >= 1"); return PE_ERR_ARG; }
+    const pe_weights& w = *weights;
+    const void* req[] = {w.fc, w.embed, w.emb_mask, w.h_shared, w.final_norm, w.lm_head};
+    for (const void* p : req)
+        if (p == nullptr) { set_error("null weight pointer"); return PE_ERR_ARG; }
+    for (int l = 0; l < 4; ++l) {
+        const pe_layer_weights& L = w.layer[l];
+        const void* lp[] = {L.w_qkv, L.w_o, L.mlp_norm, L.w_gate, L.w_up, L.w_down};
+        for (const void* p : lp)
+            if (p == nullptr) { set_error("null layer weight pointer"); return PE_ERR_ARG; }
+        if (l == 0 && (L.norm_e == nullptr || L.norm_h == nullptr)) { set_error("layer 0 needs norm_e and norm_h"); return PE_ERR_ARG; }
+        if (l > 0 && L.attn_norm == nullptr) { set_error("layers 1..3 need attn_norm"); return PE_ERR_ARG; }
+    }
+    PE_CUDA_TRY(cudaSetDevice(device));
+    int cc_major = 0, cc_minor = 0;
+    PE_CUDA_TRY(cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, device));
+    PE_CUDA_TRY(cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, device));
+    if (cc_major != 10 || cc_minor != 3) {
+        set_error("libpe.so is built for sm_103a; device compute capability is " + std::to_string(cc_major) + "." +
+                  std::to_string(cc_minor));
+        return PE_ERR_UNSUPPORTED;
+    }
+
+    pe_handle* h = new pe_handle();
+    h->cfg = *cfg;
+    h->w = w;
+    h->device = device;
+    h->max_batch = max_batch;
+    h->max_rows = max_batch * cfg->k_max;
+    h->elem = cfg->dtype == PE_DTYPE_BF16 ? 2 : 4;
+    const char* pdl_env = std::getenv("PE_PDL");
+    h->pdl = pdl_env != nullptr && pdl_env[0] == '1';
+    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        free_handle(h);
+        set_error("cudaDeviceGetAttribute failed");
+        return PE_ERR_CUDA;
+    }
+
+    const int H = cfg->hidden, F = cfg->ffn, V = cfg->vocab, hd = cfg->head_dim;
+    const int nq = cfg->n_q_heads, nkv = cfg->n_kv_heads;
+    const int qd = nq * hd, qkv_rows = (nq + 2 * nkv) * hd;
+    const size_t R = static_cast<size_t>(h->max_rows), E = h->elem;
+
+    // split-K scratch: the largest plan over every row count this handle accepts
+    size_t ws = 0;
+    int tiles = 1;
+    const int elem_bytes = static_cast<int>(E);
+    struct Shape { int M, Kd, epi; };
+    const Shape shapes[] = {{H, 3 * H, EPI_STORE}, {qkv_rows, 2 * H, EPI_QKV}, {qkv_rows, H, EPI_QKV},
+                            {H, qd, EPI_RESID},    {F, H, EPI_SWIGLU},        {H, F, EPI_RESID},
+                            {V, H, EPI_ARGMAX}};
+    for (const Shape& s : shapes) {
+        for (int n = 1; n <= h->max_rows; ++n) {
+            GemmPlan g = plan_gemm(s.M, n, s.Kd, s.epi, elem_bytes, h->num_sms);
+            ws = ws > g.ws_floats ? ws : g.ws_floats;
+            tiles = tiles > g.tiles ? tiles : g.tiles;
+        }
+    }
+    h->gemm_ws_floats = ws;
+    h->gemm_tickets_n = tiles;
+    // attention split scratch: bounded by ~2 CTAs per SM plus one partial split per pair
+    const int G = nq / nkv;
+    const size_t pairs_max = static_cast<size_t>(max_batch) * nkv;
+    h->attn_ws_floats = (2 * static_cast<size_t>(h->num_sms) + 2 * pairs_max) * (cfg->k_max * G) * (hd + 2);
+    h->attn_tickets_n = static_cast<int>(pairs_max);
+
+    int a = PE_OK;
+    if (a == PE_OK) a = dev_alloc(&h->h, static_cast<size_t>(max_batch) * H * 4);
+    if (a == PE_OK) a = dev_alloc(&h->resid, R * H * 4);
+    if (a == PE_OK) a = dev_alloc(&h->u, R * 2 * H * E);
+    if (a == PE_OK) a = dev_alloc(&h->xn, R * H * E);
+    if (a == PE_OK) a = dev_alloc(&h->q, R * qd * E);
+    if (a == PE_OK) a = dev_alloc(&h->attn, R * qd * E);
+    if (a == PE_OK) a = dev_alloc(&h->act, R * F * E);
+    if (a == PE_OK) a = dev_alloc(&h->amax, R * 8);
+    if (a == PE_OK) a = dev_alloc(&h->row_slot, R * 4);
+    if (a == PE_OK) a = dev_alloc(&h->rope_cs, R * (hd / 2) * sizeof(float2));
+    if (a == PE_OK) a = dev_alloc(&h->inv_freq, (hd / 2) * sizeof(double));
+    if (a == PE_OK) a = dev_alloc(&h->gemm_ws, h->gemm_ws_floats * 4);
+    if (a == PE_OK) a = dev_alloc(&h->gemm_tickets, static_cast<size_t>(h->gemm_tickets_n) * 4);
+    if (a == PE_OK) a = dev_alloc(&h->attn_ws, h->attn_ws_floats * 4);
+    if (a == PE_OK) a = dev_alloc(&h->attn_tickets, static_cast<size_t>(h->attn_tickets_n) * 4);
+    if (a == PE_OK) a = dev_alloc(&h->err, 16);
+    if (a != PE_OK) {
+        free_handle(h);
+        return a;
+    }
+    // zero what must start at zero: tickets, error word, and the activation
+    // buffers (TMA reads only rows < N, but keep them defined)
+    bool zok = cudaMemset(h->gemm_tickets, 0, static_cast<size_t>(h->gemm_tickets_n) * 4) == cudaSuccess &&
+               cudaMemset(h->attn_tickets, 0, static_cast<size_t>(h->attn_tickets_n) * 4) == cudaSuccess &&
+               cudaMemset(h->err, 0, 16) == cudaSuccess && cudaMemset(h->u, 0, R * 2 * H * E) == cudaSuccess &&
+               cudaMemset(h->xn, 0, R * H * E) == cudaSuccess && cudaMemset(h->attn, 0, R * qd * E) == cudaSuccess &&
+               cudaMemset(h->act, 0, R * F * E) == cudaSuccess;
+    std::vector<double> inv(hd / 2);
+    for (int i = 0; i < hd / 2; ++i) inv[i] = std::pow(static_cast<double>(cfg->rope_theta), -2.0 * i / hd);
+    zok = zok && cudaMemcpy(h->inv_freq, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice) == cudaSuccess;
+    zok = zok && cudaDeviceSynchronize() == cudaSuccess;
+    if (!zok) {
+        free_handle(h);
+        set_error("workspace initialisation failed");
+        return PE_ERR_CUDA;
+    }
+
+    rc = weight_map(h, &h->tm_fc, w.fc, H, 3 * H, 128);
+    if (rc == PE_OK) rc = weight_map(h, &h->tm_lm, w.lm_head, V, H, 128);
+    for (int l = 0; l < 4 && rc == PE_OK; ++l) {
+        const pe_layer_weights& L = w.layer[l];
+        rc = weight_map(h, &h->tm_qkv[l], L.w_qkv, qkv_rows, l == 0 ? 2 * H : H, 128);
+        if (rc == PE_OK) rc = weight_map(h, &h->tm_o[l], L.w_o, H, qd, 128);
+        if (rc == PE_OK) rc = weight_map(h, &h->tm_gate[l], L.w_gate, F, H, 64);
+        if (rc == PE_OK) rc = weight_map(h, &h->tm_up[l], L.w_up, F, H, 64);
+        if (rc == PE_OK) rc = weight_map(h, &h->tm_down[l], L.w_down, H, F, 128);
+    }
+    if (rc != PE_OK) {
+        free_handle(h);
+        return rc;
+    }
+    *out = h;
+    return PE_OK;
+}
+
+void pe_destroy(pe_handle* h) {
+    if (h == nullptr) return;
+    cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    free_handle(h);
+}
+
+int pe_last_launch_count(const pe_handle* h) { return h ? h->last_launches : 0; }
+
+int pe_device_errors(pe_handle* h, void* stream, uint32_t* out_bits) {
+    if (h == nullptr || out_bits == nullptr) { set_error("null argument"); return PE_ERR_ARG; }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned bits = 0;
+    PE_CUDA_TRY(cudaMemcpyAsync(&bits, h->err, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
+    PE_CUDA_TRY(cudaStreamSynchronize(s));
+    PE_CUDA_TRY(cudaMemsetAsync(h->err, 0, sizeof(unsigned), s));
+    PE_CUDA_TRY(cudaStreamSynchronize(s));
+    *out_bits = bits;
+    return PE_OK;
+}
+
+int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, const void* target_hidden,
+             const int32_t* positions, const int32_t* seq_lens, const int32_t* page_table, int32_t max_pages,
+             int32_t num_pages, void* k_cache, void* v_cache, int32_t* drafts, float* logits_dbg, int32_t* status,
+             void* stream) {
+    if (h == nullptr) { set_error("null handle"); return PE_ERR_ARG; }
+    if (B < 1 || B > h->max_batch) { set_error("B out of range 1..max_batch"); return PE_ERR_ARG; }
+    if (K < 1 || K > h->cfg.k_max) { set_error("K out of range 1..k_max"); return PE_ERR_ARG; }
+    if (!last_token || !target_hidden || !positions || !seq_lens || !page_table || !k_cache || !v_cache || !drafts ||
+        !status) {
+        set_error("null tensor argument");
+        return PE_ERR_ARG;
+    }
+    if (max_pages < 1 || num_pages < 1) { set_error("max_pages and num_pages must be >= 1"); return PE_ERR_ARG; }
+    const pe_config& c = h->cfg;
+    const int H = c.hidden, F = c.ffn, V = c.vocab, hd = c.head_dim, nq = c.n_q_heads, nkv = c.n_kv_heads;
+    const int qd = nq * hd, qkv_rows = (nq + 2 * nkv) * hd;
+    const int R = B * K;
+    const int eb = static_cast<int>(h->elem);
+    const int dt = c.dtype;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool pdl = h->pdl;
+    int launches = 0;
+    int rc;
+
+    // GEMM plans (bn depends only on the row count)
+    const GemmPlan p_fc = plan_gemm(H, B, 3 * H, EPI_STORE, eb, h->num_sms);
+    const GemmPlan p_qkv0 = plan_gemm(qkv_rows, R, 2 * H, EPI_QKV, eb, h->num_sms);
+    const GemmPlan p_qkv = plan_gemm(qkv_rows, R, H, EPI_QKV, eb, h->num_sms);
+    const GemmPlan p_o = plan_gemm(H, R, qd, EPI_RESID, eb, h->num_sms);
+    const GemmPlan p_gu = plan_gemm(F, R, H, EPI_SWIGLU, eb, h->num_sms);
+    const GemmPlan p_down = plan_gemm(H, R, F, EPI_RESID, eb, h->num_sms);
+    const GemmPlan p_lm = plan_gemm(V, R, H, EPI_ARGMAX, eb, h->num_sms);
+    const AttnPlan p_at = plan_attention(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms);
+    if (p_at.ws_floats > h->attn_ws_floats) { set_error("attention scratch too small for this max_pages"); return PE_ERR_ARG; }
+
+    CUtensorMap tm_th, tm_u, tm_xn, tm_attn, tm_act;
+    const int bn_rows = p_qkv.bn;   // all row-count-R GEMMs share bn
+    if ((rc = act_map(h, &tm_th, target_hidden, B, 3 * H, p_fc.bn)) != PE_OK) return rc;
+    if ((rc = act_map(h, &tm_u, h->u, R, 2 * H, bn_rows)) != PE_OK) return rc;
+    if ((rc = act_map(h, &tm_xn, h->xn, R, H, bn_rows)) != PE_OK) return rc;
+    if ((rc = act_map(h, &tm_attn, h->attn, R, qd, bn_rows)) != PE_OK) return rc;
+    if ((rc = act_map(h, &tm_act, h->act, R, F, bn_rows)) != PE_OK) return rc;
+
+    GemmParams base{};
+    base.N = R;
+    base.ws = h->gemm_ws;
+    base.tickets = h->gemm_tickets;
+    base.err = h->err;
+
+    // a1: h = W_fc [h_lo; h_mid; h_hi]
+    {
+        GemmParams p = base;
+        p.M = H; p.N = B; p.Kd = 3 * H;
+        p.out_f32 = h->h; p.ld_out = H;
+        if ((rc = launch_gemm(dt, EPI_STORE, h->tm_fc, h->tm_fc, tm_th, p_fc, p, s, pdl)) != PE_OK) return rc;
+        ++launches;
+    }
+    // a2: rows, slots, RoPE table, status, argmax reset
+    {
+        RowBuildParams rp{};
+        rp.B = B; rp.K = K; rp.H = H; rp.V = V; rp.hd = hd;
+        rp.max_pages = max_pages; rp.num_pages = num_pages; rp.page_size = c.page_size;
+        rp.last_token = last_token; rp.positions = positions; rp.seq_lens = seq_lens; rp.page_table = page_table;
+        rp.h = h->h; rp.embed = h->w.embed; rp.emb_mask = h->w.emb_mask; rp.h_shared = h->w.h_shared;
+        rp.norm_e = h->w.layer[0].norm_e; rp.norm_h = h->w.layer[0].norm_h; rp.eps = c.rms_eps;
+        rp.u = h->u; rp.resid = h->resid; rp.row_slot = h->row_slot; rp.rope_cs = h->rope_cs;
+        rp.inv_freq = h->inv_freq; rp.amax = h->amax; rp.status = status;
+        if ((rc = launch_row_build(dt, rp, s, pdl)) != PE_OK) return rc;
+        ++launches;
+    }
+    const size_t layer_elems = static_cast<size_t>(num_pages) * nkv * c.page_size * hd;
+    for (int l = 0; l < 4; ++l) {
+        const pe_layer_weights& L = h->w.layer[l];
+        char* kc = static_cast<char*>(k_cache) + l * layer_elems * h->elem;
+        char* vc = static_cast<char*>(v_cache) + l * layer_elems * h->elem;
+        if (l > 0) {
+            if ((rc = launch_rmsnorm(dt, h->resid, L.attn_norm, h->xn, R, H, c.rms_eps, s, pdl)) != PE_OK) return rc;
+            ++launches;
+        }
+        {   // a3: QKV + RoPE + paged KV write
+            GemmParams p = base;
+            p.M = qkv_rows; p.Kd = l == 0 ? 2 * H : H;
+            p.out_act = h->q; p.ld_act = qd;
+            p.k_cache = kc; p.v_cache = vc; p.nq_hd = qd; p.nkv = nkv; p.hd = hd;
+            p.row_slot = h->row_slot; p.rope_cs = h->rope_cs;
+            if ((rc = launch_gemm(dt, EPI_QKV, h->tm_qkv[l], h->tm_qkv[l], l == 0 ? tm_u : tm_xn,
+                                  l == 0 ? p_qkv0 : p_qkv, p, s, pdl)) != PE_OK)
+                return rc;
+            ++launches;
+        }
+        {   // a4: paged attention
+            AttnParams ap{};
+            ap.B = B; ap.K = K; ap.nq = nq; ap.nkv = nkv; ap.hd = hd;
+            ap.max_pages = max_pages; ap.num_pages = num_pages; ap.page_size = c.page_size;
+            ap.chunk = p_at.chunk; ap.max_splits = p_at.max_splits;
+            ap.q = h->q; ap.k_cache = kc; ap.v_cache = vc; ap.page_table = page_table; ap.seq_lens = seq_lens;
+            ap.status = status; ap.out = h->attn; ap.ws = h->attn_ws; ap.tickets = h->attn_tickets; ap.err = h->err;
+            if ((rc = launch_attention(dt, ap, s, pdl)) != PE_OK) return rc;
+            ++launches;
+        }
+        {   // a5: O projection + residual
+            GemmParams p = base;
+            p.M = H; p.Kd = qd; p.out_f32 = h->resid; p.ld_out = H;
+            if ((rc = launch_gemm(dt, EPI_RESID, h->tm_o[l], h->tm_o[l], tm_attn, p_o, p, s, pdl)) != PE_OK) return rc;
+            ++launches;
+        }
+        if ((rc = launch_rmsnorm(dt, h->resid, L.mlp_norm, h->xn, R, H, c.rms_eps, s, pdl)) != PE_OK) return rc;
+        ++launches;
+        {   // a6: gate/up + SwiGLU, then down + residual
+            GemmParams p = base;
+            p.M = F; p.Kd = H; p.out_act = h->act; p.ld_act = F;
+            if ((rc = launch_gemm(dt, EPI_SWIGLU, h->tm_gate[l], h->tm_up[l], tm_xn, p_gu, p, s, pdl)) != PE_OK) return rc;
+            ++launches;
+            GemmParams d = base;
+            d.M = H; d.Kd = F; d.out_f32 = h->resid; d.ld_out = H;
+            if ((rc = launch_gemm(dt, EPI_RESID, h->tm_down[l], h->tm_down[l], tm_act, p_down, d, s, pdl)) != PE_OK) return rc;
+            ++launches;
+        }
+    }
+    // a7: final norm, LM head + fused argmax
+    if ((rc = launch_rmsnorm(dt, h->resid, h->w.final_norm, h->xn, R, H, c.rms_eps, s, pdl)) != PE_OK) return rc;
+    ++launches;
+    {
+        GemmParams p = base;
+        p.M = V; p.Kd = H; p.amax = h->amax; p.logits = logits_dbg; p.ld_logits = V;
+        if ((rc = launch_gemm(dt, EPI_ARGMAX, h->tm_lm, h->tm_lm, tm_xn, p_lm, p, s, pdl)) != PE_OK) return rc;
+        ++launches;
+    }
+    if ((rc = launch_argmax_finalize(h->amax, status, B, K, drafts, s, pdl)) != PE_OK) return rc;
+    ++launches;
+    h->last_launches = launches;
+    return PE_OK;
+}
+
+int pe_verify_rebuild(pe_handle* h, int32_t B, int32_t K, const int32_t* drafts, const int32_t* target_tokens,
+                      const int32_t* page_table, int32_t max_pages, int32_t num_pages, const int32_t* positions,
+                      const int32_t* seq_lens, int32_t* positions_out, int32_t* seq_lens_out, int32_t* accepted,
+                      int32_t* bonus, int32_t* emitted, int32_t* slot_mapping, int32_t* rollback_slots,
+                      int32_t* status, void* stream) {
+    (void)h;
+    if (B < 1) { set_error("B must be >= 1"); return PE_ERR_ARG; }
+    if (K < 1 || K > 31) { set_error("K must be in 1..31"); return PE_ERR_ARG; }
+    if (max_pages < 1 || num_pages < 1) { set_error("max_pages and num_pages must be >= 1"); return PE_ERR_ARG; }
+    if (!drafts || !target_tokens || !page_table || !positions || !seq_lens || !positions_out || !seq_lens_out ||
+        !accepted || !bonus || !slot_mapping || !rollback_slots || !status) {
+        set_error("null tensor argument");
+        return PE_ERR_ARG;
+    }
+    return launch_verify_rebuild(B, K, drafts, target_tokens, page_table, max_pages, num_pages, 16, positions,
+                                 seq_lens, positions_out, seq_lens_out, accepted, bonus, emitted, slot_mapping,
+                                 rollback_slots, status, static_cast<cudaStream_t>(stream));
+}
+
+int pe_linear_scratch(int32_t dtype, int32_t M, int32_t N, int32_t Kd, int64_t* ws_floats, int32_t* n_tickets) {
+    if (ws_floats == nullptr || n_tickets == nullptr) { set_error("null argument"); return PE_ERR_ARG; }
+    if (dtype != PE_DTYPE_BF16 && dtype != PE_DTYPE_FP32) { set_error("unknown dtype"); return PE_ERR_ARG; }
+    if (M < 1 || N < 1 || Kd < 1) { set_error("M, N, Kd must be >= 1"); return PE_ERR_ARG; }
+    int dev = 0, sms = 0;
+    PE_CUDA_TRY(cudaGetDevice(&dev));
+    PE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const GemmPlan g = plan_gemm(M, N, Kd, EPI_STORE, dtype == PE_DTYPE_BF16 ? 2 : 4, sms);
+    *ws_floats = static_cast<int64_t>(g.ws_floats);
+    *n_tickets = g.tiles;
+    return PE_OK;
+}
+
+int pe_linear(int32_t dtype, int32_t M, int32_t N, int32_t Kd, const void* w, const void* x, float* y, float* ws,
+              int32_t* tickets, void* stream) {
+    if (!w || !x || !y || !tickets) { set_error("null tensor argument"); return PE_ERR_ARG; }
+    if (dtype != PE_DTYPE_BF16 && dtype != PE_DTYPE_FP32) { set_error("unknown dtype"); return PE_ERR_ARG; }
+    if (M < 1 || N < 1 || Kd < 1 || Kd % 8 != 0) { set_error("need M, N >= 1 and Kd a positive multiple of 8"); return PE_ERR_ARG; }
+    int dev = 0, sms = 0;
+    PE_CUDA_TRY(cudaGetDevice(&dev));
+    PE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const int eb = dtype == PE_DTYPE_BF16 ? 2 : 4;
+    const GemmPlan g = plan_gemm(M, N, Kd, EPI_STORE, eb, sms);
+    if (g.ws_floats > 0 && ws == nullptr) { set_error("this shape needs split-K scratch"); return PE_ERR_ARG; }
+    CUtensorMap ta, tb;
+    int rc = encode_tmap_2d(&ta, w, dtype, Kd, M, static_cast<uint64_t>(Kd) * eb, 128 / eb, 128);
+    if (rc == PE_OK) rc = encode_tmap_2d(&tb, x, dtype, Kd, N, static_cast<uint64_t>(Kd) * eb, 128 / eb, g.bn);
+    if (rc != PE_OK) return rc;
+    GemmParams p{};
+    p.M = M; p.N = N; p.Kd = Kd; p.out_f32 = y; p.ld_out = M; p.ws = ws; p.tickets = tickets; p.err = nullptr;
+    return launch_gemm(dtype, EPI_STORE, ta, ta, tb, g, p, static_cast<cudaStream_t>(stream), false);
+}
+
+}  // extern "C"

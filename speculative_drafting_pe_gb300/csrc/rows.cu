@@ -1,0 +1,170 @@
+// Row construction, RMSNorm and argmax finalisation.
+//
+// k_row_build builds the K input rows of every request (P-EAGLE post,
+// "Solution overview / step-by-step drafting", Step 2): row 0 from the real
+// token embedding and the FC-fused target hidden state, rows 1..K-1 from the
+// learned mask embedding emb_mask and the shared hidden state h_shared. Layer
+// 0 attends over the 2H concat [RMSNorm_e(emb); RMSNorm_h(hid)] and its
+// residual stream starts at `hid`. The same kernel validates each request,
+// computes each row's cache slot (entry S_b + j) and RoPE cos/sin (position
+// Q_b + j), and clears the packed argmax records for this step.
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pe {
+namespace {
+
+constexpr int kRowThreads = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[w];
+    return t;
+}
+
+// Status of request b: capacity, page indices of entries 0..S+K-1, inputs.
+__device__ int request_status(const RowBuildParams& p, int b, float* red_unused) {
+    const int S = p.seq_lens[b];
+    const int tok = p.last_token[b];
+    const int Q = p.positions[b];
+    if (S < 0 || Q < 0 || tok < 0 || tok >= p.V) return PE_REQ_BAD_INPUT;
+    if (static_cast<long long>(S) + p.K > static_cast<long long>(p.max_pages) * p.page_size) return PE_REQ_CAPACITY;
+    const int n_pages = (S + p.K + p.page_size - 1) / p.page_size;
+    int bad = 0;
+    for (int i = threadIdx.x; i < n_pages; i += blockDim.x) {
+        const int pg = p.page_table[static_cast<size_t>(b) * p.max_pages + i];
+        if (pg < 0 || pg >= p.num_pages) bad = 1;
+    }
+    bad = __syncthreads_or(bad);
+    return bad ? PE_REQ_BAD_PAGE : PE_REQ_OK;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams p) {
+    __shared__ float red[32];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int r = blockIdx.x;
+    const int b = r / p.K;
+    const int j = r - b * p.K;
+    const int H = p.H;
+    const int st = request_status(p, b, red);
+    if (j == 0 && threadIdx.x == 0) p.status[b] = st;
+    if (threadIdx.x == 0) p.amax[r] = 0ull;
+
+    T* u = static_cast<T*>(p.u) + static_cast<size_t>(r) * 2 * H;
+    float* resid = p.resid + static_cast<size_t>(r) * H;
+    const T* emb;
+    if (j == 0) emb = static_cast<const T*>(p.embed) + static_cast<size_t>(st == PE_REQ_OK ? p.last_token[b] : 0) * H;
+    else emb = static_cast<const T*>(p.emb_mask);
+    const T* ge = static_cast<const T*>(p.norm_e);
+    const T* gh = static_cast<const T*>(p.norm_h);
+    const T* hsh = static_cast<const T*>(p.h_shared);
+    const float* h0 = p.h + static_cast<size_t>(b) * H;
+
+    float ss_e = 0.f, ss_h = 0.f;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) {
+        const float e = Elem<T>::to_f(emb[i]);
+        const float hv = (j == 0) ? h0[i] : Elem<T>::to_f(hsh[i]);
+        ss_e += e * e;
+        ss_h += hv * hv;
+    }
+    const float tot_e = block_sum(ss_e, red);
+    const float tot_h = block_sum(ss_h, red);
+    const float inv_e = rsqrtf(tot_e / H + p.eps);
+    const float inv_h = rsqrtf(tot_h / H + p.eps);
+    for (int i = threadIdx.x; i < H; i += blockDim.x) {
+        const float e = Elem<T>::to_f(emb[i]);
+        const float hv = (j == 0) ? h0[i] : Elem<T>::to_f(hsh[i]);
+        const bool ok = st == PE_REQ_OK;
+        u[i] = Elem<T>::from_f(ok ? e * inv_e * Elem<T>::to_f(ge[i]) : 0.f);
+        u[H + i] = Elem<T>::from_f(ok ? hv * inv_h * Elem<T>::to_f(gh[i]) : 0.f);
+        resid[i] = ok ? hv : 0.f;
+    }
+
+    if (threadIdx.x == 0) {
+        int slot = -1;
+        if (st == PE_REQ_OK) {
+            const int e = p.seq_lens[b] + j;
+            const int pg = p.page_table[static_cast<size_t>(b) * p.max_pages + e / p.page_size];
+            slot = pg * p.page_size + e % p.page_size;
+        }
+        p.row_slot[r] = slot;
+    }
+    // RoPE table for this row: angle = (Q_b + j) * inv_freq_i in double,
+    // reduced to [-pi, pi] in double, then sin/cos in float.
+    const int half = p.hd / 2;
+    const double pos = static_cast<double>(st == PE_REQ_OK ? p.positions[b] + j : 0);
+    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+        const double a = pos * p.inv_freq[i];
+        const double two_pi = 6.283185307179586476925286766559;
+        const double red_a = a - two_pi * rint(a / two_pi);
+        float s, c;
+        sincosf(static_cast<float>(red_a), &s, &c);
+        p.rope_cs[static_cast<size_t>(r) * half + i] = make_float2(c, s);
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads)
+    k_rmsnorm(const float* __restrict__ x, const T* __restrict__ gain, T* __restrict__ out, int H, float eps) {
+    __shared__ float red[32];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int r = blockIdx.x;
+    const float* xr = x + static_cast<size_t>(r) * H;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) ss += xr[i] * xr[i];
+    const float inv = rsqrtf(block_sum(ss, red) / H + eps);
+    T* o = out + static_cast<size_t>(r) * H;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) o[i] = Elem<T>::from_f(xr[i] * inv * Elem<T>::to_f(gain[i]));
+}
+
+__global__ void k_argmax_finalize(const unsigned long long* __restrict__ amax, const int32_t* __restrict__ status,
+                                  int B, int K, int32_t* __restrict__ drafts) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= B * K) return;
+    const int b = r / K;
+    const unsigned long long key = amax[r];
+    drafts[r] = (status[b] == PE_REQ_OK && key != 0ull) ? static_cast<int32_t>(argmax_key_index(key)) : -1;
+}
+
+}  // namespace
+
+int launch_row_build(int dtype, const RowBuildParams& p, cudaStream_t s, bool pdl) {
+    const dim3 grid(p.B * p.K), block(kRowThreads);
+    if (dtype == PE_DTYPE_BF16) PE_CUDA_TRY(launch_ex(k_row_build<__nv_bfloat16>, grid, block, 0, s, pdl, p));
+    else PE_CUDA_TRY(launch_ex(k_row_build<float>, grid, block, 0, s, pdl, p));
+    return PE_OK;
+}
+
+int launch_rmsnorm(int dtype, const float* x, const void* gain, void* out, int rows, int H, float eps,
+                   cudaStream_t s, bool pdl) {
+    const dim3 grid(rows), block(kRowThreads);
+    if (dtype == PE_DTYPE_BF16)
+        PE_CUDA_TRY(launch_ex(k_rmsnorm<__nv_bfloat16>, grid, block, 0, s, pdl, x,
+                              static_cast<const __nv_bfloat16*>(gain), static_cast<__nv_bfloat16*>(out), H, eps));
+    else
+        PE_CUDA_TRY(launch_ex(k_rmsnorm<float>, grid, block, 0, s, pdl, x, static_cast<const float*>(gain),
+                              static_cast<float*>(out), H, eps));
+    return PE_OK;
+}
+
+int launch_argmax_finalize(const unsigned long long* amax, const int32_t* status, int B, int K, int32_t* drafts,
+                           cudaStream_t s, bool pdl) {
+    const int R = B * K;
+    PE_CUDA_TRY(launch_ex(k_argmax_finalize, dim3((R + 127) / 128), dim3(128), 0, s, pdl, amax, status, B, K, drafts));
+    return PE_OK;
+}
+
+}  // namespace pe

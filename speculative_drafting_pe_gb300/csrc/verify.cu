@@ -1,0 +1,93 @@
+// Fused greedy verification + batch-metadata rebuild + KV rollback.
+//
+// One warp per request. With the target's argmax tokens g for the K+1
+// verified positions (P-EAGLE post, "Solution overview": the target checks
+// all K drafts in one pass; greedy decoding keeps the output identical to the
+// target's own), the kernel computes in one pass:
+//   a     = length of the longest prefix with d == g          (warp ballot)
+//   bonus = g[a]
+//   kept  = min(a, K-1) + 1 drafter-cache rows stay committed
+//   S'    = S + kept,  Q' = Q + a + 1
+//   slot_mapping[j] = page_table[(S'+j)/16]*16 + (S'+j)%16,  j < K
+//   rollback: slots of entries S' .. S+K-1, then -1
+// A request whose next K entries exceed its page table, or whose page index
+// is out of range, gets a per-request status and pass-through metadata.
+#include "common.cuh"
+#include "internal.h"
+
+namespace pe {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    k_verify_rebuild(int B, int K, const int32_t* __restrict__ drafts, const int32_t* __restrict__ target,
+                     const int32_t* __restrict__ page_table, int max_pages, int num_pages, int page_size,
+                     const int32_t* positions, const int32_t* seq_lens, int32_t* positions_out,
+                     int32_t* seq_lens_out, int32_t* __restrict__ accepted, int32_t* __restrict__ bonus,
+                     int32_t* __restrict__ emitted, int32_t* __restrict__ slot_mapping,
+                     int32_t* __restrict__ rollback, int32_t* __restrict__ status) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int b = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (b >= B) return;
+    const unsigned full = 0xffffffffu;
+
+    const int dj = lane < K ? drafts[static_cast<size_t>(b) * K + lane] : 0;
+    const int gj = lane <= K ? target[static_cast<size_t>(b) * (K + 1) + lane] : 0;
+    const unsigned mism = __ballot_sync(full, lane < K && dj != gj);
+    const int a = mism ? (__ffs(mism) - 1) : K;
+    const int bon = __shfl_sync(full, gj, a);
+
+    const int S = seq_lens[b];
+    const int Q = positions[b];
+    __syncwarp();
+    const int kept = min(a, K - 1) + 1;
+    const int S2 = S + kept;
+    const int Q2 = Q + a + 1;
+
+    int st = PE_REQ_OK;
+    if (S < 0 || Q < 0) st = PE_REQ_BAD_INPUT;
+    else if (static_cast<long long>(S2) + K > static_cast<long long>(max_pages) * page_size) st = PE_REQ_CAPACITY;
+    int slot = -1;
+    int bad = 0;
+    if (st == PE_REQ_OK && lane < K) {
+        const int e = S2 + lane;
+        const int page = page_table[static_cast<size_t>(b) * max_pages + e / page_size];
+        if (page < 0 || page >= num_pages) bad = 1;
+        else slot = page * page_size + e % page_size;
+    }
+    if (__any_sync(full, bad) && st == PE_REQ_OK) st = PE_REQ_BAD_PAGE;
+    const bool ok = st == PE_REQ_OK;
+
+    if (lane < K) {
+        slot_mapping[static_cast<size_t>(b) * K + lane] = ok ? slot : -1;
+        rollback[static_cast<size_t>(b) * K + lane] = (ok && lane < K - kept) ? slot : -1;
+    }
+    if (emitted != nullptr && lane <= K)
+        emitted[static_cast<size_t>(b) * (K + 1) + lane] = lane < a ? dj : (lane == a ? bon : -1);
+    if (lane == 0) {
+        accepted[b] = a;
+        bonus[b] = bon;
+        status[b] = st;
+        seq_lens_out[b] = ok ? S2 : S;
+        positions_out[b] = ok ? Q2 : Q;
+    }
+}
+
+}  // namespace
+
+int launch_verify_rebuild(int B, int K, const int32_t* drafts, const int32_t* target, const int32_t* page_table,
+                          int max_pages, int num_pages, int page_size, const int32_t* positions,
+                          const int32_t* seq_lens, int32_t* positions_out, int32_t* seq_lens_out,
+                          int32_t* accepted, int32_t* bonus, int32_t* emitted, int32_t* slot_mapping,
+                          int32_t* rollback, int32_t* status, cudaStream_t s) {
+    const dim3 grid((B + kWarpsPerBlock - 1) / kWarpsPerBlock), block(kWarpsPerBlock * 32);
+    PE_CUDA_TRY(launch_ex(k_verify_rebuild, grid, block, 0, s, false, B, K, drafts, target, page_table, max_pages,
+                          num_pages, page_size, positions, seq_lens, positions_out, seq_lens_out, accepted, bonus,
+                          emitted, slot_mapping, rollback, status));
+    return PE_OK;
+}
+
+}  // namespace pe

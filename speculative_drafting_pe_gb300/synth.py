@@ -236,9 +236,10 @@ def make_verify_inputs(B, K, vocab, seq_range, alpha, seed, page_size=16):
 
 
 def weights_to_numpy(W):
-    """float64 host copies of a weight dict (for the oracle)."""
+    """Host float32 copies of a weight dict for the oracle (exact for bf16 and
+    fp32 values; the oracle widens to float64 as it computes)."""
     def cv(t):
-        return None if t is None else t.detach().to("cpu", torch.float64).numpy()
+        return None if t is None else t.detach().to("cpu", torch.float32).numpy()
     out = {k: cv(v) for k, v in W.items() if k != "layers"}
     out["layers"] = [{k: cv(v) for k, v in L.items()} for L in W["layers"]]
     return out

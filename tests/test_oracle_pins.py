@@ -132,12 +132,13 @@ def test_build_rows_row0_real_rest_placeholders():
     u, resid = oracle.build_rows(TINY, Wn, inp.last_token.numpy(), h, 4)
     H = TINY.hidden
     for b in range(2):
-        e0 = Wn["embed"][inp.last_token[b]]
-        np.testing.assert_allclose(u[b, 0, :H], e0 / np.sqrt(np.mean(e0 ** 2) + 1e-6) * Wn["layers"][0]["norm_e"])
+        e0 = Wn["embed"][inp.last_token[b]].astype(np.float64)
+        ge = Wn["layers"][0]["norm_e"].astype(np.float64)
+        np.testing.assert_allclose(u[b, 0, :H], e0 / np.sqrt(np.mean(e0 ** 2) + 1e-6) * ge)
         np.testing.assert_allclose(resid[b, 0], h[b])
         for j in range(1, 4):
-            m = Wn["emb_mask"]
-            np.testing.assert_allclose(u[b, j, :H], m / np.sqrt(np.mean(m ** 2) + 1e-6) * Wn["layers"][0]["norm_e"])
+            m = Wn["emb_mask"].astype(np.float64)
+            np.testing.assert_allclose(u[b, j, :H], m / np.sqrt(np.mean(m ** 2) + 1e-6) * ge)
             np.testing.assert_allclose(resid[b, j], Wn["h_shared"])
 
 
