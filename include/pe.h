@@ -176,6 +176,27 @@ int pe_linear(int32_t dtype, int32_t M, int32_t N, int32_t Kd, const void* w, co
  * (PE_DEVERR_* bits; 0 = no device-side wait gave up). */
 int pe_device_errors(pe_handle* h, void* stream, uint32_t* out_bits);
 
+/* Kernel kinds of the draft pass, for launch accounting and profiling. */
+#define PE_KERNEL_FC         0
+#define PE_KERNEL_ROW_BUILD  1
+#define PE_KERNEL_RMSNORM    2
+#define PE_KERNEL_QKV        3
+#define PE_KERNEL_ATTENTION  4
+#define PE_KERNEL_O_PROJ     5
+#define PE_KERNEL_GATE_UP    6
+#define PE_KERNEL_DOWN       7
+#define PE_KERNEL_LM_HEAD    8
+#define PE_KERNEL_ARGMAX     9
+#define PE_KERNEL_COUNT      10
+
+/* Measurement hook: after pe_profile_start, every launch of `kernel_kind`
+ * made by pe_draft (up to max_launches of them) is bracketed by CUDA events
+ * recorded on the launch stream. pe_profile_stop waits for those events and
+ * returns the summed device time (ms) and the number of launches timed. */
+int pe_profile_start(pe_handle* h, int32_t kernel_kind, int32_t max_launches);
+int pe_profile_stop(pe_handle* h, float* total_ms, int32_t* launches);
+const char* pe_kernel_name(int32_t kind);
+
 /* Number of kernels the last pe_draft call enqueued (for launch accounting). */
 int pe_last_launch_count(const pe_handle* h);
 

@@ -20,7 +20,9 @@ PE_DTYPE_BF16, PE_DTYPE_FP32 = 0, 1
 EXPORTS = (
     "pe_init_drafter", "pe_draft", "pe_verify_rebuild", "pe_device_errors",
     "pe_last_launch_count", "pe_destroy", "pe_last_error", "pe_abi_version", "pe_linear_scratch", "pe_linear",
+    "pe_profile_start", "pe_profile_stop", "pe_kernel_name",
 )
+KERNEL_KINDS = ("fc", "row_build", "rmsnorm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "argmax")
 
 _i32 = ctypes.c_int32
 _vp = ctypes.c_void_p
@@ -88,6 +90,12 @@ def load():
     lib.pe_linear_scratch.restype = ctypes.c_int
     lib.pe_linear.argtypes = [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.pe_linear.restype = ctypes.c_int
+    lib.pe_profile_start.argtypes = [_vp, _i32, _i32]
+    lib.pe_profile_start.restype = ctypes.c_int
+    lib.pe_profile_stop.argtypes = [_vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_i32)]
+    lib.pe_profile_stop.restype = ctypes.c_int
+    lib.pe_kernel_name.argtypes = [_i32]
+    lib.pe_kernel_name.restype = ctypes.c_char_p
     _LIB = lib
     return lib
 
@@ -173,6 +181,17 @@ class Drafter:
                                _p(page_table), page_table.shape[1], num_pages, _p(k_cache), _p(v_cache),
                                _p(drafts), _p(logits), _p(status), _stream_ptr(stream)))
         return drafts, status
+
+    def profile_start(self, kind, max_launches):
+        """Time every launch of one kernel kind (name from KERNEL_KINDS) with
+        CUDA events on its launch stream until profile_stop()."""
+        _check(load().pe_profile_start(self._h, KERNEL_KINDS.index(kind), max_launches))
+
+    def profile_stop(self):
+        """(total device ms, launches timed) since profile_start()."""
+        ms, n = ctypes.c_float(0), _i32(0)
+        _check(load().pe_profile_stop(self._h, ctypes.byref(ms), ctypes.byref(n)))
+        return ms.value, n.value
 
     def launch_count(self):
         return load().pe_last_launch_count(self._h)

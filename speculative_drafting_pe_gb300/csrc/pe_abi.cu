@@ -55,6 +55,10 @@ struct pe_handle {
     CUtensorMap tm_fc, tm_lm;
     CUtensorMap tm_qkv[4], tm_o[4], tm_gate[4], tm_up[4], tm_down[4];
     int last_launches = 0;
+    // profiling hook (pe_profile_start / pe_profile_stop)
+    int prof_kind = -1;
+    int prof_used = 0;
+    std::vector<cudaEvent_t> prof_events;
 };
 
 namespace pe {
@@ -129,6 +133,7 @@ int act_map(const pe_handle* h, CUtensorMap* m, const void* x, int rows, int col
 
 void free_handle(pe_handle* h) {
     if (h == nullptr) return;
+    for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
     void* ptrs[] = {h->h,    h->resid,    h->u,        h->xn,         h->q,       h->attn,         h->act,
                     h->amax, h->row_slot, h->rope_cs, h->inv_freq, h->gemm_ws, h->gemm_tickets, h->attn_ws,
                     h->attn_tickets, h->err};
@@ -380,13 +385,27 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     base.tickets = h->gemm_tickets;
     base.err = h->err;
 
+    // Every launch goes through `run`, which counts it and, when the kernel
+    // kind is being profiled, brackets it with CUDA events on stream s.
+    auto run = [&](int kind, auto&& fn) -> int {
+        const bool prof = h->prof_kind == kind && h->prof_used + 2 <= static_cast<int>(h->prof_events.size());
+        if (prof) cudaEventRecord(h->prof_events[h->prof_used], s);
+        const int r = fn();
+        if (r == PE_OK) ++launches;
+        if (prof) {
+            cudaEventRecord(h->prof_events[h->prof_used + 1], s);
+            h->prof_used += 2;
+        }
+        return r;
+    };
+
     // a1: h = W_fc [h_lo; h_mid; h_hi]
     {
         GemmParams p = base;
         p.M = H; p.N = B; p.Kd = 3 * H;
         p.out_f32 = h->h; p.ld_out = H;
-        if ((rc = launch_gemm(dt, EPI_STORE, h->tm_fc, h->tm_fc, tm_th, p_fc, p, s, pdl)) != PE_OK) return rc;
-        ++launches;
+        rc = run(PE_KERNEL_FC, [&] { return launch_gemm(dt, EPI_STORE, h->tm_fc, h->tm_fc, tm_th, p_fc, p, s, pdl); });
+        if (rc != PE_OK) return rc;
     }
     // a2: rows, slots, RoPE table, status, argmax reset
     {
@@ -398,8 +417,7 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         rp.norm_e = h->w.layer[0].norm_e; rp.norm_h = h->w.layer[0].norm_h; rp.eps = c.rms_eps;
         rp.u = h->u; rp.resid = h->resid; rp.row_slot = h->row_slot; rp.rope_cs = h->rope_cs;
         rp.inv_freq = h->inv_freq; rp.amax = h->amax; rp.status = status;
-        if ((rc = launch_row_build(dt, rp, s, pdl)) != PE_OK) return rc;
-        ++launches;
+        if ((rc = run(PE_KERNEL_ROW_BUILD, [&] { return launch_row_build(dt, rp, s, pdl); })) != PE_OK) return rc;
     }
     const size_t layer_elems = static_cast<size_t>(num_pages) * nkv * c.page_size * hd;
     for (int l = 0; l < 4; ++l) {
@@ -407,8 +425,9 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         char* kc = static_cast<char*>(k_cache) + l * layer_elems * h->elem;
         char* vc = static_cast<char*>(v_cache) + l * layer_elems * h->elem;
         if (l > 0) {
-            if ((rc = launch_rmsnorm(dt, h->resid, L.attn_norm, h->xn, R, H, c.rms_eps, s, pdl)) != PE_OK) return rc;
-            ++launches;
+            rc = run(PE_KERNEL_RMSNORM,
+                     [&] { return launch_rmsnorm(dt, h->resid, L.attn_norm, h->xn, R, H, c.rms_eps, s, pdl); });
+            if (rc != PE_OK) return rc;
         }
         {   // a3: QKV + RoPE + paged KV write
             GemmParams p = base;
@@ -416,10 +435,11 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
             p.out_act = h->q; p.ld_act = qd;
             p.k_cache = kc; p.v_cache = vc; p.nq_hd = qd; p.nkv = nkv; p.hd = hd;
             p.row_slot = h->row_slot; p.rope_cs = h->rope_cs;
-            if ((rc = launch_gemm(dt, EPI_QKV, h->tm_qkv[l], h->tm_qkv[l], l == 0 ? tm_u : tm_xn,
-                                  l == 0 ? p_qkv0 : p_qkv, p, s, pdl)) != PE_OK)
-                return rc;
-            ++launches;
+            rc = run(PE_KERNEL_QKV, [&] {
+                return launch_gemm(dt, EPI_QKV, h->tm_qkv[l], h->tm_qkv[l], l == 0 ? tm_u : tm_xn,
+                                   l == 0 ? p_qkv0 : p_qkv, p, s, pdl);
+            });
+            if (rc != PE_OK) return rc;
         }
         {   // a4: paged attention
             AttnParams ap{};
@@ -428,41 +448,86 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
             ap.chunk = p_at.chunk; ap.max_splits = p_at.max_splits;
             ap.q = h->q; ap.k_cache = kc; ap.v_cache = vc; ap.page_table = page_table; ap.seq_lens = seq_lens;
             ap.status = status; ap.out = h->attn; ap.ws = h->attn_ws; ap.tickets = h->attn_tickets; ap.err = h->err;
-            if ((rc = launch_attention(dt, ap, s, pdl)) != PE_OK) return rc;
-            ++launches;
+            if ((rc = run(PE_KERNEL_ATTENTION, [&] { return launch_attention(dt, ap, s, pdl); })) != PE_OK) return rc;
         }
         {   // a5: O projection + residual
             GemmParams p = base;
             p.M = H; p.Kd = qd; p.out_f32 = h->resid; p.ld_out = H;
-            if ((rc = launch_gemm(dt, EPI_RESID, h->tm_o[l], h->tm_o[l], tm_attn, p_o, p, s, pdl)) != PE_OK) return rc;
-            ++launches;
+            rc = run(PE_KERNEL_O_PROJ,
+                     [&] { return launch_gemm(dt, EPI_RESID, h->tm_o[l], h->tm_o[l], tm_attn, p_o, p, s, pdl); });
+            if (rc != PE_OK) return rc;
         }
-        if ((rc = launch_rmsnorm(dt, h->resid, L.mlp_norm, h->xn, R, H, c.rms_eps, s, pdl)) != PE_OK) return rc;
-        ++launches;
+        rc = run(PE_KERNEL_RMSNORM,
+                 [&] { return launch_rmsnorm(dt, h->resid, L.mlp_norm, h->xn, R, H, c.rms_eps, s, pdl); });
+        if (rc != PE_OK) return rc;
         {   // a6: gate/up + SwiGLU, then down + residual
             GemmParams p = base;
             p.M = F; p.Kd = H; p.out_act = h->act; p.ld_act = F;
-            if ((rc = launch_gemm(dt, EPI_SWIGLU, h->tm_gate[l], h->tm_up[l], tm_xn, p_gu, p, s, pdl)) != PE_OK) return rc;
-            ++launches;
+            rc = run(PE_KERNEL_GATE_UP,
+                     [&] { return launch_gemm(dt, EPI_SWIGLU, h->tm_gate[l], h->tm_up[l], tm_xn, p_gu, p, s, pdl); });
+            if (rc != PE_OK) return rc;
             GemmParams d = base;
             d.M = H; d.Kd = F; d.out_f32 = h->resid; d.ld_out = H;
-            if ((rc = launch_gemm(dt, EPI_RESID, h->tm_down[l], h->tm_down[l], tm_act, p_down, d, s, pdl)) != PE_OK) return rc;
-            ++launches;
+            rc = run(PE_KERNEL_DOWN,
+                     [&] { return launch_gemm(dt, EPI_RESID, h->tm_down[l], h->tm_down[l], tm_act, p_down, d, s, pdl); });
+            if (rc != PE_OK) return rc;
         }
     }
     // a7: final norm, LM head + fused argmax
-    if ((rc = launch_rmsnorm(dt, h->resid, h->w.final_norm, h->xn, R, H, c.rms_eps, s, pdl)) != PE_OK) return rc;
-    ++launches;
+    rc = run(PE_KERNEL_RMSNORM,
+             [&] { return launch_rmsnorm(dt, h->resid, h->w.final_norm, h->xn, R, H, c.rms_eps, s, pdl); });
+    if (rc != PE_OK) return rc;
     {
         GemmParams p = base;
         p.M = V; p.Kd = H; p.amax = h->amax; p.logits = logits_dbg; p.ld_logits = V;
-        if ((rc = launch_gemm(dt, EPI_ARGMAX, h->tm_lm, h->tm_lm, tm_xn, p_lm, p, s, pdl)) != PE_OK) return rc;
-        ++launches;
+        rc = run(PE_KERNEL_LM_HEAD,
+                 [&] { return launch_gemm(dt, EPI_ARGMAX, h->tm_lm, h->tm_lm, tm_xn, p_lm, p, s, pdl); });
+        if (rc != PE_OK) return rc;
     }
-    if ((rc = launch_argmax_finalize(h->amax, status, B, K, drafts, s, pdl)) != PE_OK) return rc;
-    ++launches;
+    rc = run(PE_KERNEL_ARGMAX, [&] { return launch_argmax_finalize(h->amax, status, B, K, drafts, s, pdl); });
+    if (rc != PE_OK) return rc;
     h->last_launches = launches;
     return PE_OK;
+}
+
+int pe_profile_start(pe_handle* h, int32_t kernel_kind, int32_t max_launches) {
+    if (h == nullptr || kernel_kind < 0 || kernel_kind >= PE_KERNEL_COUNT || max_launches < 1) {
+        set_error("bad profiling arguments");
+        return PE_ERR_ARG;
+    }
+    for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
+    h->prof_events.assign(2 * static_cast<size_t>(max_launches), nullptr);
+    for (auto& e : h->prof_events) PE_CUDA_TRY(cudaEventCreate(&e));
+    h->prof_used = 0;
+    h->prof_kind = kernel_kind;
+    return PE_OK;
+}
+
+int pe_profile_stop(pe_handle* h, float* total_ms, int32_t* launches) {
+    if (h == nullptr || total_ms == nullptr || launches == nullptr) { set_error("null argument"); return PE_ERR_ARG; }
+    double total = 0.0;
+    int n = 0;
+    for (int i = 0; i + 1 < h->prof_used; i += 2) {
+        PE_CUDA_TRY(cudaEventSynchronize(h->prof_events[i + 1]));
+        float ms = 0.f;
+        PE_CUDA_TRY(cudaEventElapsedTime(&ms, h->prof_events[i], h->prof_events[i + 1]));
+        total += ms;
+        ++n;
+    }
+    for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
+    h->prof_events.clear();
+    h->prof_used = 0;
+    h->prof_kind = -1;
+    *total_ms = static_cast<float>(total);
+    *launches = n;
+    return PE_OK;
+}
+
+const char* pe_kernel_name(int32_t kind) {
+    static const char* names[PE_KERNEL_COUNT] = {"fc_gemm", "row_build", "rmsnorm", "qkv_rope_kv_gemm",
+                                                 "paged_attention", "o_proj_resid_gemm", "gate_up_swiglu_gemm",
+                                                 "down_resid_gemm", "lm_head_argmax_gemm", "argmax_finalize"};
+    return (kind >= 0 && kind < PE_KERNEL_COUNT) ? names[kind] : "unknown";
 }
 
 int pe_verify_rebuild(pe_handle* h, int32_t B, int32_t K, const int32_t* drafts, const int32_t* target_tokens,
