@@ -172,6 +172,27 @@ int pe_linear_scratch(int32_t dtype, int32_t M, int32_t N, int32_t Kd, int64_t* 
 int pe_linear(int32_t dtype, int32_t M, int32_t N, int32_t Kd, const void* w, const void* x, float* y,
               float* ws, int32_t* tickets, void* stream);
 
+/* One whole step (pe_draft, then pe_verify_rebuild on its drafts) captured
+ * once into a CUDA graph and replayed with a single launch. The arguments are
+ * those of pe_draft and pe_verify_rebuild (drafts are shared; draft_status and
+ * verify_status are the two status arrays); every pointer is baked into the
+ * graph, so callers update buffer CONTENTS between launches, not addresses.
+ * When positions_out/seq_lens_out alias positions/seq_lens, each replay
+ * advances the batch metadata in place. Creation synchronises nothing and
+ * enqueues nothing; launches are asynchronous on `stream`. */
+typedef struct pe_step_graph pe_step_graph;
+int pe_step_graph_create(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, const void* target_hidden,
+                         const int32_t* positions, const int32_t* seq_lens, const int32_t* page_table,
+                         int32_t max_pages, int32_t num_pages, void* k_cache, void* v_cache, int32_t* drafts,
+                         int32_t* draft_status, const int32_t* target_tokens, int32_t* positions_out,
+                         int32_t* seq_lens_out, int32_t* accepted, int32_t* bonus, int32_t* emitted,
+                         int32_t* slot_mapping, int32_t* rollback_slots, int32_t* verify_status,
+                         pe_step_graph** out);
+int pe_step_graph_launch(pe_step_graph* g, void* stream);
+/* kernels one replay launches */
+int pe_step_graph_launch_count(const pe_step_graph* g);
+void pe_step_graph_destroy(pe_step_graph* g);
+
 /* Synchronise `stream` and return (then clear) the device error word of h
  * (PE_DEVERR_* bits; 0 = no device-side wait gave up). */
 int pe_device_errors(pe_handle* h, void* stream, uint32_t* out_bits);

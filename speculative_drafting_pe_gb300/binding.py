@@ -21,6 +21,7 @@ EXPORTS = (
     "pe_init_drafter", "pe_draft", "pe_verify_rebuild", "pe_device_errors",
     "pe_last_launch_count", "pe_destroy", "pe_last_error", "pe_abi_version", "pe_linear_scratch", "pe_linear",
     "pe_profile_start", "pe_profile_stop", "pe_kernel_name",
+    "pe_step_graph_create", "pe_step_graph_launch", "pe_step_graph_launch_count", "pe_step_graph_destroy",
 )
 KERNEL_KINDS = ("fc", "row_build", "rmsnorm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "argmax")
 
@@ -96,6 +97,15 @@ def load():
     lib.pe_profile_stop.restype = ctypes.c_int
     lib.pe_kernel_name.argtypes = [_i32]
     lib.pe_kernel_name.restype = ctypes.c_char_p
+    lib.pe_step_graph_create.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp,
+                                         _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(_vp)]
+    lib.pe_step_graph_create.restype = ctypes.c_int
+    lib.pe_step_graph_launch.argtypes = [_vp, _vp]
+    lib.pe_step_graph_launch.restype = ctypes.c_int
+    lib.pe_step_graph_launch_count.argtypes = [_vp]
+    lib.pe_step_graph_launch_count.restype = ctypes.c_int
+    lib.pe_step_graph_destroy.argtypes = [_vp]
+    lib.pe_step_graph_destroy.restype = None
     _LIB = lib
     return lib
 
@@ -196,6 +206,13 @@ class Drafter:
     def launch_count(self):
         return load().pe_last_launch_count(self._h)
 
+    def step_graph(self, last_token, target_hidden, positions, seq_lens, page_table, num_pages, k_cache, v_cache,
+                   K, target_tokens, positions_out=None, seq_lens_out=None):
+        """Capture draft + verify/rebuild into a replayable StepGraph over
+        fixed buffers (outputs allocated here unless given)."""
+        return StepGraph(self, last_token, target_hidden, positions, seq_lens, page_table, num_pages, k_cache,
+                         v_cache, K, target_tokens, positions_out, seq_lens_out)
+
     def device_errors(self, stream=None):
         bits = ctypes.c_uint32(0)
         _check(load().pe_device_errors(self._h, _stream_ptr(stream), ctypes.byref(bits)))
@@ -205,6 +222,55 @@ class Drafter:
         if getattr(self, "_h", None) is not None and self._h.value:
             load().pe_destroy(self._h)
             self._h = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class StepGraph:
+    """One draft pass + verify/rebuild captured into a CUDA graph by the
+    library; ``launch()`` replays it. Buffers are fixed at capture."""
+
+    def __init__(self, drafter, last_token, target_hidden, positions, seq_lens, page_table, num_pages, k_cache,
+                 v_cache, K, target_tokens, positions_out=None, seq_lens_out=None):
+        lib = load()
+        dev = drafter.device
+        B = last_token.shape[0]
+        for name, t in (("last_token", last_token), ("positions", positions), ("seq_lens", seq_lens),
+                        ("page_table", page_table), ("target_tokens", target_tokens)):
+            _need(t, torch.int32, dev, name)
+        _need(target_hidden, drafter.dtype, dev, "target_hidden")
+        z = lambda *s: torch.zeros(*s, dtype=torch.int32, device=dev)
+        self.inputs = dict(last_token=last_token, target_hidden=target_hidden, positions=positions,
+                           seq_lens=seq_lens, page_table=page_table, target_tokens=target_tokens,
+                           k_cache=k_cache, v_cache=v_cache)
+        self.out = dict(drafts=z(B, K), draft_status=z(B), accepted=z(B), bonus=z(B), emitted=z(B, K + 1),
+                        slot_mapping=z(B, K), rollback_slots=z(B, K), status=z(B),
+                        positions=positions_out if positions_out is not None else z(B),
+                        seq_lens=seq_lens_out if seq_lens_out is not None else z(B))
+        o = self.out
+        g = _vp()
+        _check(lib.pe_step_graph_create(
+            drafter._h, B, K, _p(last_token), _p(target_hidden), _p(positions), _p(seq_lens), _p(page_table),
+            page_table.shape[1], num_pages, _p(k_cache), _p(v_cache), _p(o["drafts"]), _p(o["draft_status"]),
+            _p(target_tokens), _p(o["positions"]), _p(o["seq_lens"]), _p(o["accepted"]), _p(o["bonus"]),
+            _p(o["emitted"]), _p(o["slot_mapping"]), _p(o["rollback_slots"]), _p(o["status"]), ctypes.byref(g)))
+        self._g = g
+        self._drafter = drafter     # keeps the handle (and its workspaces) alive
+
+    def launch(self, stream=None):
+        _check(load().pe_step_graph_launch(self._g, _stream_ptr(stream)))
+
+    def launch_count(self):
+        return load().pe_step_graph_launch_count(self._g)
+
+    def close(self):
+        if getattr(self, "_g", None) is not None and self._g.value:
+            load().pe_step_graph_destroy(self._g)
+            self._g = _vp()
 
     def __del__(self):
         try:

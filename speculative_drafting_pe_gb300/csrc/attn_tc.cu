@@ -1,0 +1,398 @@
+// Tensor-core decode-style paged GQA attention (bf16 KV cache).
+//
+// Row j of request b (all nq/nkv query heads of one kv head packed as
+// rows j*G + g) attends to cache entries 0 .. S_b + j; scores are scaled by
+// 1/sqrt(hd); softmax is online in fp32 (base-2 exponent).
+//
+// One CTA per (request, kv head, entry split). KV pages are TMA-staged into
+// shared memory: a tile is 64 cache entries = 4 pages; each page of one kv
+// head is loaded as 128-byte-swizzled boxes [16 entries x 64 dims] (two per
+// page at hd = 128). QK^T and PV run on mma.sync m16n8k16 (bf16 in, fp32
+// accumulate), one 16-row query tile per warp, K fragments read with
+// ldmatrix and V fragments with ldmatrix.trans from the swizzled tiles.
+// Splits of one (request, kv head) are combined by the last CTA to arrive, in
+// split order, from fp32 partials (unnormalised output, running max, sum).
+#include <cfloat>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTile = 64;          // cache entries per tile (4 pages)
+constexpr int kStages = 3;
+constexpr int kBoxBytes = 16 * 128;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte offset of (entry e, 8-element chunk c) inside a [64 x HD] tile made of
+// HD/64 sub-tiles [64 entries x 128 B] with the 128-byte swizzle.
+template <int HD>
+__device__ __forceinline__ uint32_t tile_off(int e, int c) {
+    const int sub = c >> 3;
+    const int cw = c & 7;
+    return static_cast<uint32_t>(sub * (kTile * 128) + e * 128 + ((cw ^ (e & 7)) << 4));
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    constexpr int kTileBytes = kTile * HD * 2;     // one of K or V
+    constexpr int kSub = HD / 64;                  // 128-byte sub-tiles per entry row
+    constexpr int kNT = HD / 8;                    // n-tiles of the output
+    constexpr int kKS = HD / 16;                   // k-steps of QK^T
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sK = smem;
+    uint8_t* sV = smem + kStages * kTileBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sV + kStages * kTileBytes);
+    __shared__ int s_last;
+
+    const int pair = blockIdx.x;
+    const int b = pair / p.nkv;
+    const int kvh = pair - b * p.nkv;
+    const int split = blockIdx.y;
+    const int G = p.nq / p.nkv;
+    const int K = p.K;
+    const int Rq = K * G;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gid = lane >> 2, tig = lane & 3;
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    const size_t row_stride = static_cast<size_t>(p.nq) * HD;
+
+    pdl_launch_dependents();
+    pdl_wait();
+
+    if (p.status[b] != PE_REQ_OK) {
+        if (split == 0) {
+            for (int idx = tid; idx < Rq * HD; idx += kThreads) {
+                const int qr = idx / HD, d = idx - (idx / HD) * HD;
+                const int j = qr / G, g = qr - j * G;
+                out[static_cast<size_t>(b * K + j) * row_stride + static_cast<size_t>(kvh * G + g) * HD + d] =
+                    __float2bfloat16_rn(0.f);
+            }
+        }
+        return;
+    }
+    const int S = p.seq_lens[b];
+    const int total = S + K;
+    const int nsplit = (total + p.chunk - 1) / p.chunk;
+    if (split >= nsplit) return;
+    const int e0 = split * p.chunk;
+    const int e1 = min(total, e0 + p.chunk);
+    const int n_tiles = (e1 - e0 + kTile - 1) / kTile;
+    const int32_t* pt = p.page_table + static_cast<size_t>(b) * p.max_pages;
+    const int last_page = (total - 1) >> 4;       // last page index holding a valid entry
+
+    if (tid == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const uint64_t pol = l2_policy_evict_first();
+    auto issue = [&](int t) {   // thread 0 only
+        const int st = t % kStages;
+        mbar_arrive_expect_tx(&full[st], 2u * kTileBytes);
+        const int pbase = (e0 + t * kTile) >> 4;
+        for (int pg = 0; pg < kTile / 16; ++pg) {
+            const int pi = pbase + pg;
+            // pages past the request's last entry load as zeros (negative,
+            // out-of-range page coordinate)
+            const int pc = pi <= last_page ? pt[pi] + p.layer_page0 : -1;
+            for (int sb = 0; sb < kSub; ++sb) {
+                const uint32_t off = static_cast<uint32_t>(sb * (kTile * 128) + pg * kBoxBytes);
+                tma_load_4d(sK + st * kTileBytes + off, &tmK, &full[st], sb * 64, 0, kvh, pc, pol);
+                tma_load_4d(sV + st * kTileBytes + off, &tmV, &full[st], sb * 64, 0, kvh, pc, pol);
+            }
+        }
+    };
+    if (tid == 0)
+        for (int t = 0; t < min(kStages, n_tiles); ++t) issue(t);
+
+    // this warp's 16 query rows (packed j*G + g); rows >= Rq are padding
+    const int n_mt = (Rq + 15) >> 4;
+    const bool active = warp < n_mt;
+    const int r_lo = warp * 16 + gid;
+    const int r_hi = r_lo + 8;
+    const int j_lo = r_lo / G, j_hi = r_hi / G;
+    uint32_t qa[kKS][4];
+    if (active) {
+#pragma unroll
+        for (int kk = 0; kk < kKS; ++kk) {
+#pragma unroll
+            for (int hv = 0; hv < 2; ++hv) {           // hv = 0: k lo half, 1: k hi half
+                const int d = kk * 16 + hv * 8 + tig * 2;
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {       // rr = 0: row g, 1: row g + 8
+                    const int r = rr ? r_hi : r_lo;
+                    uint32_t v = 0u;
+                    if (r < Rq) {
+                        const int j = r / G, g = r - (r / G) * G;
+                        v = *reinterpret_cast<const uint32_t*>(
+                            q + static_cast<size_t>(b * K + j) * row_stride + static_cast<size_t>(kvh * G + g) * HD + d);
+                    }
+                    qa[kk][hv * 2 + rr] = v;
+                }
+            }
+        }
+    }
+
+    float o[kNT][4];
+#pragma unroll
+    for (int i = 0; i < kNT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    const float sl2 = rsqrtf(static_cast<float>(HD)) * 1.4426950408889634f;
+    const int lim_lo = S + j_lo, lim_hi = S + j_hi;   // last visible entry per row
+
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % kStages;
+        if (!mbar_wait(&full[st], static_cast<uint32_t>((t / kStages) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT)) ok = false;
+        const int tbase = e0 + t * kTile;
+        if (active && ok) {
+            const uint32_t kb = smem_u32(sK + st * kTileBytes);
+            const uint32_t vb = smem_u32(sV + st * kTileBytes);
+            float s[8][4];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+            const int mi = lane >> 3, rr8 = lane & 7;
+#pragma unroll
+            for (int kk = 0; kk < kKS; ++kk) {
+#pragma unroll
+                for (int nt = 0; nt < 8; nt += 2) {
+                    const int e = nt * 8 + (mi >> 1) * 8 + rr8;
+                    const int c = kk * 2 + (mi & 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kb + tile_off<HD>(e, c), b0, b1, b2, b3);
+                    mma_bf16(s[nt], qa[kk], b0, b1);
+                    mma_bf16(s[nt + 1], qa[kk], b2, b3);
+                }
+            }
+            // mask + online softmax (log2 domain)
+            float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int e = tbase + nt * 8 + tig * 2 + c;
+                    const bool in = e < e1;
+                    s[nt][c] = (in && e <= lim_lo) ? s[nt][c] * sl2 : -INFINITY;
+                    s[nt][2 + c] = (in && e <= lim_hi) ? s[nt][2 + c] * sl2 : -INFINITY;
+                    mx_lo = fmaxf(mx_lo, s[nt][c]);
+                    mx_hi = fmaxf(mx_hi, s[nt][2 + c]);
+                }
+            }
+            mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+            mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+            mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+            mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+            const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+            const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+            const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+            const float corr_lo = exp2f(m_lo - base_lo), corr_hi = exp2f(m_hi - base_hi);
+            m_lo = mn_lo;
+            m_hi = mn_hi;
+            float sum_lo = 0.f, sum_hi = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                s[nt][0] = exp2f(s[nt][0] - base_lo);
+                s[nt][1] = exp2f(s[nt][1] - base_lo);
+                s[nt][2] = exp2f(s[nt][2] - base_hi);
+                s[nt][3] = exp2f(s[nt][3] - base_hi);
+                sum_lo += s[nt][0] + s[nt][1];
+                sum_hi += s[nt][2] + s[nt][3];
+            }
+            l_lo = l_lo * corr_lo + sum_lo;
+            l_hi = l_hi * corr_hi + sum_hi;
+#pragma unroll
+            for (int i = 0; i < kNT; ++i) {
+                o[i][0] *= corr_lo;
+                o[i][1] *= corr_lo;
+                o[i][2] *= corr_hi;
+                o[i][3] *= corr_hi;
+            }
+            // O += P V
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                uint32_t pa[4];
+                pa[0] = pack_bf16(s[2 * ks][0], s[2 * ks][1]);
+                pa[1] = pack_bf16(s[2 * ks][2], s[2 * ks][3]);
+                pa[2] = pack_bf16(s[2 * ks + 1][0], s[2 * ks + 1][1]);
+                pa[3] = pack_bf16(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+#pragma unroll
+                for (int np = 0; np < kNT; np += 2) {
+                    const int e = ks * 16 + (mi & 1) * 8 + rr8;
+                    const int c = np + (mi >> 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vb + tile_off<HD>(e, c), b0, b1, b2, b3);
+                    mma_bf16(o[np], pa, b0, b1);
+                    mma_bf16(o[np + 1], pa, b2, b3);
+                }
+            }
+        }
+        // all threads agree on whether every wait succeeded before reusing a stage
+        if (!__syncthreads_and(ok ? 1 : 0)) {
+            ok = false;
+            break;
+        }
+        if (tid == 0 && t + kStages < n_tiles) issue(t + kStages);
+    }
+    if (!ok) {
+        __nanosleep(100000);    // let copies still in flight land before exit
+        return;
+    }
+
+    // full row sums across the quad
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+
+    if (nsplit == 1) {
+        if (active) {
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = rr ? r_hi : r_lo;
+                if (r < Rq) {
+                    const float l = rr ? l_hi : l_lo;
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    const int j = r / G, g = r - (r / G) * G;
+                    __nv_bfloat16* dst = out + static_cast<size_t>(b * K + j) * row_stride + static_cast<size_t>(kvh * G + g) * HD;
+#pragma unroll
+                    for (int nt = 0; nt < kNT; ++nt) {
+                        const int d = nt * 8 + tig * 2;
+                        *reinterpret_cast<__nv_bfloat162*>(dst + d) =
+                            __floats2bfloat162_rn(o[nt][rr * 2] * inv, o[nt][rr * 2 + 1] * inv);
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // split partials: [pair][split][Rq][HD + 2] = (unnormalised o..., m (log2), l)
+    constexpr int kRec = HD + 2;
+    float* mine = p.ws + (static_cast<size_t>(pair) * p.max_splits + split) * Rq * kRec;
+    if (active) {
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int r = rr ? r_hi : r_lo;
+            if (r < Rq) {
+                float* rec = mine + static_cast<size_t>(r) * kRec;
+#pragma unroll
+                for (int nt = 0; nt < kNT; ++nt) {
+                    const int d = nt * 8 + tig * 2;
+                    __stcg(reinterpret_cast<float2*>(rec + d), make_float2(o[nt][rr * 2], o[nt][rr * 2 + 1]));
+                }
+                if (tig == 0) {
+                    __stcg(rec + HD, rr ? m_hi : m_lo);
+                    __stcg(rec + HD + 1, rr ? l_hi : l_lo);
+                }
+            }
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int old = atomicAdd(p.tickets + pair, 1);
+        s_last = (old == nsplit - 1) ? 1 : 0;
+        if (s_last) atomicExch(p.tickets + pair, 0);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const float* base = p.ws + static_cast<size_t>(pair) * p.max_splits * Rq * kRec;
+    // every thread combines (row, dim pair) items in split order
+    for (int item = tid; item < Rq * (HD / 2); item += kThreads) {
+        const int r = item / (HD / 2);
+        const int d = (item - r * (HD / 2)) * 2;
+        float M = -INFINITY;
+        for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(base + (static_cast<size_t>(s) * Rq + r) * kRec + HD));
+        float den = 0.f, n0 = 0.f, n1 = 0.f;
+        for (int s = 0; s < nsplit; ++s) {
+            const float* rec = base + (static_cast<size_t>(s) * Rq + r) * kRec;
+            const float ls = __ldcg(rec + HD + 1);
+            if (ls <= 0.f) continue;
+            const float w = exp2f(__ldcg(rec + HD) - M);
+            const float2 ov = __ldcg(reinterpret_cast<const float2*>(rec + d));
+            den = fmaf(ls, w, den);
+            n0 = fmaf(w, ov.x, n0);
+            n1 = fmaf(w, ov.y, n1);
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        const int j = r / G, g = r - (r / G) * G;
+        __nv_bfloat16* dst = out + static_cast<size_t>(b * K + j) * row_stride + static_cast<size_t>(kvh * G + g) * HD + d;
+        *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(n0 * inv, n1 * inv);
+    }
+}
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+template <int HD>
+int launch_hd(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, cudaStream_t s, bool pdl) {
+    const size_t smem = 2 * kStages * static_cast<size_t>(kTile) * HD * 2 + kStages * 8 + 1024;
+    auto kern = k_attn_tc<HD>;
+    static size_t smem_set[64] = {};
+    int dev = 0;
+    PE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64 || smem > smem_set[dev]) {
+        PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+        if (dev >= 0 && dev < 64) smem_set[dev] = smem;
+    }
+    PE_CUDA_TRY(launch_ex(kern, dim3(p.B * p.nkv, p.max_splits), dim3(kThreads), smem, s, pdl, tk, tv, p));
+    return PE_OK;
+}
+
+}  // namespace
+
+AttnPlan plan_attention_tc(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms) {
+    AttnPlan a{};
+    const int max_entries = max_pages * page_size;
+    const int pairs = B * nkv;
+    const int want = ceil_div(num_sms, pairs);           // about one wave of CTAs
+    int chunk = ceil_div(ceil_div(max_entries, want), kTile) * kTile;
+    if (chunk < 2 * kTile) chunk = 2 * kTile;
+    a.chunk = chunk;
+    a.max_splits = ceil_div(max_entries, chunk);
+    const int Rq = K * (nq / nkv);
+    a.ws_floats = a.max_splits > 1 ? static_cast<size_t>(pairs) * a.max_splits * Rq * (hd + 2) : 0;
+    a.tickets = pairs;
+    return a;
+}
+
+int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, cudaStream_t s,
+                        bool pdl) {
+    if (p.hd == 128) return launch_hd<128>(tk, tv, p, s, pdl);
+    if (p.hd == 64) return launch_hd<64>(tk, tv, p, s, pdl);
+    set_error("attention: head_dim must be 64 or 128");
+    return PE_ERR_UNSUPPORTED;
+}
+
+}  // namespace pe

@@ -266,27 +266,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_acc = *tmem_slot;
 
     pdl_launch_dependents();
-    pdl_wait();
+    // Everything but the producer waits here for the previous kernel in the
+    // stream (a no-op without programmatic dependent launch).
+    if (warp != 0) pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_x = l2_policy_evict_last();
             constexpr int kBK = kRowBytes / static_cast<int>(sizeof(T));
-            int s = 0;
-            uint32_t ph = 0;
-            for (int kb = kb0; kb < kb1; ++kb) {
+            auto load_a = [&](int st, int kb) {
+                uint8_t* a_dst = sA + static_cast<size_t>(st) * kABytes;
+                if constexpr (EPI == EPI_SWIGLU) {
+                    tma_load_2d(a_dst, &tmA, &full[st], kb * kBK, m_tile * 64, pol_w);
+                    tma_load_2d(a_dst + kABytes / 2, &tmA2, &full[st], kb * kBK, m_tile * 64, pol_w);
+                } else {
+                    tma_load_2d(a_dst, &tmA, &full[st], kb * kBK, m_tile * kBM, pol_w);
+                }
+            };
+            auto load_b = [&](int st, int kb) {
+                tma_load_2d(sB + static_cast<size_t>(st) * b_bytes, &tmB, &full[st], kb * kBK, n_tile * bn, pol_x);
+            };
+            // Weights do not depend on earlier kernels: start streaming the
+            // weight tiles of the first stages before the dependency wait,
+            // then add the token tiles of those stages.
+            const int pre = min(stages, kb1 - kb0);
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full[i], kABytes + b_bytes);
+                load_a(i, kb0 + i);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i) load_b(i, kb0 + i);
+            int s = pre % stages;
+            uint32_t ph = (pre == stages) ? 1u : 0u;
+            for (int kb = kb0 + pre; kb < kb1; ++kb) {
                 if (!mbar_wait(&empty[s], ph ^ 1u, p.err, PE_DEVERR_GEMM_TIMEOUT)) break;
                 mbar_arrive_expect_tx(&full[s], kABytes + b_bytes);
-                const int kx = kb * kBK;
-                uint8_t* a_dst = sA + static_cast<size_t>(s) * kABytes;
-                if constexpr (EPI == EPI_SWIGLU) {
-                    tma_load_2d(a_dst, &tmA, &full[s], kx, m_tile * 64, pol_w);
-                    tma_load_2d(a_dst + kABytes / 2, &tmA2, &full[s], kx, m_tile * 64, pol_w);
-                } else {
-                    tma_load_2d(a_dst, &tmA, &full[s], kx, m_tile * kBM, pol_w);
-                }
-                tma_load_2d(sB + static_cast<size_t>(s) * b_bytes, &tmB, &full[s], kx, n_tile * bn, pol_x);
+                load_a(s, kb);
+                load_b(s, kb);
                 if (++s == stages) {
                     s = 0;
                     ph ^= 1u;
@@ -339,8 +356,14 @@ template <typename T, int EPI>
 int launch_typed(const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B, const GemmPlan& plan,
                  const GemmParams& p, cudaStream_t stream, bool pdl) {
     auto kern = k_gemm<T, EPI>;
-    PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(plan.smem_bytes)));
+    static size_t smem_set[64] = {};
+    int dev = 0;
+    PE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64 || plan.smem_bytes > smem_set[dev]) {
+        PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(plan.smem_bytes)));
+        if (dev >= 0 && dev < 64) smem_set[dev] = plan.smem_bytes;
+    }
     PE_CUDA_TRY(launch_ex(kern, dim3(plan.units), dim3(kThreads), plan.smem_bytes, stream, pdl, A, A2, B, p));
     return PE_OK;
 }

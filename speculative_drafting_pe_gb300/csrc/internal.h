@@ -109,7 +109,8 @@ int launch_argmax_finalize(const unsigned long long* amax, const int32_t* status
 struct AttnParams {
     int B, K, nq, nkv, hd, max_pages, num_pages, page_size;
     int chunk;        // cache entries per split
-    int max_splits;   // grid.z
+    int max_splits;   // grid.y
+    int layer_page0;  // layer * num_pages: first page of this layer in the 4-D KV tensor map
     const void* q;            // [R, nq*hd] T (rotated)
     const void* k_cache;      // this layer
     const void* v_cache;
@@ -128,6 +129,10 @@ struct AttnPlan {
 };
 AttnPlan plan_attention(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms);
 int launch_attention(int dtype, const AttnParams& p, cudaStream_t s, bool pdl);
+// bf16 tensor-core variant; tk / tv are 4-D maps {hd, 16, nkv, 4 * num_pages}
+AttnPlan plan_attention_tc(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms);
+int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, cudaStream_t s, bool pdl);
+int encode_tmap_kv(CUtensorMap* map, const void* cache, int hd, int nkv, int num_pages);
 
 // ---------------------------------------------------------------- verify
 

@@ -109,6 +109,35 @@ int encode_tmap_2d(CUtensorMap* map, const void* base, int dtype, uint64_t inner
     return PE_OK;
 }
 
+// bf16 paged KV cache [4][num_pages][nkv][16][hd] as a 4-D tensor
+// {hd, 16 slots, nkv, 4 * num_pages}; box = one page of one kv head, 64 dims
+// (128 bytes) wide, 128-byte swizzle.
+int encode_tmap_kv(CUtensorMap* map, const void* cache, int hd, int nkv, int num_pages) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (fn == nullptr) {
+        set_error("cuTensorMapEncodeTiled entry point not available");
+        return PE_ERR_CUDA;
+    }
+    if ((reinterpret_cast<uintptr_t>(cache) & 15u) != 0) {
+        set_error("KV cache must be 16-byte aligned");
+        return PE_ERR_ARG;
+    }
+    const uint64_t e = 2;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(hd), 16, static_cast<cuuint64_t>(nkv),
+                          4ull * static_cast<cuuint64_t>(num_pages)};
+    cuuint64_t strides[3] = {hd * e, 16ull * hd * e, static_cast<cuuint64_t>(nkv) * 16ull * hd * e};
+    cuuint32_t box[4] = {64, 16, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled (KV) failed with code " + std::to_string(static_cast<int>(r)));
+        return PE_ERR_CUDA;
+    }
+    return PE_OK;
+}
+
 }  // namespace pe
 
 using namespace pe;
@@ -154,8 +183,8 @@ int check_config(const pe_config& c) {
         set_error("n_q_heads*head_dim and n_kv_heads*head_dim must be multiples of 128");
         return PE_ERR_UNSUPPORTED;
     }
-    if (c.hidden % 64 != 0 || c.ffn % 64 != 0 || c.hidden <= 0 || c.ffn <= 0) {
-        set_error("hidden and ffn must be positive multiples of 64");
+    if (c.hidden % 64 != 0 || c.ffn % 64 != 0 || c.hidden <= 0 || c.ffn <= 0 || c.hidden > 8192) {
+        set_error("hidden and ffn must be positive multiples of 64, hidden <= 8192");
         return PE_ERR_UNSUPPORTED;
     }
     if (c.vocab <= 0) { set_error("vocab must be positive"); return PE_ERR_ARG; }
@@ -224,7 +253,7 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
     h->max_rows = max_batch * cfg->k_max;
     h->elem = cfg->dtype == PE_DTYPE_BF16 ? 2 : 4;
     const char* pdl_env = std::getenv("PE_PDL");
-    h->pdl = pdl_env != nullptr && pdl_env[0] == '1';
+    h->pdl = !(pdl_env != nullptr && pdl_env[0] == '0');
     if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
         free_handle(h);
         set_error("cudaDeviceGetAttribute failed");
@@ -368,7 +397,9 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     const GemmPlan p_gu = plan_gemm(F, R, H, EPI_SWIGLU, eb, h->num_sms);
     const GemmPlan p_down = plan_gemm(H, R, F, EPI_RESID, eb, h->num_sms);
     const GemmPlan p_lm = plan_gemm(V, R, H, EPI_ARGMAX, eb, h->num_sms);
-    const AttnPlan p_at = plan_attention(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms);
+    const bool attn_tc = dt == PE_DTYPE_BF16;
+    const AttnPlan p_at = attn_tc ? plan_attention_tc(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms)
+                                  : plan_attention(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms);
     if (p_at.ws_floats > h->attn_ws_floats) { set_error("attention scratch too small for this max_pages"); return PE_ERR_ARG; }
 
     CUtensorMap tm_th, tm_u, tm_xn, tm_attn, tm_act;
@@ -378,6 +409,11 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     if ((rc = act_map(h, &tm_xn, h->xn, R, H, bn_rows)) != PE_OK) return rc;
     if ((rc = act_map(h, &tm_attn, h->attn, R, qd, bn_rows)) != PE_OK) return rc;
     if ((rc = act_map(h, &tm_act, h->act, R, F, bn_rows)) != PE_OK) return rc;
+    CUtensorMap tm_kc, tm_vc;
+    if (attn_tc) {
+        if ((rc = encode_tmap_kv(&tm_kc, k_cache, hd, nkv, num_pages)) != PE_OK) return rc;
+        if ((rc = encode_tmap_kv(&tm_vc, v_cache, hd, nkv, num_pages)) != PE_OK) return rc;
+    }
 
     GemmParams base{};
     base.N = R;
@@ -448,7 +484,11 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
             ap.chunk = p_at.chunk; ap.max_splits = p_at.max_splits;
             ap.q = h->q; ap.k_cache = kc; ap.v_cache = vc; ap.page_table = page_table; ap.seq_lens = seq_lens;
             ap.status = status; ap.out = h->attn; ap.ws = h->attn_ws; ap.tickets = h->attn_tickets; ap.err = h->err;
-            if ((rc = run(PE_KERNEL_ATTENTION, [&] { return launch_attention(dt, ap, s, pdl); })) != PE_OK) return rc;
+            ap.layer_page0 = l * num_pages;
+            rc = run(PE_KERNEL_ATTENTION, [&] {
+                return attn_tc ? launch_attention_tc(tm_kc, tm_vc, ap, s, pdl) : launch_attention(dt, ap, s, pdl);
+            });
+            if (rc != PE_OK) return rc;
         }
         {   // a5: O projection + residual
             GemmParams p = base;
@@ -580,6 +620,75 @@ int pe_linear(int32_t dtype, int32_t M, int32_t N, int32_t Kd, const void* w, co
     GemmParams p{};
     p.M = M; p.N = N; p.Kd = Kd; p.out_f32 = y; p.ld_out = M; p.ws = ws; p.tickets = tickets; p.err = nullptr;
     return launch_gemm(dtype, EPI_STORE, ta, ta, tb, g, p, static_cast<cudaStream_t>(stream), false);
+}
+
+struct pe_step_graph {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    int launches = 0;
+};
+
+int pe_step_graph_create(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, const void* target_hidden,
+                         const int32_t* positions, const int32_t* seq_lens, const int32_t* page_table,
+                         int32_t max_pages, int32_t num_pages, void* k_cache, void* v_cache, int32_t* drafts,
+                         int32_t* draft_status, const int32_t* target_tokens, int32_t* positions_out,
+                         int32_t* seq_lens_out, int32_t* accepted, int32_t* bonus, int32_t* emitted,
+                         int32_t* slot_mapping, int32_t* rollback_slots, int32_t* verify_status,
+                         pe_step_graph** out) {
+    if (h == nullptr || out == nullptr) { set_error("null argument"); return PE_ERR_ARG; }
+    *out = nullptr;
+    PE_CUDA_TRY(cudaSetDevice(h->device));
+    cudaStream_t cs = nullptr;
+    PE_CUDA_TRY(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+    const int saved_prof = h->prof_kind;
+    h->prof_kind = -1;   // no profiling events inside a graph
+    cudaError_t ce = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    int rc = ce == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+    if (rc == PE_OK)
+        rc = pe_draft(h, B, K, last_token, target_hidden, positions, seq_lens, page_table, max_pages, num_pages,
+                      k_cache, v_cache, drafts, nullptr, draft_status, cs);
+    const int n_draft = h->last_launches;
+    if (rc == PE_OK)
+        rc = pe_verify_rebuild(h, B, K, drafts, target_tokens, page_table, max_pages, num_pages, positions, seq_lens,
+                               positions_out, seq_lens_out, accepted, bonus, emitted, slot_mapping, rollback_slots,
+                               verify_status, cs);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ee = cudaStreamEndCapture(cs, &graph);
+    h->prof_kind = saved_prof;
+    cudaStreamDestroy(cs);
+    if (rc != PE_OK || ee != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        if (rc == PE_OK) set_error(std::string("graph capture failed: ") + cudaGetErrorString(ee));
+        return rc == PE_OK ? PE_ERR_CUDA : rc;
+    }
+    cudaGraphExec_t exec = nullptr;
+    const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
+    if (ie != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        set_error(std::string("cudaGraphInstantiate: ") + cudaGetErrorString(ie));
+        return PE_ERR_CUDA;
+    }
+    pe_step_graph* g = new pe_step_graph();
+    g->graph = graph;
+    g->exec = exec;
+    g->launches = n_draft + 1;
+    *out = g;
+    return PE_OK;
+}
+
+int pe_step_graph_launch(pe_step_graph* g, void* stream) {
+    if (g == nullptr) { set_error("null graph"); return PE_ERR_ARG; }
+    PE_CUDA_TRY(cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream)));
+    return PE_OK;
+}
+
+int pe_step_graph_launch_count(const pe_step_graph* g) { return g ? g->launches : 0; }
+
+void pe_step_graph_destroy(pe_step_graph* g) {
+    if (g == nullptr) return;
+    if (g->exec) cudaGraphExecDestroy(g->exec);
+    if (g->graph) cudaGraphDestroy(g->graph);
+    delete g;
 }
 
 }  // extern "C"

@@ -30,8 +30,31 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return t;
 }
 
-// Status of request b: capacity, page indices of entries 0..S+K-1, inputs.
-__device__ int request_status(const RowBuildParams& p, int b, float* red_unused) {
+// 4-element vector load / store of the config dtype as float4.
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+__device__ __forceinline__ float dot4(float4 a) { return a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w; }
+__device__ __forceinline__ float4 scale4(float4 a, float s, float4 g) {
+    return make_float4(a.x * s * g.x, a.y * s * g.y, a.z * s * g.z, a.w * s * g.w);
+}
+
+constexpr int kMaxG = 8;   // 4-element groups per thread: H <= 4 * 8 * 256
+
+// Status of request b: inputs, capacity, page indices of entries 0..S+K-1.
+__device__ int request_status(const RowBuildParams& p, int b) {
     const int S = p.seq_lens[b];
     const int tok = p.last_token[b];
     const int Q = p.positions[b];
@@ -50,49 +73,70 @@ __device__ int request_status(const RowBuildParams& p, int b, float* red_unused)
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams p) {
     __shared__ float red[32];
-    pdl_launch_dependents();
-    pdl_wait();
     const int r = blockIdx.x;
     const int b = r / p.K;
     const int j = r - b * p.K;
     const int H = p.H;
-    const int st = request_status(p, b, red);
-    if (j == 0 && threadIdx.x == 0) p.status[b] = st;
-    if (threadIdx.x == 0) p.amax[r] = 0ull;
-
+    const int ng = H / 4;
+    const int tid = threadIdx.x;
+    // weights (independent of earlier kernels) are read before the dependency wait
+    float4 ge[kMaxG], gh[kMaxG], ev[kMaxG], hv[kMaxG];
+#pragma unroll
+    for (int i = 0; i < kMaxG; ++i) {
+        const int g = tid + i * kRowThreads;
+        if (g < ng) {
+            ge[i] = load4(static_cast<const T*>(p.norm_e) + 4 * g);
+            gh[i] = load4(static_cast<const T*>(p.norm_h) + 4 * g);
+            if (j > 0) {
+                ev[i] = load4(static_cast<const T*>(p.emb_mask) + 4 * g);
+                hv[i] = load4(static_cast<const T*>(p.h_shared) + 4 * g);
+            }
+        }
+    }
+    pdl_launch_dependents();
+    pdl_wait();
+    const int st = request_status(p, b);
+    const bool ok = st == PE_REQ_OK;
+    if (j == 0 && tid == 0) p.status[b] = st;
+    if (tid == 0) p.amax[r] = 0ull;
+    if (j == 0) {
+        const T* emb = static_cast<const T*>(p.embed) + static_cast<size_t>(ok ? p.last_token[b] : 0) * H;
+        const float* h0 = p.h + static_cast<size_t>(b) * H;
+#pragma unroll
+        for (int i = 0; i < kMaxG; ++i) {
+            const int g = tid + i * kRowThreads;
+            if (g < ng) {
+                ev[i] = load4(emb + 4 * g);
+                hv[i] = load4(h0 + 4 * g);
+            }
+        }
+    }
+    float ss_e = 0.f, ss_h = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxG; ++i) {
+        if (tid + i * kRowThreads < ng) {
+            ss_e += dot4(ev[i]);
+            ss_h += dot4(hv[i]);
+        }
+    }
+    const float inv_e = ok ? rsqrtf(block_sum(ss_e, red) / H + p.eps) : 0.f;
+    const float inv_h = ok ? rsqrtf(block_sum(ss_h, red) / H + p.eps) : 0.f;
     T* u = static_cast<T*>(p.u) + static_cast<size_t>(r) * 2 * H;
     float* resid = p.resid + static_cast<size_t>(r) * H;
-    const T* emb;
-    if (j == 0) emb = static_cast<const T*>(p.embed) + static_cast<size_t>(st == PE_REQ_OK ? p.last_token[b] : 0) * H;
-    else emb = static_cast<const T*>(p.emb_mask);
-    const T* ge = static_cast<const T*>(p.norm_e);
-    const T* gh = static_cast<const T*>(p.norm_h);
-    const T* hsh = static_cast<const T*>(p.h_shared);
-    const float* h0 = p.h + static_cast<size_t>(b) * H;
-
-    float ss_e = 0.f, ss_h = 0.f;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) {
-        const float e = Elem<T>::to_f(emb[i]);
-        const float hv = (j == 0) ? h0[i] : Elem<T>::to_f(hsh[i]);
-        ss_e += e * e;
-        ss_h += hv * hv;
-    }
-    const float tot_e = block_sum(ss_e, red);
-    const float tot_h = block_sum(ss_h, red);
-    const float inv_e = rsqrtf(tot_e / H + p.eps);
-    const float inv_h = rsqrtf(tot_h / H + p.eps);
-    for (int i = threadIdx.x; i < H; i += blockDim.x) {
-        const float e = Elem<T>::to_f(emb[i]);
-        const float hv = (j == 0) ? h0[i] : Elem<T>::to_f(hsh[i]);
-        const bool ok = st == PE_REQ_OK;
-        u[i] = Elem<T>::from_f(ok ? e * inv_e * Elem<T>::to_f(ge[i]) : 0.f);
-        u[H + i] = Elem<T>::from_f(ok ? hv * inv_h * Elem<T>::to_f(gh[i]) : 0.f);
-        resid[i] = ok ? hv : 0.f;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kMaxG; ++i) {
+        const int g = tid + i * kRowThreads;
+        if (g < ng) {
+            store4(u + 4 * g, scale4(ev[i], inv_e, ge[i]));
+            store4(u + H + 4 * g, scale4(hv[i], inv_h, gh[i]));
+            store4(resid + 4 * g, ok ? hv[i] : zero);
+        }
     }
 
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         int slot = -1;
-        if (st == PE_REQ_OK) {
+        if (ok) {
             const int e = p.seq_lens[b] + j;
             const int pg = p.page_table[static_cast<size_t>(b) * p.max_pages + e / p.page_size];
             slot = pg * p.page_size + e % p.page_size;
@@ -102,14 +146,14 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
     // RoPE table for this row: angle = (Q_b + j) * inv_freq_i in double,
     // reduced to [-pi, pi] in double, then sin/cos in float.
     const int half = p.hd / 2;
-    const double pos = static_cast<double>(st == PE_REQ_OK ? p.positions[b] + j : 0);
-    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    const double pos = static_cast<double>(ok ? p.positions[b] + j : 0);
+    for (int i = tid; i < half; i += blockDim.x) {
         const double a = pos * p.inv_freq[i];
         const double two_pi = 6.283185307179586476925286766559;
         const double red_a = a - two_pi * rint(a / two_pi);
-        float s, c;
-        sincosf(static_cast<float>(red_a), &s, &c);
-        p.rope_cs[static_cast<size_t>(r) * half + i] = make_float2(c, s);
+        float sn, cs;
+        sincosf(static_cast<float>(red_a), &sn, &cs);
+        p.rope_cs[static_cast<size_t>(r) * half + i] = make_float2(cs, sn);
     }
 }
 
@@ -117,15 +161,34 @@ template <typename T>
 __global__ void __launch_bounds__(kRowThreads)
     k_rmsnorm(const float* __restrict__ x, const T* __restrict__ gain, T* __restrict__ out, int H, float eps) {
     __shared__ float red[32];
+    const int r = blockIdx.x;
+    const int ng = H / 4;
+    const int tid = threadIdx.x;
+    float4 g4[kMaxG], x4[kMaxG];
+#pragma unroll
+    for (int i = 0; i < kMaxG; ++i) {
+        const int g = tid + i * kRowThreads;
+        if (g < ng) g4[i] = load4(gain + 4 * g);      // weights: before the dependency wait
+    }
     pdl_launch_dependents();
     pdl_wait();
-    const int r = blockIdx.x;
     const float* xr = x + static_cast<size_t>(r) * H;
     float ss = 0.f;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) ss += xr[i] * xr[i];
+#pragma unroll
+    for (int i = 0; i < kMaxG; ++i) {
+        const int g = tid + i * kRowThreads;
+        if (g < ng) {
+            x4[i] = load4(xr + 4 * g);
+            ss += dot4(x4[i]);
+        }
+    }
     const float inv = rsqrtf(block_sum(ss, red) / H + eps);
     T* o = out + static_cast<size_t>(r) * H;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) o[i] = Elem<T>::from_f(xr[i] * inv * Elem<T>::to_f(gain[i]));
+#pragma unroll
+    for (int i = 0; i < kMaxG; ++i) {
+        const int g = tid + i * kRowThreads;
+        if (g < ng) store4(o + 4 * g, scale4(x4[i], inv, g4[i]));
+    }
 }
 
 __global__ void k_argmax_finalize(const unsigned long long* __restrict__ amax, const int32_t* __restrict__ status,
