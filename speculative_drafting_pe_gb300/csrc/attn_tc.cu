@@ -10,8 +10,11 @@
 // page at hd = 128). QK^T and PV run on mma.sync m16n8k16 (bf16 in, fp32
 // accumulate), one 16-row query tile per warp, K fragments read with
 // ldmatrix and V fragments with ldmatrix.trans from the swizzled tiles.
-// Splits of one (request, kv head) are combined by the last CTA to arrive, in
-// split order, from fp32 partials (unnormalised output, running max, sum).
+// The entry splits of one (request, kv head) form one thread-block cluster:
+// each CTA leaves its fp32 partial (unnormalised output, running max, sum) in
+// its own shared memory, and after a cluster barrier every CTA combines a
+// slice of the rows by reading its peers' partials through distributed shared
+// memory, in split order. No global scratch is used.
 #include <cfloat>
 
 #include "common.cuh"
@@ -21,10 +24,11 @@ namespace pe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 constexpr int kTile = 64;          // cache entries per tile (4 pages)
 constexpr int kStages = 3;
 constexpr int kBoxBytes = 16 * 128;
+constexpr int kMaxRq = 128;        // K * nq/nkv query rows per kv head
+constexpr int kMaxCluster = 8;     // portable cluster size
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -69,7 +73,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sK = smem;
     uint8_t* sV = smem + kStages * kTileBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(sV + kStages * kTileBytes);
-    __shared__ int s_last;
+    __shared__ float s_m[kMaxRq], s_l[kMaxRq];   // per-row running max (log2) and sum of this split
 
     const int pair = blockIdx.x;
     const int b = pair / p.nkv;
@@ -87,24 +91,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
     pdl_wait();
 
-    if (p.status[b] != PE_REQ_OK) {
-        if (split == 0) {
-            for (int idx = tid; idx < Rq * HD; idx += kThreads) {
-                const int qr = idx / HD, d = idx - (idx / HD) * HD;
-                const int j = qr / G, g = qr - j * G;
-                out[static_cast<size_t>(b * K + j) * row_stride + static_cast<size_t>(kvh * G + g) * HD + d] =
-                    __float2bfloat16_rn(0.f);
-            }
-        }
-        return;
-    }
-    const int S = p.seq_lens[b];
+    // Every CTA of a cluster runs to the end (cluster barriers); CTAs without
+    // work simply contribute an empty partial.
+    const int C = gridDim.y;                 // cluster size = entry splits per (request, kv head)
+    const bool req_ok = p.status[b] == PE_REQ_OK;
+    const int S = req_ok ? p.seq_lens[b] : 0;
     const int total = S + K;
-    const int nsplit = (total + p.chunk - 1) / p.chunk;
-    if (split >= nsplit) return;
     const int e0 = split * p.chunk;
-    const int e1 = min(total, e0 + p.chunk);
-    const int n_tiles = (e1 - e0 + kTile - 1) / kTile;
+    const int e1 = req_ok ? min(total, e0 + p.chunk) : e0;
+    const int n_tiles = e1 > e0 ? (e1 - e0 + kTile - 1) / kTile : 0;
     const int32_t* pt = p.page_table + static_cast<size_t>(b) * p.max_pages;
     const int last_page = (total - 1) >> 4;       // last page index holding a valid entry
 
@@ -143,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r_hi = r_lo + 8;
     const int j_lo = r_lo / G, j_hi = r_hi / G;
     uint32_t qa[kKS][4];
-    if (active) {
+    if (active && n_tiles > 0) {
 #pragma unroll
         for (int kk = 0; kk < kKS; ++kk) {
 #pragma unroll
@@ -264,25 +259,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (tid == 0 && t + kStages < n_tiles) issue(t + kStages);
     }
-    if (!ok) {
-        __nanosleep(100000);    // let copies still in flight land before exit
-        return;
-    }
+    if (!ok) __nanosleep(100000);    // a wait gave up: let copies still in flight land
 
     // full row sums across the quad
     l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
     l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
     l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
     l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+    if (!ok) l_lo = l_hi = 0.f;
 
-    if (nsplit == 1) {
+    if (C == 1) {
         if (active) {
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
                 const int r = rr ? r_hi : r_lo;
                 if (r < Rq) {
                     const float l = rr ? l_hi : l_lo;
-                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    const float inv = (req_ok && l > 0.f) ? 1.f / l : 0.f;
                     const int j = r / G, g = r - (r / G) * G;
                     __nv_bfloat16* dst = out + static_cast<size_t>(b * K + j) * row_stride + static_cast<size_t>(kvh * G + g) * HD;
 #pragma unroll
@@ -297,60 +290,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
-    // split partials: [pair][split][Rq][HD + 2] = (unnormalised o..., m (log2), l)
-    constexpr int kRec = HD + 2;
-    float* mine = p.ws + (static_cast<size_t>(pair) * p.max_splits + split) * Rq * kRec;
+    // Split partial into this CTA's shared memory. The KV stage buffers are
+    // free again (every tile was consumed before the last block barrier).
+    float* s_o = reinterpret_cast<float*>(smem);      // [Rq][HD]
     if (active) {
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
             const int r = rr ? r_hi : r_lo;
             if (r < Rq) {
-                float* rec = mine + static_cast<size_t>(r) * kRec;
 #pragma unroll
                 for (int nt = 0; nt < kNT; ++nt) {
                     const int d = nt * 8 + tig * 2;
-                    __stcg(reinterpret_cast<float2*>(rec + d), make_float2(o[nt][rr * 2], o[nt][rr * 2 + 1]));
+                    *reinterpret_cast<float2*>(s_o + r * HD + d) = make_float2(o[nt][rr * 2], o[nt][rr * 2 + 1]);
                 }
                 if (tig == 0) {
-                    __stcg(rec + HD, rr ? m_hi : m_lo);
-                    __stcg(rec + HD + 1, rr ? l_hi : l_lo);
+                    s_m[r] = rr ? m_hi : m_lo;
+                    s_l[r] = rr ? l_hi : l_lo;
                 }
             }
         }
     }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const int old = atomicAdd(p.tickets + pair, 1);
-        s_last = (old == nsplit - 1) ? 1 : 0;
-        if (s_last) atomicExch(p.tickets + pair, 0);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    const float* base = p.ws + static_cast<size_t>(pair) * p.max_splits * Rq * kRec;
-    // every thread combines (row, dim pair) items in split order
-    for (int item = tid; item < Rq * (HD / 2); item += kThreads) {
-        const int r = item / (HD / 2);
-        const int d = (item - r * (HD / 2)) * 2;
+    cluster_sync_all();
+
+    // CTA `rank` combines rows rank, rank + C, ... from all C partials, in split order.
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t o_base = smem_u32(s_o), m_base = smem_u32(s_m), l_base = smem_u32(s_l);
+    const int my_rows = (Rq - static_cast<int>(rank) + C - 1) / C;
+    for (int item = tid; item < my_rows * (HD / 2); item += kThreads) {
+        const int r = static_cast<int>(rank) + (item / (HD / 2)) * C;
+        const int d = (item - (item / (HD / 2)) * (HD / 2)) * 2;
         float M = -INFINITY;
-        for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(base + (static_cast<size_t>(s) * Rq + r) * kRec + HD));
+        for (int sp = 0; sp < C; ++sp) M = fmaxf(M, dsmem_ld(dsmem_addr(m_base + 4u * r, sp)));
         float den = 0.f, n0 = 0.f, n1 = 0.f;
-        for (int s = 0; s < nsplit; ++s) {
-            const float* rec = base + (static_cast<size_t>(s) * Rq + r) * kRec;
-            const float ls = __ldcg(rec + HD + 1);
+        for (int sp = 0; sp < C; ++sp) {
+            const float ls = dsmem_ld(dsmem_addr(l_base + 4u * r, sp));
             if (ls <= 0.f) continue;
-            const float w = exp2f(__ldcg(rec + HD) - M);
-            const float2 ov = __ldcg(reinterpret_cast<const float2*>(rec + d));
+            const float w = exp2f(dsmem_ld(dsmem_addr(m_base + 4u * r, sp)) - M);
+            const float2 ov = dsmem_ld2(dsmem_addr(o_base + 4u * (r * HD + d), sp));
             den = fmaf(ls, w, den);
             n0 = fmaf(w, ov.x, n0);
             n1 = fmaf(w, ov.y, n1);
         }
-        const float inv = den > 0.f ? 1.f / den : 0.f;
+        const float inv = (req_ok && den > 0.f) ? 1.f / den : 0.f;
         const int j = r / G, g = r - (r / G) * G;
         __nv_bfloat16* dst = out + static_cast<size_t>(b * K + j) * row_stride + static_cast<size_t>(kvh * G + g) * HD + d;
         *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(n0 * inv, n1 * inv);
     }
+    // peers may still be reading this CTA's partial
+    cluster_sync_all();
 }
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -366,7 +353,21 @@ int launch_hd(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
         PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
         if (dev >= 0 && dev < 64) smem_set[dev] = smem;
     }
-    PE_CUDA_TRY(launch_ex(kern, dim3(p.B * p.nkv, p.max_splits), dim3(kThreads), smem, s, pdl, tk, tv, p));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.B * p.nkv, p.max_splits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = static_cast<unsigned>(p.max_splits);
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    PE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, tk, tv, p));
     return PE_OK;
 }
 
@@ -376,14 +377,16 @@ AttnPlan plan_attention_tc(int B, int K, int nq, int nkv, int hd, int max_pages,
     AttnPlan a{};
     const int max_entries = max_pages * page_size;
     const int pairs = B * nkv;
-    const int want = ceil_div(num_sms, pairs);           // about one wave of CTAs
-    int chunk = ceil_div(ceil_div(max_entries, want), kTile) * kTile;
-    if (chunk < 2 * kTile) chunk = 2 * kTile;
+    int C = ceil_div(num_sms, pairs);                    // about one wave of CTAs
+    if (C > kMaxCluster) C = kMaxCluster;
+    if (C < 1) C = 1;
+    int chunk = ceil_div(ceil_div(max_entries, C), kTile) * kTile;
+    C = ceil_div(max_entries, chunk);                    // splits actually needed
     a.chunk = chunk;
-    a.max_splits = ceil_div(max_entries, chunk);
-    const int Rq = K * (nq / nkv);
-    a.ws_floats = a.max_splits > 1 ? static_cast<size_t>(pairs) * a.max_splits * Rq * (hd + 2) : 0;
-    a.tickets = pairs;
+    a.max_splits = C;                                    // one cluster of C CTAs per (request, kv head)
+    a.ws_floats = 0;
+    a.tickets = 0;
+    (void)K; (void)nq; (void)hd;
     return a;
 }
 

@@ -196,10 +196,26 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, uint32_t tmem_acc,
             float v[kChunk];
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) v[i] = 0.f;
-            for (int s = 0; s < p.splits; ++s) {
-                const float* src = base + (static_cast<size_t>(s) * bn + c0) * kBM + ml;
+            // issue the loads of up to kGroup splits at once, then add them
+            // in split order (the sum does not depend on arrival order)
+            constexpr int kGroup = 4;
+            for (int s0 = 0; s0 < p.splits; s0 += kGroup) {
+                float t[kGroup][kChunk];
 #pragma unroll
-                for (int i = 0; i < kChunk; ++i) v[i] += __ldcg(src + static_cast<size_t>(i) * kBM);
+                for (int u = 0; u < kGroup; ++u) {
+                    if (s0 + u < p.splits) {
+                        const float* src = base + (static_cast<size_t>(s0 + u) * bn + c0) * kBM + ml;
+#pragma unroll
+                        for (int i = 0; i < kChunk; ++i) t[u][i] = __ldcg(src + static_cast<size_t>(i) * kBM);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kGroup; ++u) {
+                    if (s0 + u < p.splits) {
+#pragma unroll
+                        for (int i = 0; i < kChunk; ++i) v[i] += t[u][i];
+                    }
+                }
             }
             apply_chunk<T, EPI>(p, v, ml, m_tile, n_base + c0, stile);
         }
@@ -215,7 +231,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, uint32_t tmem_acc,
 // ------------------------------------------------------------ kernel
 
 template <typename T, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
            const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
