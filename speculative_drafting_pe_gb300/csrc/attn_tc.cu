@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sK = smem;
     uint8_t* sV = smem + kStages * kTileBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(sV + kStages * kTileBytes);
+    int* s_pages = reinterpret_cast<int*>(full + kStages);   // page coordinates of this CTA's entry range
     __shared__ float s_m[kMaxRq], s_l[kMaxRq];   // per-row running max (log2) and sum of this split
 
     const int pair = blockIdx.x;
@@ -109,18 +110,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
     }
+    // page coordinates of every tile of this CTA, read once; pages past the
+    // request's last entry get a negative (out-of-range, zero-filled) coordinate
+    const int n_pg = n_tiles * (kTile / 16);
+    const int pg0 = e0 >> 4;
+    for (int i = tid; i < n_pg; i += kThreads) {
+        const int pi = pg0 + i;
+        s_pages[i] = pi <= last_page ? pt[pi] + p.layer_page0 : -1;
+    }
     __syncthreads();
 
     const uint64_t pol = l2_policy_evict_first();
     auto issue = [&](int t) {   // thread 0 only
         const int st = t % kStages;
         mbar_arrive_expect_tx(&full[st], 2u * kTileBytes);
-        const int pbase = (e0 + t * kTile) >> 4;
         for (int pg = 0; pg < kTile / 16; ++pg) {
-            const int pi = pbase + pg;
-            // pages past the request's last entry load as zeros (negative,
-            // out-of-range page coordinate)
-            const int pc = pi <= last_page ? pt[pi] + p.layer_page0 : -1;
+            const int pc = s_pages[t * (kTile / 16) + pg];
             for (int sb = 0; sb < kSub; ++sb) {
                 const uint32_t off = static_cast<uint32_t>(sb * (kTile * 128) + pg * kBoxBytes);
                 tma_load_4d(sK + st * kTileBytes + off, &tmK, &full[st], sb * 64, 0, kvh, pc, pol);
@@ -344,7 +349,8 @@ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 template <int HD>
 int launch_hd(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, cudaStream_t s, bool pdl) {
-    const size_t smem = 2 * kStages * static_cast<size_t>(kTile) * HD * 2 + kStages * 8 + 1024;
+    const size_t smem = 2 * kStages * static_cast<size_t>(kTile) * HD * 2 + kStages * 8 +
+                        (static_cast<size_t>(p.chunk) / 16 + 4) * sizeof(int) + 1024;
     auto kern = k_attn_tc<HD>;
     static size_t smem_set[64] = {};
     int dev = 0;

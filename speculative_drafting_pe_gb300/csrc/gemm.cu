@@ -28,6 +28,7 @@ constexpr int kRowBytes = 128;               // one 128-byte swizzle row per til
 constexpr int kABytes = kBM * kRowBytes;     // 16 KB weight tile per stage
 constexpr int kChunk = 16;                   // accumulator columns per tcgen05.ld
 constexpr int kPitch = kBM + 4;              // epilogue staging row pitch (floats)
+constexpr int kMaxClusterSplits = 16;        // cluster split-K: at most 16 CTAs per tile
 
 __host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn) {
     size_t off = static_cast<size_t>(stages) * (kABytes + static_cast<size_t>(bn) * kRowBytes);
@@ -44,16 +45,19 @@ __host__ __device__ inline uint32_t tmem_cols_for(int bn) {
 
 // ------------------------------------------------------------ epilogues
 
+// Columns i of the chunk with bit i of `colmask` clear are skipped (another
+// CTA of the cluster owns them).
 template <typename T, int EPI>
 __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v)[kChunk], int ml, int m_tile,
-                                            int n0, float* stile) {
+                                            int n0, float* stile, uint32_t colmask) {
+    auto col_ok = [&](int i) { return n0 + i < p.N && ((colmask >> i) & 1u); };
     if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
         const int m = m_tile * kBM + ml;
         if (m < p.M) {
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) {
                 const int n = n0 + i;
-                if (n < p.N) {
+                if (col_ok(i)) {
                     float* dst = p.out_f32 + static_cast<size_t>(n) * p.ld_out + m;
                     if constexpr (EPI == EPI_RESID) *dst += v[i];
                     else *dst = v[i];
@@ -66,14 +70,14 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
             const int n = n0 + i;
-            if (p.logits != nullptr && valid && n < p.N) p.logits[static_cast<size_t>(n) * p.ld_logits + m] = v[i];
+            if (p.logits != nullptr && valid && col_ok(i)) p.logits[static_cast<size_t>(n) * p.ld_logits + m] = v[i];
             unsigned long long key = valid ? argmax_key(v[i], static_cast<uint32_t>(m)) : 0ull;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
                 const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
                 key = o > key ? o : key;
             }
-            if ((ml & 31) == 0 && n < p.N && key != 0ull) atomicMax(p.amax + n, key);
+            if ((ml & 31) == 0 && col_ok(i) && key != 0ull) atomicMax(p.amax + n, key);
         }
     } else if constexpr (EPI == EPI_SWIGLU) {
         // rows 0..63 of the tile are gate rows, 64..127 the matching up rows
@@ -89,7 +93,7 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
 #pragma unroll
             for (int i = ibeg; i < ibeg + kChunk / 2; ++i) {
                 const int n = n0 + i;
-                if (n < p.N) {
+                if (col_ok(i)) {
                     const float g = stile[i * kPitch + fl];
                     const float u = stile[i * kPitch + fl + 64];
                     out[static_cast<size_t>(n) * p.ld_act + f] = Elem<T>::from_f(silu_f(g) * u);
@@ -117,7 +121,7 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
             for (int i = 0; i < kChunk; ++i) {
                 const int n = n0 + i;
                 outv[i] = 0.f;
-                if (n < p.N) {
+                if (col_ok(i)) {
                     const float2 cs = p.rope_cs[static_cast<size_t>(n) * half + fi];
                     const float y = stile[i * kPitch + partner];
                     outv[i] = lo ? (v[i] * cs.x - y * cs.y) : (v[i] * cs.x + y * cs.y);
@@ -133,7 +137,7 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
 #pragma unroll
                 for (int i = 0; i < kChunk; ++i) {
                     const int n = n0 + i;
-                    if (n < p.N) q[static_cast<size_t>(n) * p.ld_act + m] = Elem<T>::from_f(outv[i]);
+                    if (col_ok(i)) q[static_cast<size_t>(n) * p.ld_act + m] = Elem<T>::from_f(outv[i]);
                 }
             } else {
                 const int r = m - p.nq_hd - (region == 2 ? p.nkv * hd : 0);
@@ -143,7 +147,7 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
 #pragma unroll
                 for (int i = 0; i < kChunk; ++i) {
                     const int n = n0 + i;
-                    if (n < p.N) {
+                    if (col_ok(i)) {
                         const int slot = p.row_slot[n];
                         if (slot >= 0) {
                             const size_t page = static_cast<size_t>(slot >> 4);
@@ -159,7 +163,8 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
 
 template <typename T, int EPI>
 __device__ __forceinline__ void epilogue(const GemmParams& p, uint32_t tmem_acc, uint64_t* tfull, float* stile,
-                                         int* sflag, int m_tile, int n_tile, int split, int warp, int lane) {
+                                         int* sflag, float* part, int m_tile, int n_tile, int split, int warp,
+                                         int lane) {
     const int quad = warp & 3;               // TMEM lane quadrant this warp may read
     const int ml = quad * 32 + lane;         // tile row = TMEM lane
     const uint32_t t_row = tmem_acc + (static_cast<uint32_t>(quad * 32) << 16);
@@ -171,7 +176,16 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, uint32_t tmem_acc,
 
     const int bn = p.bn;
     const int n_base = n_tile * bn;
-    if (p.splits > 1) {
+    if (p.splits > 1 && p.cluster) {
+        // cluster split-K: leave this split's partial tile in shared memory
+        // (the stage ring is free once the accumulator is complete)
+        for (int c0 = 0; c0 < bn; c0 += kChunk) {
+            float v[kChunk];
+            tmem_ld16(t_row + c0, v);
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) part[(c0 + i) * kBM + ml] = v[i];
+        }
+    } else if (p.splits > 1) {
         const int tile = m_tile * p.n_tiles + n_tile;
         float* mine = p.ws + (static_cast<size_t>(tile) * p.splits + split) * bn * kBM;
         for (int c0 = 0; c0 < bn; c0 += kChunk) {
@@ -217,14 +231,44 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, uint32_t tmem_acc,
                     }
                 }
             }
-            apply_chunk<T, EPI>(p, v, ml, m_tile, n_base + c0, stile);
+            apply_chunk<T, EPI>(p, v, ml, m_tile, n_base + c0, stile, 0xFFFFu);
         }
     } else {
         for (int c0 = 0; c0 < bn; c0 += kChunk) {
             float v[kChunk];
             tmem_ld16(t_row + c0, v);
-            apply_chunk<T, EPI>(p, v, ml, m_tile, n_base + c0, stile);
+            apply_chunk<T, EPI>(p, v, ml, m_tile, n_base + c0, stile, 0xFFFFu);
         }
+    }
+}
+
+// Cluster split-K, second half: after a cluster barrier, CTA `rank` sums the
+// columns c with c % splits == rank over all peers' partial tiles (read through
+// distributed shared memory, in split order) and applies the epilogue to them.
+template <typename T, int EPI>
+__device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile, const float* part, int m_tile,
+                                               int n_tile, int warp, int lane) {
+    const int ml = (warp & 3) * 32 + lane;
+    const int bn = p.bn;
+    const int C = p.splits;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t base = smem_u32(part);
+    for (int c0 = 0; c0 < bn; c0 += kChunk) {
+        float v[kChunk];
+        uint32_t mask = 0;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            v[i] = 0.f;
+            if ((c0 + i) % C == static_cast<int>(rank)) mask |= 1u << i;
+        }
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            if ((mask >> i) & 1u) {
+                const uint32_t a = base + 4u * static_cast<uint32_t>((c0 + i) * kBM + ml);
+                for (int sp = 0; sp < C; ++sp) v[i] += dsmem_ld(dsmem_addr(a, sp));
+            }
+        }
+        apply_chunk<T, EPI>(p, v, ml, m_tile, n_tile * bn + c0, stile, mask);
     }
 }
 
@@ -251,10 +295,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int unit = blockIdx.x;
-    const int n_tile = unit % p.n_tiles;
-    const int rest = unit / p.n_tiles;
-    const int split = rest % p.splits;
-    const int m_tile = rest / p.splits;
+    const int split = unit % p.splits;       // splits of one tile are adjacent (one cluster)
+    const int rest = unit / p.splits;
+    const int n_tile = rest % p.n_tiles;
+    const int m_tile = rest / p.n_tiles;
     const int kb0 = split * p.kb_per_split;
     const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
     const uint32_t tmem_cols = tmem_cols_for(bn);
@@ -351,7 +395,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncwarp();
     } else {
-        epilogue<T, EPI>(p, tmem_acc, tfull, stile, sflag, m_tile, n_tile, split, warp, lane);
+        epilogue<T, EPI>(p, tmem_acc, tfull, stile, sflag, reinterpret_cast<float*>(smem), m_tile, n_tile, split,
+                         warp, lane);
+    }
+    if (p.splits > 1 && p.cluster) {
+        __syncthreads();              // this CTA's partial is in shared memory
+        cluster_sync_all();           // ... and so are the peers'
+        if (warp >= 2 && !sflag[0])
+            cluster_reduce<T, EPI>(p, stile, reinterpret_cast<const float*>(smem), m_tile, n_tile, warp, lane);
+        cluster_sync_all();           // peers are done reading this CTA's partial
     }
 
     tc_fence_before_sync();
@@ -378,9 +430,28 @@ int launch_typed(const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap&
     if (dev < 0 || dev >= 64 || plan.smem_bytes > smem_set[dev]) {
         PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(plan.smem_bytes)));
+        PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
         if (dev >= 0 && dev < 64) smem_set[dev] = plan.smem_bytes;
     }
-    PE_CUDA_TRY(launch_ex(kern, dim3(plan.units), dim3(kThreads), plan.smem_bytes, stream, pdl, A, A2, B, p));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.units);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = plan.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    int na = 1;
+    if (p.cluster && plan.splits > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(plan.splits);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        na = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    PE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, A, A2, B, p));
     return PE_OK;
 }
 
@@ -402,7 +473,7 @@ inline int round_up(int a, int b) { return ceil_div(a, b) * b; }
 
 }  // namespace
 
-GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms) {
+GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster) {
     GemmPlan g{};
     const int bk = kRowBytes / elem_bytes;
     g.kb_total = ceil_div(Kd, bk);
@@ -416,22 +487,41 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms) {
     const int rows_per_tile = epi == EPI_SWIGLU ? 64 : kBM;
     g.m_tiles = ceil_div(M, rows_per_tile);
     g.tiles = g.m_tiles * g.n_tiles;
-    int splits = 1;
-    const int target = 2 * num_sms;
-    if (g.tiles < target && epi != EPI_ARGMAX) {
-        splits = ceil_div(target, g.tiles);
-        const int cap = g.kb_total / 4 > 1 ? g.kb_total / 4 : 1;   // >= 4 k-blocks per split
-        splits = splits < cap ? splits : cap;
-    }
-    g.kb_per_split = ceil_div(g.kb_total, splits);
-    g.splits = ceil_div(g.kb_total, g.kb_per_split);
-    g.units = g.tiles * g.splits;
+    // shared-memory ring: ~100 KB (two CTAs per SM) for narrow token tiles
     const size_t stage = kABytes + static_cast<size_t>(g.bn) * kRowBytes;
     const size_t budget = g.bn <= 64 ? 100 * 1024 : 190 * 1024;
     int st = static_cast<int>(budget / stage);
     g.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
     g.smem_bytes = gemm_smem_bytes(g.stages, g.bn);
-    g.ws_floats = g.splits > 1 ? static_cast<size_t>(g.tiles) * g.splits * g.bn * kBM : 0;
+    const int ctas_per_sm = g.smem_bytes <= 113 * 1024 ? 2 : 1;
+    int splits = 1;
+    if (epi != EPI_ARGMAX) {
+        if (cluster) {
+            // the splits of a tile form one cluster; aim at ~0.85 of the resident CTA slots
+            const int target = (num_sms * ctas_per_sm * 27) / 32;
+            const int max_c = ctas_per_sm == 2 ? kMaxClusterSplits : 8;
+            splits = target / g.tiles;
+            splits = splits > max_c ? max_c : splits;
+            const int cap = g.kb_total / 2 > 1 ? g.kb_total / 2 : 1;   // >= 2 k-blocks per split
+            splits = splits < cap ? splits : cap;
+            splits = splits < 1 ? 1 : splits;
+        } else if (g.tiles < 2 * num_sms) {
+            splits = ceil_div(2 * num_sms, g.tiles);
+            const int cap = g.kb_total / 4 > 1 ? g.kb_total / 4 : 1;   // >= 4 k-blocks per split
+            splits = splits < cap ? splits : cap;
+        }
+    }
+    g.kb_per_split = ceil_div(g.kb_total, splits);
+    g.splits = ceil_div(g.kb_total, g.kb_per_split);
+    g.cluster = cluster && g.splits > 1;
+    if (g.cluster && static_cast<size_t>(g.stages) * stage < static_cast<size_t>(g.bn) * kBM * 4) {
+        // the partial tile must fit in the freed stage ring
+        g.kb_per_split = g.kb_total;
+        g.splits = 1;
+        g.cluster = false;
+    }
+    g.units = g.tiles * g.splits;
+    g.ws_floats = (g.splits > 1 && !g.cluster) ? static_cast<size_t>(g.tiles) * g.splits * g.bn * kBM : 0;
     return g;
 }
 
@@ -444,6 +534,7 @@ int launch_gemm(int dtype, int epi, const CUtensorMap& A, const CUtensorMap& A2,
     p.kb_per_split = plan.kb_per_split;
     p.bn = plan.bn;
     p.stages = plan.stages;
+    p.cluster = plan.cluster ? 1 : 0;
     if (dtype == PE_DTYPE_BF16) return launch_dispatch<__nv_bfloat16>(epi, A, A2, B, plan, p, stream, pdl);
     return launch_dispatch<float>(epi, A, A2, B, plan, p, stream, pdl);
 }

@@ -55,7 +55,9 @@ struct GemmParams {
     unsigned long long* amax;   // [N]
     float* logits;              // [N, ld_logits] or null
     int ld_logits;
-    // split-K scratch
+    // split-K: cluster != 0 reduces through distributed shared memory;
+    // otherwise partials go through ws and the tile's ticket
+    int cluster;
     float* ws;
     int* tickets;
     unsigned* err;
@@ -65,11 +67,12 @@ struct GemmPlan {
     int bn, n_tiles, m_tiles, splits, kb_total, kb_per_split, stages;
     int units;
     size_t smem_bytes;
-    size_t ws_floats;   // split-K scratch needed (0 if splits == 1)
+    size_t ws_floats;   // global split-K scratch needed (0 if splits == 1 or cluster)
     int tiles;          // tickets needed
+    bool cluster;       // splits of a tile form one thread-block cluster
 };
 
-GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms);
+GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster);
 int launch_gemm(int dtype, int epi, const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B,
                 const GemmPlan& plan, GemmParams p, cudaStream_t stream, bool pdl);
 

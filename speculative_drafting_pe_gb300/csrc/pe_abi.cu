@@ -275,7 +275,7 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
                             {V, H, EPI_ARGMAX}};
     for (const Shape& s : shapes) {
         for (int n = 1; n <= h->max_rows; ++n) {
-            GemmPlan g = plan_gemm(s.M, n, s.Kd, s.epi, elem_bytes, h->num_sms);
+            GemmPlan g = plan_gemm(s.M, n, s.Kd, s.epi, elem_bytes, h->num_sms, true);
             ws = ws > g.ws_floats ? ws : g.ws_floats;
             tiles = tiles > g.tiles ? tiles : g.tiles;
         }
@@ -390,13 +390,13 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     int rc;
 
     // GEMM plans (bn depends only on the row count)
-    const GemmPlan p_fc = plan_gemm(H, B, 3 * H, EPI_STORE, eb, h->num_sms);
-    const GemmPlan p_qkv0 = plan_gemm(qkv_rows, R, 2 * H, EPI_QKV, eb, h->num_sms);
-    const GemmPlan p_qkv = plan_gemm(qkv_rows, R, H, EPI_QKV, eb, h->num_sms);
-    const GemmPlan p_o = plan_gemm(H, R, qd, EPI_RESID, eb, h->num_sms);
-    const GemmPlan p_gu = plan_gemm(F, R, H, EPI_SWIGLU, eb, h->num_sms);
-    const GemmPlan p_down = plan_gemm(H, R, F, EPI_RESID, eb, h->num_sms);
-    const GemmPlan p_lm = plan_gemm(V, R, H, EPI_ARGMAX, eb, h->num_sms);
+    const GemmPlan p_fc = plan_gemm(H, B, 3 * H, EPI_STORE, eb, h->num_sms, true);
+    const GemmPlan p_qkv0 = plan_gemm(qkv_rows, R, 2 * H, EPI_QKV, eb, h->num_sms, true);
+    const GemmPlan p_qkv = plan_gemm(qkv_rows, R, H, EPI_QKV, eb, h->num_sms, true);
+    const GemmPlan p_o = plan_gemm(H, R, qd, EPI_RESID, eb, h->num_sms, true);
+    const GemmPlan p_gu = plan_gemm(F, R, H, EPI_SWIGLU, eb, h->num_sms, true);
+    const GemmPlan p_down = plan_gemm(H, R, F, EPI_RESID, eb, h->num_sms, true);
+    const GemmPlan p_lm = plan_gemm(V, R, H, EPI_ARGMAX, eb, h->num_sms, true);
     const bool attn_tc = dt == PE_DTYPE_BF16;
     const AttnPlan p_at = attn_tc ? plan_attention_tc(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms)
                                   : plan_attention(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms);
@@ -596,7 +596,7 @@ int pe_linear_scratch(int32_t dtype, int32_t M, int32_t N, int32_t Kd, int64_t* 
     int dev = 0, sms = 0;
     PE_CUDA_TRY(cudaGetDevice(&dev));
     PE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    const GemmPlan g = plan_gemm(M, N, Kd, EPI_STORE, dtype == PE_DTYPE_BF16 ? 2 : 4, sms);
+    const GemmPlan g = plan_gemm(M, N, Kd, EPI_STORE, dtype == PE_DTYPE_BF16 ? 2 : 4, sms, false);
     *ws_floats = static_cast<int64_t>(g.ws_floats);
     *n_tickets = g.tiles;
     return PE_OK;
@@ -611,7 +611,7 @@ int pe_linear(int32_t dtype, int32_t M, int32_t N, int32_t Kd, const void* w, co
     PE_CUDA_TRY(cudaGetDevice(&dev));
     PE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     const int eb = dtype == PE_DTYPE_BF16 ? 2 : 4;
-    const GemmPlan g = plan_gemm(M, N, Kd, EPI_STORE, eb, sms);
+    const GemmPlan g = plan_gemm(M, N, Kd, EPI_STORE, eb, sms, false);
     if (g.ws_floats > 0 && ws == nullptr) { set_error("this shape needs split-K scratch"); return PE_ERR_ARG; }
     CUtensorMap ta, tb;
     int rc = encode_tmap_2d(&ta, w, dtype, Kd, M, static_cast<uint64_t>(Kd) * eb, 128 / eb, 128);
