@@ -28,7 +28,7 @@ constexpr int kTile = 64;          // cache entries per tile (4 pages)
 constexpr int kStages = 3;
 constexpr int kBoxBytes = 16 * 128;
 constexpr int kMaxRq = 128;        // K * nq/nkv query rows per kv head
-constexpr int kMaxCluster = 8;     // portable cluster size
+constexpr int kMaxCluster = 16;    // non-portable cluster size limit
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -347,16 +347,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+size_t attn_smem_bytes(int hd, int chunk) {
+    return 2 * kStages * static_cast<size_t>(kTile) * hd * 2 + kStages * 8 +
+           (static_cast<size_t>(chunk) / 16 + 4) * sizeof(int) + 1024;
+}
+
 template <int HD>
 int launch_hd(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, cudaStream_t s, bool pdl) {
-    const size_t smem = 2 * kStages * static_cast<size_t>(kTile) * HD * 2 + kStages * 8 +
-                        (static_cast<size_t>(p.chunk) / 16 + 4) * sizeof(int) + 1024;
+    const size_t smem = attn_smem_bytes(HD, p.chunk);
     auto kern = k_attn_tc<HD>;
     static size_t smem_set[64] = {};
     int dev = 0;
     PE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64 || smem > smem_set[dev]) {
         PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+        PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
         if (dev >= 0 && dev < 64) smem_set[dev] = smem;
     }
     cudaLaunchConfig_t cfg = {};
@@ -379,20 +384,65 @@ int launch_hd(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
 
 }  // namespace
 
+// Largest cluster size (<= 16) for which every (request, kv head) cluster is
+// resident in one wave, from the occupancy calculator (cached per size).
+static int max_active_clusters(int hd, int C, size_t smem) {
+    static int cache[2][17] = {};
+    int& c = cache[hd == 128 ? 1 : 0][C];
+    if (c != 0) return c;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C, C);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = static_cast<unsigned>(C);
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e;
+    if (hd == 128) {
+        cudaFuncSetAttribute(k_attn_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        cudaFuncSetAttribute(k_attn_tc<128>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaOccupancyMaxActiveClusters(&n, k_attn_tc<128>, &cfg);
+    } else {
+        cudaFuncSetAttribute(k_attn_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        cudaFuncSetAttribute(k_attn_tc<64>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaOccupancyMaxActiveClusters(&n, k_attn_tc<64>, &cfg);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        n = -1;   // size not launchable
+    }
+    c = n == 0 ? -1 : n;
+    return c;
+}
+
 AttnPlan plan_attention_tc(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms) {
     AttnPlan a{};
     const int max_entries = max_pages * page_size;
     const int pairs = B * nkv;
-    int C = ceil_div(num_sms, pairs);                    // about one wave of CTAs
-    if (C > kMaxCluster) C = kMaxCluster;
-    if (C < 1) C = 1;
-    int chunk = ceil_div(ceil_div(max_entries, C), kTile) * kTile;
+    int want = ceil_div(num_sms, pairs);                 // about one wave of CTAs
+    if (want > kMaxCluster) want = kMaxCluster;
+    if (want < 1) want = 1;
+    int C = 1, chunk = ceil_div(max_entries, kTile) * kTile;
+    for (int c = want; c >= 2; --c) {
+        const int ch = ceil_div(ceil_div(max_entries, c), kTile) * kTile;
+        const int n = max_active_clusters(hd, c, attn_smem_bytes(hd, ch));
+        if (n > 0 && n >= pairs) {                       // every cluster resident at once
+            C = c;
+            chunk = ch;
+            break;
+        }
+    }
     C = ceil_div(max_entries, chunk);                    // splits actually needed
     a.chunk = chunk;
     a.max_splits = C;                                    // one cluster of C CTAs per (request, kv head)
     a.ws_floats = 0;
     a.tickets = 0;
-    (void)K; (void)nq; (void)hd;
+    (void)K; (void)nq;
     return a;
 }
 

@@ -28,7 +28,7 @@ constexpr int kRowBytes = 128;               // one 128-byte swizzle row per til
 constexpr int kABytes = kBM * kRowBytes;     // 16 KB weight tile per stage
 constexpr int kChunk = 16;                   // accumulator columns per tcgen05.ld
 constexpr int kPitch = kBM + 4;              // epilogue staging row pitch (floats)
-constexpr int kMaxClusterSplits = 16;        // cluster split-K: at most 16 CTAs per tile
+constexpr int kMaxClusterSplits = 8;         // cluster split-K: at most 8 CTAs per tile
 
 __host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn) {
     size_t off = static_cast<size_t>(stages) * (kABytes + static_cast<size_t>(bn) * kRowBytes);
@@ -497,9 +497,11 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     int splits = 1;
     if (epi != EPI_ARGMAX) {
         if (cluster) {
-            // the splits of a tile form one cluster; aim at ~0.85 of the resident CTA slots
-            const int target = (num_sms * ctas_per_sm * 27) / 32;
-            const int max_c = ctas_per_sm == 2 ? kMaxClusterSplits : 8;
+            // the splits of a tile form one cluster of <= 8 CTAs; aim at one wave
+            // that leaves room on each SM for the next kernel's CTAs to start
+            // streaming their weights early (programmatic dependent launch)
+            const int target = ctas_per_sm == 2 ? (num_sms * 3) / 2 : num_sms;
+            const int max_c = kMaxClusterSplits;
             splits = target / g.tiles;
             splits = splits > max_c ? max_c : splits;
             const int cap = g.kb_total / 2 > 1 ? g.kb_total / 2 : 1;   // >= 2 k-blocks per split
