@@ -172,6 +172,26 @@ int pe_linear_scratch(int32_t dtype, int32_t M, int32_t N, int32_t Kd, int64_t* 
 int pe_linear(int32_t dtype, int32_t M, int32_t N, int32_t Kd, const void* w, const void* x, float* y,
               float* ws, int32_t* tickets, void* stream);
 
+/* pe_linear for callers that cannot allocate device memory (this entry point
+ * has no counterpart in the paper). Some callers may not call cudaMalloc
+ * where they run a GEMM: code running while another thread captures a CUDA
+ * graph in global capture mode, where cudaMalloc is prohibited, or runtimes
+ * whose device memory is fully reserved by their own allocator. This variant
+ * computes the same y[n, m] = sum_k w[m, k] * x[n, k] as pe_linear (same
+ * arguments minus ws / tickets) but keeps its split-K scratch in fixed arrays
+ * inside the library: 8 MiB of partials and 4096 tickets per device, held
+ * until the process exits. It allocates nothing.
+ *  - Shapes whose plan needs more scratch than that return PE_ERR_ARG with a
+ *    message giving the need and the maximum (pe_linear has no such limit).
+ *  - The first call on each device looks up the arrays' device addresses
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture that should contain later calls.
+ *  - Every call on a device shares the same arrays: calls that can overlap
+ *    on the GPU (several streams or host threads) race and must be serialised
+ *    by the caller. Each call clears the tickets it uses on its stream. */
+int pe_linear_noalloc(int32_t dtype, int32_t M, int32_t N, int32_t Kd, const void* w, const void* x, float* y,
+                      void* stream);
+
 /* One whole step (pe_draft, then pe_verify_rebuild on its drafts) captured
  * once into a CUDA graph and replayed with a single launch. The arguments are
  * those of pe_draft and pe_verify_rebuild (drafts are shared; draft_status and

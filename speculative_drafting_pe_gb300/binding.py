@@ -22,6 +22,7 @@ EXPORTS = (
     "pe_last_launch_count", "pe_destroy", "pe_last_error", "pe_abi_version", "pe_linear_scratch", "pe_linear",
     "pe_profile_start", "pe_profile_stop", "pe_kernel_name",
     "pe_step_graph_create", "pe_step_graph_launch", "pe_step_graph_launch_count", "pe_step_graph_destroy",
+    "pe_linear_noalloc",
 )
 KERNEL_KINDS = ("fc", "row_build", "rmsnorm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "argmax")
 
@@ -91,6 +92,8 @@ def load():
     lib.pe_linear_scratch.restype = ctypes.c_int
     lib.pe_linear.argtypes = [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.pe_linear.restype = ctypes.c_int
+    lib.pe_linear_noalloc.argtypes = [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp]
+    lib.pe_linear_noalloc.restype = ctypes.c_int
     lib.pe_profile_start.argtypes = [_vp, _i32, _i32]
     lib.pe_profile_start.restype = ctypes.c_int
     lib.pe_profile_stop.argtypes = [_vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_i32)]
@@ -293,6 +296,23 @@ def linear(w, x, stream=None):
     tickets = torch.zeros(max(nt.value, 1), dtype=torch.int32, device=w.device)
     y = torch.empty(N, M, dtype=torch.float32, device=w.device)
     _check(lib.pe_linear(dtype, M, N, Kd, _p(w), _p(x), _p(y), _p(ws), _p(tickets), _stream_ptr(stream)))
+    return y
+
+
+def linear_noalloc(w, x, y=None, stream=None):
+    """y = x @ w.T through pe_linear_noalloc, which allocates no device memory
+    (its split-K scratch is built into the library). Pass `y` to avoid the
+    output allocation here as well."""
+    lib = load()
+    M, Kd = w.shape
+    N = x.shape[0]
+    dtype = PE_DTYPE_BF16 if w.dtype == torch.bfloat16 else PE_DTYPE_FP32
+    _need(x, w.dtype, w.device, "x")
+    _need(w, w.dtype, w.device, "w")
+    if y is None:
+        y = torch.empty(N, M, dtype=torch.float32, device=w.device)
+    _need(y, torch.float32, w.device, "y")
+    _check(lib.pe_linear_noalloc(dtype, M, N, Kd, _p(w), _p(x), _p(y), _stream_ptr(stream)))
     return y
 
 
