@@ -159,6 +159,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x, device=None):
+    """Largest value of x over all ranks of the default process group (the
+    timing every rank reports is the slowest rank's); x itself when there is
+    no group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_steps_per_s(world, steps, elapsed_ms):
+    """Replicas: every rank runs `steps` steps of its own batch; the job
+    processed world * steps steps in the slowest rank's time."""
+    return world * steps / (elapsed_ms / 1e3)
+
+
 # ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
 
 def oracle_worker(args):
@@ -304,13 +323,9 @@ def bench_ours(args):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
     ms_per_step = elapsed_ms / args.steps
-    value = world * args.steps / (elapsed_ms / 1e3)
+    value = whole_job_steps_per_s(world, args.steps, elapsed_ms)
     acc = sg.out["accepted"].cpu().numpy()
     assert (sg.out["drafts"] == drafts).all().item()
 
@@ -386,11 +401,7 @@ def bench_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
@@ -444,7 +455,7 @@ def bench_ours(args):
         "roofline": roof,
         "kernel_share": {k: round(v / total_share, 4) for k, v in sorted(shares.items(), key=lambda x: -x[1])},
         "clocks": clocks,
-        "e2e": {"value": world * args.steps / (e2e_ms / 1e3), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_steps_per_s(world, args.steps, e2e_ms), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
     }
@@ -465,18 +476,23 @@ def bench_ours(args):
 
 
 def read_profile_traffic(kernel, workload):
-    """DRAM bytes per launch from a committed ncu summary, if it matches the
-    current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.json")
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    profiles/traffic_<kernel>_<workload>.md, if that summary was taken on the
+    current kernel sources (its source_hash line); else None."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith(("source_hash", "dram_bytes_per_launch")):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_hash") != kernel_source_hash():
+        return None
     try:
-        with open(path) as f:
-            rec = json.load(f)
-        if rec.get("source_hash") != kernel_source_hash():
-            return None
-        return rec.get("dram_bytes_per_launch")
-    except (OSError, ValueError):
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
         return None
 
 
