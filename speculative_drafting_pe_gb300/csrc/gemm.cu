@@ -32,7 +32,7 @@ constexpr int kMaxClusterSplits = 8;         // cluster split-K: at most 8 CTAs 
 
 __host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn) {
     size_t off = static_cast<size_t>(stages) * (kABytes + static_cast<size_t>(bn) * kRowBytes);
-    off += static_cast<size_t>(2 * stages + 1) * 8;   // mbarriers
+    off += static_cast<size_t>(2 * stages + 4) * 8;   // mbarriers
     off += 16;                                        // TMEM base + flags
     off = (off + 15) & ~static_cast<size_t>(15);
     off += static_cast<size_t>(kChunk) * kPitch * 4;  // epilogue staging tile
@@ -67,18 +67,35 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
     } else if constexpr (EPI == EPI_ARGMAX) {
         const int m = m_tile * kBM + ml;
         const bool valid = m < p.M;
+        unsigned long long k[kChunk];
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
-            const int n = n0 + i;
-            if (p.logits != nullptr && valid && col_ok(i)) p.logits[static_cast<size_t>(n) * p.ld_logits + m] = v[i];
-            unsigned long long key = valid ? argmax_key(v[i], static_cast<uint32_t>(m)) : 0ull;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
-                key = o > key ? o : key;
-            }
-            if ((ml & 31) == 0 && col_ok(i) && key != 0ull) atomicMax(p.amax + n, key);
+            if (p.logits != nullptr && valid && col_ok(i)) p.logits[static_cast<size_t>(n0 + i) * p.ld_logits + m] = v[i];
+            k[i] = valid ? argmax_key(v[i], static_cast<uint32_t>(m)) : 0ull;
         }
+        // Transpose-reduce over the warp's 32 rows: each round halves the
+        // columns a lane keeps and doubles the rows each kept key covers.
+        // Afterwards lanes 2c and 2c+1 hold column c's maximum.
+        const int lane = ml & 31;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int half = 8 >> r;
+            const int bit = 16 >> r;
+            const bool upper = (lane & bit) != 0;
+#pragma unroll
+            for (int j = 0; j < half; ++j) {
+                const unsigned long long send = upper ? k[j] : k[j + half];
+                const unsigned long long keep = upper ? k[j + half] : k[j];
+                const unsigned long long recv = __shfl_xor_sync(0xffffffffu, send, bit);
+                k[j] = keep > recv ? keep : recv;
+            }
+        }
+        {
+            const unsigned long long recv = __shfl_xor_sync(0xffffffffu, k[0], 1);
+            k[0] = k[0] > recv ? k[0] : recv;
+        }
+        const int c = (lane >> 1) & 15;
+        if ((lane & 1) == 0 && col_ok(c) && k[0] != 0ull) atomicMax(p.amax + n0 + c, k[0]);
     } else if constexpr (EPI == EPI_SWIGLU) {
         // rows 0..63 of the tile are gate rows, 64..127 the matching up rows
         named_bar_sync(1, 128);
@@ -161,19 +178,13 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
     }
 }
 
+// One tile's epilogue from its TMEM accumulator (t_acc: lane 0, column 0).
 template <typename T, int EPI>
-__device__ __forceinline__ void epilogue(const GemmParams& p, uint32_t tmem_acc, uint64_t* tfull, float* stile,
-                                         int* sflag, float* part, int m_tile, int n_tile, int split, int warp,
-                                         int lane) {
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_acc, float* stile, int* sflag,
+                                              float* part, int m_tile, int n_tile, int split, int warp, int lane) {
     const int quad = warp & 3;               // TMEM lane quadrant this warp may read
     const int ml = quad * 32 + lane;         // tile row = TMEM lane
-    const uint32_t t_row = tmem_acc + (static_cast<uint32_t>(quad * 32) << 16);
-    const bool ok = mbar_wait(tfull, 0, p.err, PE_DEVERR_GEMM_TIMEOUT);
-    tc_fence_after_sync();
-    if (!ok) sflag[0] = 1;
-    named_bar_sync(1, 128);
-    if (sflag[0]) return;
-
+    const uint32_t t_row = t_acc + (static_cast<uint32_t>(quad * 32) << 16);
     const int bn = p.bn;
     const int n_base = n_tile * bn;
     if (p.splits > 1 && p.cluster) {
@@ -287,21 +298,29 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t* sB = smem + static_cast<size_t>(stages) * kABytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(sB + static_cast<size_t>(stages) * b_bytes);
     uint64_t* empty = full + stages;
-    uint64_t* tfull = empty + stages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+    uint64_t* tfull = empty + stages;      // [2] accumulator ready
+    uint64_t* tempty = tfull + 2;          // [2] accumulator drained by the epilogue
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
     int* sflag = reinterpret_cast<int*>(tmem_slot + 1);
     float* stile = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(sflag + 3) + 15) & ~uintptr_t(15));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int unit = blockIdx.x;
-    const int split = unit % p.splits;       // splits of one tile are adjacent (one cluster)
-    const int rest = unit / p.splits;
-    const int n_tile = rest % p.n_tiles;
-    const int m_tile = rest / p.n_tiles;
-    const int kb0 = split * p.kb_per_split;
-    const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
-    const uint32_t tmem_cols = tmem_cols_for(bn);
+    // Work units u = blockIdx.x, blockIdx.x + gridDim.x, ... (one unit per CTA
+    // unless the launch is persistent). The splits of one tile are adjacent
+    // (one cluster in cluster split-K mode), then n tiles, then m tiles.
+    const int units = p.m_tiles * p.n_tiles * p.splits;
+    auto decode = [&](int u, int& m_tile, int& n_tile, int& split, int& kb0, int& kb1) {
+        split = u % p.splits;
+        const int rest = u / p.splits;
+        n_tile = rest % p.n_tiles;
+        m_tile = rest / p.n_tiles;
+        kb0 = split * p.kb_per_split;
+        kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+    };
+    const int nacc = p.persistent ? 2 : 1;           // double-buffered accumulator when persistent
+    const uint32_t acc_cols = tmem_cols_for(bn);
+    const uint32_t tmem_cols = acc_cols * static_cast<uint32_t>(nacc);
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
@@ -311,7 +330,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(tfull, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
         sflag[0] = 0;
         sflag[1] = 0;
         fence_mbar_init();
@@ -323,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    const uint32_t tmem_acc = *tmem_slot;
+    const uint32_t tmem_base = *tmem_slot;
 
     pdl_launch_dependents();
     // Everything but the producer waits here for the previous kernel in the
@@ -335,70 +357,122 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_x = l2_policy_evict_last();
             constexpr int kBK = kRowBytes / static_cast<int>(sizeof(T));
-            auto load_a = [&](int st, int kb) {
-                uint8_t* a_dst = sA + static_cast<size_t>(st) * kABytes;
-                if constexpr (EPI == EPI_SWIGLU) {
-                    tma_load_2d(a_dst, &tmA, &full[st], kb * kBK, m_tile * 64, pol_w);
-                    tma_load_2d(a_dst + kABytes / 2, &tmA2, &full[st], kb * kBK, m_tile * 64, pol_w);
-                } else {
-                    tma_load_2d(a_dst, &tmA, &full[st], kb * kBK, m_tile * kBM, pol_w);
+            int s = 0;
+            uint32_t ph = 0;
+            bool first = true, ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                int m_tile, n_tile, split, kb0, kb1;
+                decode(u, m_tile, n_tile, split, kb0, kb1);
+                auto load_a = [&](int st, int kb) {
+                    uint8_t* a_dst = sA + static_cast<size_t>(st) * kABytes;
+                    if constexpr (EPI == EPI_SWIGLU) {
+                        tma_load_2d(a_dst, &tmA, &full[st], kb * kBK, m_tile * 64, pol_w);
+                        tma_load_2d(a_dst + kABytes / 2, &tmA2, &full[st], kb * kBK, m_tile * 64, pol_w);
+                    } else {
+                        tma_load_2d(a_dst, &tmA, &full[st], kb * kBK, m_tile * kBM, pol_w);
+                    }
+                };
+                auto load_b = [&](int st, int kb) {
+                    tma_load_2d(sB + static_cast<size_t>(st) * b_bytes, &tmB, &full[st], kb * kBK, n_tile * bn,
+                                pol_x);
+                };
+                int kb = kb0;
+                if (first) {
+                    // Weights do not depend on earlier kernels: start streaming
+                    // the first stages' weight tiles before the dependency
+                    // wait, then add the token tiles of those stages.
+                    const int pre = min(stages, kb1 - kb0);
+                    for (int i = 0; i < pre; ++i) {
+                        mbar_arrive_expect_tx(&full[i], kABytes + b_bytes);
+                        load_a(i, kb0 + i);
+                    }
+                    pdl_wait();
+                    for (int i = 0; i < pre; ++i) load_b(i, kb0 + i);
+                    s = pre % stages;
+                    ph = (pre == stages) ? 1u : 0u;
+                    kb = kb0 + pre;
+                    first = false;
                 }
-            };
-            auto load_b = [&](int st, int kb) {
-                tma_load_2d(sB + static_cast<size_t>(st) * b_bytes, &tmB, &full[st], kb * kBK, n_tile * bn, pol_x);
-            };
-            // Weights do not depend on earlier kernels: start streaming the
-            // weight tiles of the first stages before the dependency wait,
-            // then add the token tiles of those stages.
-            const int pre = min(stages, kb1 - kb0);
-            for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&full[i], kABytes + b_bytes);
-                load_a(i, kb0 + i);
-            }
-            pdl_wait();
-            for (int i = 0; i < pre; ++i) load_b(i, kb0 + i);
-            int s = pre % stages;
-            uint32_t ph = (pre == stages) ? 1u : 0u;
-            for (int kb = kb0 + pre; kb < kb1; ++kb) {
-                if (!mbar_wait(&empty[s], ph ^ 1u, p.err, PE_DEVERR_GEMM_TIMEOUT)) break;
-                mbar_arrive_expect_tx(&full[s], kABytes + b_bytes);
-                load_a(s, kb);
-                load_b(s, kb);
-                if (++s == stages) {
-                    s = 0;
-                    ph ^= 1u;
+                for (; kb < kb1; ++kb) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], kABytes + b_bytes);
+                    load_a(s, kb);
+                    load_b(s, kb);
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
+            if (first) pdl_wait();
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = umma_idesc(UmmaKind<T>::kFmt, kBM, bn);
             int s = 0;
             uint32_t ph = 0;
-            for (int kb = kb0; kb < kb1; ++kb) {
-                if (!mbar_wait(&full[s], ph, p.err, PE_DEVERR_GEMM_TIMEOUT)) break;
+            int it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
+                int m_tile, n_tile, split, kb0, kb1;
+                decode(u, m_tile, n_tile, split, kb0, kb1);
+                const int acc = it % nacc;
+                const int use = it / nacc;
+                // wait until the epilogue has drained this accumulator's previous use
+                if (!mbar_wait(&tempty[acc], static_cast<uint32_t>(use & 1) ^ 1u, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after_sync();
-                const uint32_t a_addr = smem_u32(sA + static_cast<size_t>(s) * kABytes);
-                const uint32_t b_addr = smem_u32(sB + static_cast<size_t>(s) * b_bytes);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * acc_cols;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&full[s], ph, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_addr = smem_u32(sA + static_cast<size_t>(s) * kABytes);
+                    const uint32_t b_addr = smem_u32(sB + static_cast<size_t>(s) * b_bytes);
 #pragma unroll
-                for (int kk = 0; kk < kRowBytes / 32; ++kk) {
-                    UmmaKind<T>::mma(tmem_acc, umma_desc_sw128(a_addr + kk * 32), umma_desc_sw128(b_addr + kk * 32),
-                                     idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kRowBytes / 32; ++kk) {
+                        UmmaKind<T>::mma(d_tmem, umma_desc_sw128(a_addr + kk * 32), umma_desc_sw128(b_addr + kk * 32),
+                                         idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&empty[s]);
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
-                umma_commit(&empty[s]);
-                if (++s == stages) {
-                    s = 0;
-                    ph ^= 1u;
-                }
+                umma_commit(&tfull[acc]);
             }
-            umma_commit(tfull);
         }
         __syncwarp();
     } else {
-        epilogue<T, EPI>(p, tmem_acc, tfull, stile, sflag, reinterpret_cast<float*>(smem), m_tile, n_tile, split,
-                         warp, lane);
+        int it = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+            int m_tile, n_tile, split, kb0, kb1;
+            decode(u, m_tile, n_tile, split, kb0, kb1);
+            const int acc = it % nacc;
+            const int use = it / nacc;
+            const bool ok = mbar_wait(&tfull[acc], static_cast<uint32_t>(use & 1), p.err, PE_DEVERR_GEMM_TIMEOUT);
+            tc_fence_after_sync();
+            if (!ok) sflag[0] = 1;
+            named_bar_sync(1, 128);
+            if (sflag[0]) break;
+            epilogue_tile<T, EPI>(p, tmem_base + static_cast<uint32_t>(acc) * acc_cols, stile, sflag,
+                                  reinterpret_cast<float*>(smem), m_tile, n_tile, split, warp, lane);
+            tc_fence_before_sync();
+            mbar_arrive(&tempty[acc]);
+        }
     }
     if (p.splits > 1 && p.cluster) {
+        // cluster split-K (one unit per CTA): reduce through distributed shared memory
+        int m_tile, n_tile, split, kb0, kb1;
+        decode(blockIdx.x, m_tile, n_tile, split, kb0, kb1);
         __syncthreads();              // this CTA's partial is in shared memory
         cluster_sync_all();           // ... and so are the peers'
         if (warp >= 2 && !sflag[0])
@@ -416,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_acc, tmem_cols);
+        tmem_dealloc(tmem_base, tmem_cols);
     }
 }
 
@@ -434,7 +508,7 @@ int launch_typed(const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap&
         if (dev >= 0 && dev < 64) smem_set[dev] = plan.smem_bytes;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(plan.units);
+    cfg.gridDim = dim3(plan.grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = plan.smem_bytes;
     cfg.stream = stream;
@@ -523,6 +597,11 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
         g.cluster = false;
     }
     g.units = g.tiles * g.splits;
+    // Without split-K the kernel is persistent: one CTA per resident slot
+    // walks the tiles with a double-buffered TMEM accumulator, so the
+    // epilogue of one tile overlaps the mainloop of the next.
+    g.persistent = g.splits == 1 && g.units > 1;
+    g.grid = g.persistent ? (g.units < num_sms * ctas_per_sm ? g.units : num_sms * ctas_per_sm) : g.units;
     g.ws_floats = (g.splits > 1 && !g.cluster) ? static_cast<size_t>(g.tiles) * g.splits * g.bn * kBM : 0;
     return g;
 }
@@ -537,6 +616,7 @@ int launch_gemm(int dtype, int epi, const CUtensorMap& A, const CUtensorMap& A2,
     p.bn = plan.bn;
     p.stages = plan.stages;
     p.cluster = plan.cluster ? 1 : 0;
+    p.persistent = plan.persistent ? 1 : 0;
     if (dtype == PE_DTYPE_BF16) return launch_dispatch<__nv_bfloat16>(epi, A, A2, B, plan, p, stream, pdl);
     return launch_dispatch<float>(epi, A, A2, B, plan, p, stream, pdl);
 }

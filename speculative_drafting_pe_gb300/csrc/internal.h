@@ -58,6 +58,7 @@ struct GemmParams {
     // split-K: cluster != 0 reduces through distributed shared memory;
     // otherwise partials go through ws and the tile's ticket
     int cluster;
+    int persistent;     // walk units with stride gridDim.x, double-buffered accumulator
     float* ws;
     int* tickets;
     unsigned* err;
@@ -70,6 +71,8 @@ struct GemmPlan {
     size_t ws_floats;   // global split-K scratch needed (0 if splits == 1 or cluster)
     int tiles;          // tickets needed
     bool cluster;       // splits of a tile form one thread-block cluster
+    bool persistent;    // grid < units: CTAs loop over tiles
+    int grid;           // CTAs launched
 };
 
 GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster);

@@ -17,6 +17,8 @@ SHAPES = [
     (1000, 33, 520),      # ragged M, N and K tail
     (384, 300, 256),      # two N tiles
     (512, 1408, 128),     # six N tiles (B=128, K=11 rows)
+    (151936, 7, 256),     # persistent: 1187 tiles over the resident CTAs (double-buffered accumulator)
+    (20000, 300, 128),    # persistent with two N tiles per weight tile
 ]
 
 
