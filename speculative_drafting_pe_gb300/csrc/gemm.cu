@@ -52,17 +52,22 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
                                             int n0, float* stile, uint32_t colmask) {
     auto col_ok = [&](int i) { return n0 + i < p.N && ((colmask >> i) & 1u); };
     if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
+        // all loads of the chunk first, then all stores (the destinations of
+        // different columns never alias, but the compiler cannot know that)
         const int m = m_tile * kBM + ml;
         if (m < p.M) {
+            float* __restrict__ base = p.out_f32 + m;
+            float old[kChunk];
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) {
-                const int n = n0 + i;
-                if (col_ok(i)) {
-                    float* dst = p.out_f32 + static_cast<size_t>(n) * p.ld_out + m;
-                    if constexpr (EPI == EPI_RESID) *dst += v[i];
-                    else *dst = v[i];
+                old[i] = 0.f;
+                if constexpr (EPI == EPI_RESID) {
+                    if (col_ok(i)) old[i] = base[static_cast<size_t>(n0 + i) * p.ld_out];
                 }
             }
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i)
+                if (col_ok(i)) base[static_cast<size_t>(n0 + i) * p.ld_out] = old[i] + v[i];
         }
     } else if constexpr (EPI == EPI_ARGMAX) {
         const int m = m_tile * kBM + ml;
@@ -105,17 +110,18 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
         const int fl = ml & 63;
         const int f = m_tile * 64 + fl;
         const int ibeg = (ml >> 6) * (kChunk / 2);
-        if (f < p.M) {
-            T* out = static_cast<T*>(p.out_act);
+        float g[kChunk / 2], u[kChunk / 2];
 #pragma unroll
-            for (int i = ibeg; i < ibeg + kChunk / 2; ++i) {
-                const int n = n0 + i;
-                if (col_ok(i)) {
-                    const float g = stile[i * kPitch + fl];
-                    const float u = stile[i * kPitch + fl + 64];
-                    out[static_cast<size_t>(n) * p.ld_act + f] = Elem<T>::from_f(silu_f(g) * u);
-                }
-            }
+        for (int i = 0; i < kChunk / 2; ++i) {
+            g[i] = stile[(ibeg + i) * kPitch + fl];
+            u[i] = stile[(ibeg + i) * kPitch + fl + 64];
+        }
+        if (f < p.M) {
+            T* __restrict__ out = static_cast<T*>(p.out_act) + f;
+#pragma unroll
+            for (int i = 0; i < kChunk / 2; ++i)
+                if (col_ok(ibeg + i))
+                    out[static_cast<size_t>(n0 + ibeg + i) * p.ld_act] = Elem<T>::from_f(silu_f(g[i]) * u[i]);
         }
     } else if constexpr (EPI == EPI_QKV) {
         // A 128-row tile holds whole heads of exactly one of q, k, v.
@@ -124,25 +130,28 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
         const int hd = p.hd;
         const int half = hd >> 1;
         const int region = m0 < p.nq_hd ? 0 : (m0 < p.nq_hd + p.nkv * hd ? 1 : 2);
+        // loads first: slots of the chunk's rows, RoPE factors, partner values
+        int slot[kChunk];
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) slot[i] = (region > 0 && col_ok(i)) ? p.row_slot[n0 + i] : -1;
         float outv[kChunk];
         if (region < 2) {
-            named_bar_sync(1, 128);
-#pragma unroll
-            for (int i = 0; i < kChunk; ++i) stile[i * kPitch + ml] = v[i];
-            named_bar_sync(1, 128);
             const int d = ml % hd;
             const bool lo = d < half;
             const int partner = lo ? ml + half : ml - half;
             const int fi = lo ? d : d - half;
+            float2 cs[kChunk];
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i)
+                cs[i] = col_ok(i) ? p.rope_cs[static_cast<size_t>(n0 + i) * half + fi] : make_float2(1.f, 0.f);
+            named_bar_sync(1, 128);
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) stile[i * kPitch + ml] = v[i];
+            named_bar_sync(1, 128);
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) {
-                const int n = n0 + i;
-                outv[i] = 0.f;
-                if (col_ok(i)) {
-                    const float2 cs = p.rope_cs[static_cast<size_t>(n) * half + fi];
-                    const float y = stile[i * kPitch + partner];
-                    outv[i] = lo ? (v[i] * cs.x - y * cs.y) : (v[i] * cs.x + y * cs.y);
-                }
+                const float y = stile[i * kPitch + partner];
+                outv[i] = lo ? (v[i] * cs[i].x - y * cs[i].y) : (v[i] * cs[i].x + y * cs[i].y);
             }
         } else {
 #pragma unroll
@@ -150,27 +159,21 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
         }
         if (m < p.M) {
             if (region == 0) {
-                T* q = static_cast<T*>(p.out_act);
+                T* __restrict__ q = static_cast<T*>(p.out_act) + m;
 #pragma unroll
-                for (int i = 0; i < kChunk; ++i) {
-                    const int n = n0 + i;
-                    if (col_ok(i)) q[static_cast<size_t>(n) * p.ld_act + m] = Elem<T>::from_f(outv[i]);
-                }
+                for (int i = 0; i < kChunk; ++i)
+                    if (col_ok(i)) q[static_cast<size_t>(n0 + i) * p.ld_act] = Elem<T>::from_f(outv[i]);
             } else {
                 const int r = m - p.nq_hd - (region == 2 ? p.nkv * hd : 0);
                 const int kvh = r / hd;
                 const int d = r - kvh * hd;
-                T* cache = static_cast<T*>(region == 1 ? p.k_cache : p.v_cache);
+                T* __restrict__ cache = static_cast<T*>(region == 1 ? p.k_cache : p.v_cache);
 #pragma unroll
                 for (int i = 0; i < kChunk; ++i) {
-                    const int n = n0 + i;
-                    if (col_ok(i)) {
-                        const int slot = p.row_slot[n];
-                        if (slot >= 0) {
-                            const size_t page = static_cast<size_t>(slot >> 4);
-                            const int off = slot & 15;
-                            cache[((page * p.nkv + kvh) * 16 + off) * hd + d] = Elem<T>::from_f(outv[i]);
-                        }
+                    if (slot[i] >= 0) {
+                        const size_t page = static_cast<size_t>(slot[i] >> 4);
+                        const int off = slot[i] & 15;
+                        cache[((page * p.nkv + kvh) * 16 + off) * hd + d] = Elem<T>::from_f(outv[i]);
                     }
                 }
             }
@@ -178,7 +181,6 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
     }
 }
 
-// One tile's epilogue from its TMEM accumulator (t_acc: lane 0, column 0).
 template <typename T, int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_acc, float* stile, int* sflag,
                                               float* part, int m_tile, int n_tile, int split, int warp, int lane) {
