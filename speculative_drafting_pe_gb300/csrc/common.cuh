@@ -140,29 +140,6 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
-// Bulk prefetch of [p, p + bytes) into L2 (no completion to wait for).
-__device__ __forceinline__ void l2_prefetch_bulk(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
-                 : "memory");
-}
-
-// This CTA's share of an L2 prefetch of `bytes` bytes at `base`, split over
-// `parts` CTAs and issued in 32 KB pieces by `nlanes` threads (lane index
-// `lane`). base and bytes are multiples of 16.
-__device__ __forceinline__ void l2_prefetch_share(const char* base, unsigned long long bytes, int part, int parts,
-                                                  int lane, int nlanes) {
-    if (base == nullptr || bytes == 0) return;
-    const unsigned long long per = ((bytes / parts + 15) / 16) * 16;
-    const unsigned long long lo = per * static_cast<unsigned long long>(part);
-    if (lo >= bytes) return;
-    const unsigned long long hi = lo + per < bytes ? lo + per : bytes;
-    constexpr unsigned long long kPiece = 32 * 1024;
-    for (unsigned long long o = lo + kPiece * lane; o < hi; o += kPiece * nlanes) {
-        const unsigned long long n = hi - o < kPiece ? hi - o : kPiece;
-        l2_prefetch_bulk(base + o, static_cast<uint32_t>(n));
-    }
-}
-
 // ---------------------------------------------------------------- tcgen05 (5th-gen tensor cores, TMEM)
 
 // Shared-memory matrix descriptor for a K-major operand stored with the

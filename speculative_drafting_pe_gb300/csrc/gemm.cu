@@ -350,12 +350,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t tmem_base = *tmem_slot;
 
     pdl_launch_dependents();
-    // The producer warp's idle lanes pull this CTA's share of a later
-    // kernel's weights into L2 (weights never depend on earlier kernels).
-    if (warp == 0 && lane > 0) {
-        l2_prefetch_share(p.pf[0], p.pf_bytes[0], blockIdx.x, gridDim.x, lane - 1, 31);
-        l2_prefetch_share(p.pf[1], p.pf_bytes[1], blockIdx.x, gridDim.x, lane - 1, 31);
-    }
     // Everything but the producer waits here for the previous kernel in the
     // stream (a no-op without programmatic dependent launch).
     if (warp != 0) pdl_wait();

@@ -59,10 +59,6 @@ struct GemmParams {
     // otherwise partials go through ws and the tile's ticket
     int cluster;
     int persistent;     // walk units with stride gridDim.x, double-buffered accumulator
-    // weights of a later kernel to pull into L2 while this one runs
-    // (two ranges; bytes multiples of 16, bases 16-byte aligned)
-    const char* pf[2];
-    unsigned long long pf_bytes[2];
     float* ws;
     int* tickets;
     unsigned* err;

@@ -415,26 +415,6 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         if ((rc = encode_tmap_kv(&tm_vc, v_cache, hd, nkv, num_pages)) != PE_OK) return rc;
     }
 
-    // L2 prefetch plan: every GEMM pulls in the weights of the next GEMM of
-    // the pass while it runs; the last layer's down projection pulls in the
-    // head of the LM-head matrix. PE_L2_PREFETCH=0 disables it.
-    const char* pf_env = std::getenv("PE_L2_PREFETCH");
-    const bool l2pf = !(pf_env != nullptr && pf_env[0] == '0');
-    const unsigned long long wb = h->elem;
-    auto set_pf = [&](GemmParams& g, const void* a, unsigned long long abytes, const void* b, unsigned long long bbytes) {
-        g.pf[0] = l2pf ? static_cast<const char*>(a) : nullptr;
-        g.pf_bytes[0] = l2pf ? abytes : 0;
-        g.pf[1] = l2pf ? static_cast<const char*>(b) : nullptr;
-        g.pf_bytes[1] = l2pf ? bbytes : 0;
-    };
-    const unsigned long long qkv0_bytes = static_cast<unsigned long long>(qkv_rows) * 2 * H * wb;
-    const unsigned long long qkv_bytes = static_cast<unsigned long long>(qkv_rows) * H * wb;
-    const unsigned long long o_bytes = static_cast<unsigned long long>(H) * qd * wb;
-    const unsigned long long gu_bytes = static_cast<unsigned long long>(F) * H * wb;
-    const unsigned long long down_bytes = static_cast<unsigned long long>(H) * F * wb;
-    const unsigned long long lm_bytes = static_cast<unsigned long long>(V) * H * wb;
-    const unsigned long long lm_pf = lm_bytes < (64ull << 20) ? lm_bytes : (64ull << 20);
-
     GemmParams base{};
     base.N = R;
     base.ws = h->gemm_ws;
@@ -460,7 +440,6 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         GemmParams p = base;
         p.M = H; p.N = B; p.Kd = 3 * H;
         p.out_f32 = h->h; p.ld_out = H;
-        set_pf(p, h->w.layer[0].w_qkv, qkv0_bytes, nullptr, 0);
         rc = run(PE_KERNEL_FC, [&] { return launch_gemm(dt, EPI_STORE, h->tm_fc, h->tm_fc, tm_th, p_fc, p, s, pdl); });
         if (rc != PE_OK) return rc;
     }
@@ -492,7 +471,6 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
             p.out_act = h->q; p.ld_act = qd;
             p.k_cache = kc; p.v_cache = vc; p.nq_hd = qd; p.nkv = nkv; p.hd = hd;
             p.row_slot = h->row_slot; p.rope_cs = h->rope_cs;
-            set_pf(p, L.w_o, o_bytes, nullptr, 0);
             rc = run(PE_KERNEL_QKV, [&] {
                 return launch_gemm(dt, EPI_QKV, h->tm_qkv[l], h->tm_qkv[l], l == 0 ? tm_u : tm_xn,
                                    l == 0 ? p_qkv0 : p_qkv, p, s, pdl);
@@ -515,7 +493,6 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         {   // a5: O projection + residual
             GemmParams p = base;
             p.M = H; p.Kd = qd; p.out_f32 = h->resid; p.ld_out = H;
-            set_pf(p, L.w_gate, gu_bytes, L.w_up, gu_bytes);
             rc = run(PE_KERNEL_O_PROJ,
                      [&] { return launch_gemm(dt, EPI_RESID, h->tm_o[l], h->tm_o[l], tm_attn, p_o, p, s, pdl); });
             if (rc != PE_OK) return rc;
@@ -526,14 +503,11 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         {   // a6: gate/up + SwiGLU, then down + residual
             GemmParams p = base;
             p.M = F; p.Kd = H; p.out_act = h->act; p.ld_act = F;
-            set_pf(p, L.w_down, down_bytes, nullptr, 0);
             rc = run(PE_KERNEL_GATE_UP,
                      [&] { return launch_gemm(dt, EPI_SWIGLU, h->tm_gate[l], h->tm_up[l], tm_xn, p_gu, p, s, pdl); });
             if (rc != PE_OK) return rc;
             GemmParams d = base;
             d.M = H; d.Kd = F; d.out_f32 = h->resid; d.ld_out = H;
-            if (l + 1 < 4) set_pf(d, h->w.layer[l + 1].w_qkv, qkv_bytes, nullptr, 0);
-            else set_pf(d, h->w.lm_head, lm_pf, nullptr, 0);
             rc = run(PE_KERNEL_DOWN,
                      [&] { return launch_gemm(dt, EPI_RESID, h->tm_down[l], h->tm_down[l], tm_act, p_down, d, s, pdl); });
             if (rc != PE_OK) return rc;
