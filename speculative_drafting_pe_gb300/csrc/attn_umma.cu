@@ -1,0 +1,533 @@
+// Tensor-core (tcgen05 / TMEM) decode-style paged GQA attention, bf16 KV cache.
+//
+// Row j of request b (all nq/nkv query heads of one kv head packed as
+// rows j*G + g, zero-padded to the MMA's 128 rows) attends to cache entries
+// 0 .. S_b + j; scores are scaled by 1/sqrt(hd); softmax is online in fp32
+// (base-2 exponent).
+//
+// One CTA per (request, kv head, entry split); a tile is 64 cache entries
+// (4 pages). Roles (192 threads):
+//   warp 4   TMA: the packed query rows once (3-D map over q), then K and V
+//            pages of every tile (4-D map over the paged cache) into a
+//            3-stage ring, 128-byte swizzle.
+//   warp 5   TMEM allocation; lane 0 issues  S_t = Q K_t^T  (M=128, N=64,
+//            K=hd) into one of two TMEM score buffers, and  O += P_t V_t
+//            (M=128, N=hd, K=64) into the TMEM output accumulator.
+//   warps 0-3  one thread per query row (= TMEM lane): transpose V_t into
+//            a K-major tile with ldmatrix.trans, read the row of S_t from
+//            TMEM, mask, keep the running max, write P_t = exp2(S - m) as
+//            bf16 into shared memory, and rescale the TMEM output row only
+//            when the running max grows by more than 2^8.
+// The entry splits of one (request, kv head) form one thread-block cluster
+// and are combined through distributed shared memory in split order.
+#include <cfloat>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pe {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kTile = 64;           // cache entries per tile
+constexpr int kStages = 3;
+constexpr int kRows = 128;          // MMA M (query rows, zero padded)
+constexpr int kBoxBytes = 16 * 128; // one page of one kv head, 64 dims
+constexpr float kRescaleLog2 = 8.f;
+constexpr int kMaxCluster = 16;
+
+template <int HD>
+struct Layout {
+    static constexpr int kSub = HD / 64;                    // 128-byte sub-tiles per row
+    static constexpr int kQBytes = kSub * kRows * 128;      // Q: kSub x [128 rows x 128 B]
+    static constexpr int kKVBytes = kSub * kTile * 128;     // K or V tile: kSub x [64 entries x 128 B]
+    static constexpr int kVtBytes = HD * 128;               // V^T: [hd rows x 64 entries]
+    static constexpr int kPBytes = kRows * 128;             // P: [128 rows x 64 entries]
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kQBytes;
+    static constexpr int kV = kK + kStages * kKVBytes;
+    static constexpr int kVt = kV + kStages * kKVBytes;
+    static constexpr int kP = kVt + 2 * kVtBytes;
+    static constexpr int kBar = kP + 2 * kPBytes;
+    static constexpr int kNumBars = 12;   // q_full, kv_full[3], kv_empty[3], s_full[2], p_full[2], o_done
+    static constexpr int kTmem = kBar + kNumBars * 8;
+    static constexpr int kPages = kTmem + 16;
+};
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attn_umma(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    using L = Layout<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+    uint64_t* q_full = bars;
+    uint64_t* kv_full = bars + 1;
+    uint64_t* kv_empty = bars + 4;
+    uint64_t* s_full = bars + 7;
+    uint64_t* p_full = bars + 9;
+    uint64_t* o_done = bars + 11;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmem);
+    int* s_pages = reinterpret_cast<int*>(sm + L::kPages);
+    __shared__ float s_m[kRows], s_l[kRows];   // this split's per-row running max (log2) and sum
+
+    const int pair = blockIdx.x;
+    const int b = pair / p.nkv;
+    const int kvh = pair - b * p.nkv;
+    const int split = blockIdx.y;
+    const int C = gridDim.y;                   // cluster size = entry splits per (request, kv head)
+    const int G = p.nq / p.nkv;
+    const int K = p.K;
+    const int Rq = K * G;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    const size_t row_stride = static_cast<size_t>(p.nq) * HD;
+
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // Every CTA of a cluster runs to the end (cluster barriers); CTAs without
+    // work contribute an empty partial.
+    const bool req_ok = p.status[b] == PE_REQ_OK;
+    const int S = req_ok ? p.seq_lens[b] : 0;
+    const int total = S + K;
+    const int e0 = split * p.chunk;
+    const int e1 = req_ok ? min(total, e0 + p.chunk) : e0;
+    const int n_tiles = e1 > e0 ? (e1 - e0 + kTile - 1) / kTile : 0;
+    const int32_t* pt = p.page_table + static_cast<size_t>(b) * p.max_pages;
+    const int last_page = (total - 1) >> 4;
+
+    if (tid == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&p_full[s], 128);
+        }
+        mbar_init(o_done, 1);
+        fence_mbar_init();
+    }
+    // page coordinates of this CTA's tiles; pages past the request's last
+    // entry get a negative (out-of-range, zero-filled) coordinate
+    for (int i = tid; i < n_tiles * (kTile / 16); i += kThreads) {
+        const int pi = (e0 >> 4) + i;
+        s_pages[i] = pi <= last_page ? pt[pi] + p.layer_page0 : -1;
+    }
+    // zero the padding query rows Rq..127 (the TMA box fills rows < Rq)
+    for (int idx = tid; idx < (kRows - Rq) * 8 * L::kSub; idx += kThreads) {
+        const int sub = idx / ((kRows - Rq) * 8);
+        const int rem = idx - sub * (kRows - Rq) * 8;
+        const int r = Rq + rem / 8, c = rem % 8;
+        sts128(smem_u32(sm + L::kQ + sub * kRows * 128 + r * 128 + c * 16), 0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_o = tmem + 128;             // output accumulator: columns 128 .. 128+hd
+    bool ok = true;
+
+    if (warp == 4) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0 && n_tiles > 0) {
+            const uint64_t pol_kv = l2_policy_evict_first();
+            const uint64_t pol_q = l2_policy_evict_last();
+            mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(L::kSub * 128 * Rq));
+            for (int sb = 0; sb < L::kSub; ++sb)
+                tma_load_3d(sm + L::kQ + sb * kRows * 128, &tmQ, q_full, sb * 64, kvh * G, b * K, pol_q);
+            for (int t = 0; t < n_tiles; ++t) {
+                const int st = t % kStages;
+                if (t >= kStages &&
+                    !mbar_wait(&kv_empty[st], static_cast<uint32_t>((t / kStages) & 1) ^ 1u, p.err,
+                               PE_DEVERR_ATTN_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&kv_full[st], 2u * L::kKVBytes);
+                for (int pg = 0; pg < kTile / 16; ++pg) {
+                    const int pc = s_pages[t * (kTile / 16) + pg];
+                    for (int sb = 0; sb < L::kSub; ++sb) {
+                        const int off = st * L::kKVBytes + sb * kTile * 128 + pg * kBoxBytes;
+                        tma_load_4d(sm + L::kK + off, &tmK, &kv_full[st], sb * 64, 0, kvh, pc, pol_kv);
+                        tma_load_4d(sm + L::kV + off, &tmV, &kv_full[st], sb * 64, 0, kvh, pc, pol_kv);
+                    }
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0 && n_tiles > 0) {
+            const uint32_t idesc_s = umma_idesc(1, kRows, kTile);
+            const uint32_t idesc_o = umma_idesc(1, kRows, HD);
+            const uint32_t q_addr = smem_u32(sm + L::kQ);
+            auto issue_s = [&](int t) {
+                const uint32_t k_addr = smem_u32(sm + L::kK + (t % kStages) * L::kKVBytes);
+                const uint32_t d = tmem + static_cast<uint32_t>((t & 1) * kTile);
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t sub = static_cast<uint32_t>(kk >> 2), within = static_cast<uint32_t>((kk & 3) * 32);
+                    UmmaKind<__nv_bfloat16>::mma(d, umma_desc_sw128(q_addr + sub * kRows * 128 + within),
+                                                 umma_desc_sw128(k_addr + sub * kTile * 128 + within), idesc_s,
+                                                 kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&s_full[t & 1]);
+            };
+            if (!mbar_wait(q_full, 0, p.err, PE_DEVERR_ATTN_TIMEOUT) ||
+                !mbar_wait(&kv_full[0], 0, p.err, PE_DEVERR_ATTN_TIMEOUT)) {
+                ok = false;
+            } else {
+                tc_fence_after_sync();
+                issue_s(0);
+            }
+            for (int t = 0; t < n_tiles && ok; ++t) {
+                if (t + 1 < n_tiles) {
+                    if (!mbar_wait(&kv_full[(t + 1) % kStages], static_cast<uint32_t>(((t + 1) / kStages) & 1), p.err,
+                                   PE_DEVERR_ATTN_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    issue_s(t + 1);
+                }
+                if (!mbar_wait(&p_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t p_addr = smem_u32(sm + L::kP + (t & 1) * L::kPBytes);
+                const uint32_t vt_addr = smem_u32(sm + L::kVt + (t & 1) * L::kVtBytes);
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    UmmaKind<__nv_bfloat16>::mma(t_o, umma_desc_sw128(p_addr + kk * 32),
+                                                 umma_desc_sw128(vt_addr + kk * 32), idesc_o,
+                                                 (t > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(o_done);
+                umma_commit(&kv_empty[t % kStages]);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ softmax warps: thread = query row = TMEM lane
+        const int row = tid;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const bool row_ok = row < Rq;
+        const int lim = S + row / G;          // last visible entry of this row
+        const float sl2 = rsqrtf(static_cast<float>(HD)) * 1.4426950408889634f;
+        float m_used = -INFINITY, l = 0.f;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t % kStages;
+            if (t >= 1 && !mbar_wait(o_done, static_cast<uint32_t>((t - 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT)) ok = false;
+            if (ok && !mbar_wait(&kv_full[st], static_cast<uint32_t>((t / kStages) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT))
+                ok = false;
+            ok = __all_sync(0xffffffffu, ok);   // keep the warp converged for the .aligned instructions
+            if (!ok) break;
+            tc_fence_after_sync();
+            // V_t -> V^T tile (K-major for the PV MMA); warp w handles dims [w*hd/4, (w+1)*hd/4)
+            {
+                const uint32_t v_addr = smem_u32(sm + L::kV + st * L::kKVBytes);
+                const uint32_t vt = smem_u32(sm + L::kVt + (t & 1) * L::kVtBytes);
+                const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+                for (int db = 0; db < HD / 32; ++db) {
+                    const int d0 = warp * (HD / 4) + db * 8;
+                    const int c = d0 >> 3;
+#pragma unroll
+                    for (int eg = 0; eg < 2; ++eg) {
+                        const int e = eg * 32 + mi * 8 + r8;
+                        const uint32_t addr =
+                            v_addr + static_cast<uint32_t>((c >> 3) * kTile * 128 + e * 128 + (((c & 7) ^ (e & 7)) << 4));
+                        uint32_t rr[4];
+                        ldsm_x4_t(addr, rr[0], rr[1], rr[2], rr[3]);
+                        const int d = d0 + (lane >> 2);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int ee = eg * 32 + q4 * 8 + 2 * (lane & 3);
+                            const uint32_t byte =
+                                static_cast<uint32_t>(d * 128 + ((((ee >> 3) ^ (d & 7))) << 4) + (ee & 7) * 2);
+                            sts32(vt + byte, rr[q4]);
+                        }
+                    }
+                }
+            }
+            // S_t row from TMEM
+            if (!mbar_wait(&s_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT)) ok = false;
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after_sync();
+            float sv[kTile];
+#pragma unroll
+            for (int c = 0; c < kTile / 16; ++c) {
+                float v16[16];
+                tmem_ld16(tmem + lane_off + static_cast<uint32_t>((t & 1) * kTile + c * 16), v16);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) sv[c * 16 + i] = v16[i];
+            }
+            const int tbase = e0 + t * kTile;
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kTile; ++i) {
+                const int e = tbase + i;
+                const bool vis = row_ok && e < e1 && e <= lim;
+                sv[i] = vis ? sv[i] * sl2 : -INFINITY;
+                tmax = fmaxf(tmax, sv[i]);
+            }
+            const bool need = tmax > -INFINITY && (m_used == -INFINITY || tmax > m_used + kRescaleLog2);
+            float f = 1.f;
+            if (need) {
+                f = m_used == -INFINITY ? 0.f : exp2f(m_used - tmax);
+                l *= f;
+                m_used = tmax;
+            }
+            if (t > 0 && __any_sync(0xffffffffu, need)) {
+                // O holds tiles < t (their PV is complete): scale the rows in
+                // TMEM, the whole warp together (rows that need none use f = 1)
+#pragma unroll
+                for (int c = 0; c < HD / 16; ++c) {
+                    float o16[16];
+                    tmem_ld16(t_o + lane_off + static_cast<uint32_t>(c * 16), o16);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o16[i] *= f;
+                    tmem_st16(t_o + lane_off + static_cast<uint32_t>(c * 16), o16);
+                }
+            }
+            // P_t row (bf16) into the K-major P tile
+            const uint32_t prow = smem_u32(sm + L::kP + (t & 1) * L::kPBytes) + static_cast<uint32_t>(row * 128);
+            float psum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float pv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float x = sv[c * 8 + i];
+                    pv[i] = (m_used == -INFINITY || x == -INFINITY) ? 0.f : exp2f(x - m_used);
+                    psum += pv[i];
+                }
+                sts128(prow + static_cast<uint32_t>((c ^ (row & 7)) << 4), pack_bf16(pv[0], pv[1]),
+                       pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
+            }
+            l += psum;
+            fence_proxy_async_smem();     // generic-proxy writes (V^T, P) -> visible to the tensor core
+            tc_fence_before_sync();
+            mbar_arrive(&p_full[t & 1]);
+        }
+        if (ok && n_tiles > 0 &&
+            !mbar_wait(o_done, static_cast<uint32_t>((n_tiles - 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT))
+            ok = false;
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after_sync();
+        if (!ok) l = 0.f;
+        const bool have_o = ok && n_tiles > 0;   // warp-uniform
+
+        if (C == 1) {
+            const int j = row / G, g = row - (row / G) * G;
+            __nv_bfloat16* dst = out + static_cast<size_t>(b * K + j) * row_stride + static_cast<size_t>(kvh * G + g) * HD;
+            const float inv = (req_ok && have_o && l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+            for (int c = 0; c < HD / 16; ++c) {
+                float o16[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o16[i] = 0.f;
+                if (have_o) tmem_ld16(t_o + lane_off + static_cast<uint32_t>(c * 16), o16);
+                if (row_ok) {
+                    uint4 w0, w1;
+                    w0.x = pack_bf16(o16[0] * inv, o16[1] * inv);
+                    w0.y = pack_bf16(o16[2] * inv, o16[3] * inv);
+                    w0.z = pack_bf16(o16[4] * inv, o16[5] * inv);
+                    w0.w = pack_bf16(o16[6] * inv, o16[7] * inv);
+                    w1.x = pack_bf16(o16[8] * inv, o16[9] * inv);
+                    w1.y = pack_bf16(o16[10] * inv, o16[11] * inv);
+                    w1.z = pack_bf16(o16[12] * inv, o16[13] * inv);
+                    w1.w = pack_bf16(o16[14] * inv, o16[15] * inv);
+                    *reinterpret_cast<uint4*>(dst + c * 16) = w0;
+                    *reinterpret_cast<uint4*>(dst + c * 16 + 8) = w1;
+                }
+            }
+        } else {
+            // split partial into this CTA's shared memory (the K stage ring is free)
+            float* s_o = reinterpret_cast<float*>(sm + L::kK);   // [Rq][hd] fp32
+#pragma unroll
+            for (int c = 0; c < HD / 16; ++c) {
+                float o16[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o16[i] = 0.f;
+                if (have_o) tmem_ld16(t_o + lane_off + static_cast<uint32_t>(c * 16), o16);
+                if (row_ok) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) s_o[row * HD + c * 16 + i] = o16[i];
+                }
+            }
+            if (row_ok) {
+                s_m[row] = m_used;
+                s_l[row] = l;
+            }
+        }
+    }
+
+    if (!ok) __nanosleep(100000);    // a wait gave up: let copies still in flight land
+    if (C > 1) {
+        __syncthreads();
+        cluster_sync_all();
+        // CTA `rank` combines rows rank, rank + C, ... from all C partials, in split order
+        const uint32_t rank = cluster_ctarank();
+        const uint32_t o_base = smem_u32(sm + L::kK), m_base = smem_u32(s_m), l_base = smem_u32(s_l);
+        const int my_rows = (Rq - static_cast<int>(rank) + C - 1) / C;
+        for (int item = tid; item < my_rows * (HD / 2); item += kThreads) {
+            const int r = static_cast<int>(rank) + (item / (HD / 2)) * C;
+            const int d = (item - (item / (HD / 2)) * (HD / 2)) * 2;
+            float M = -INFINITY;
+            for (int sp = 0; sp < C; ++sp) M = fmaxf(M, dsmem_ld(dsmem_addr(m_base + 4u * r, sp)));
+            float den = 0.f, n0 = 0.f, n1 = 0.f;
+            for (int sp = 0; sp < C; ++sp) {
+                const float ls = dsmem_ld(dsmem_addr(l_base + 4u * r, sp));
+                if (ls <= 0.f) continue;
+                const float w = exp2f(dsmem_ld(dsmem_addr(m_base + 4u * r, sp)) - M);
+                const float2 ov = dsmem_ld2(dsmem_addr(o_base + 4u * (r * HD + d), sp));
+                den = fmaf(ls, w, den);
+                n0 = fmaf(w, ov.x, n0);
+                n1 = fmaf(w, ov.y, n1);
+            }
+            const float inv = (req_ok && den > 0.f) ? 1.f / den : 0.f;
+            const int j = r / G, g = r - (r / G) * G;
+            __nv_bfloat16* dst = out + static_cast<size_t>(b * K + j) * row_stride + static_cast<size_t>(kvh * G + g) * HD + d;
+            *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(n0 * inv, n1 * inv);
+        }
+        cluster_sync_all();           // peers may still be reading this CTA's partial
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+size_t umma_smem_bytes(int hd, int chunk) {
+    const size_t pages = (static_cast<size_t>(chunk) / 16 + 4) * sizeof(int);
+    const size_t base = hd == 128 ? static_cast<size_t>(Layout<128>::kPages) : static_cast<size_t>(Layout<64>::kPages);
+    return base + pages + 1024;
+}
+
+template <int HD>
+int max_active(int C, size_t smem) {
+    static int cache[kMaxCluster + 1] = {};
+    if (cache[C] != 0) return cache[C];
+    cudaFuncSetAttribute(k_attn_umma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaFuncSetAttribute(k_attn_umma<HD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C, C);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = static_cast<unsigned>(C);
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_attn_umma<HD>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = -1;
+    }
+    cache[C] = n == 0 ? -1 : n;
+    return cache[C];
+}
+
+template <int HD>
+int launch_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+              cudaStream_t s, bool pdl) {
+    const size_t smem = umma_smem_bytes(HD, p.chunk);
+    auto kern = k_attn_umma<HD>;
+    static size_t smem_set[64] = {};
+    int dev = 0;
+    PE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64 || smem > smem_set[dev]) {
+        PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+        PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+        if (dev >= 0 && dev < 64) smem_set[dev] = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.B * p.nkv, p.max_splits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = static_cast<unsigned>(p.max_splits);
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    PE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p));
+    return PE_OK;
+}
+
+}  // namespace
+
+AttnPlan plan_attention_umma(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms) {
+    AttnPlan a{};
+    const int max_entries = max_pages * page_size;
+    const int pairs = B * nkv;
+    int want = ceil_div(num_sms, pairs);                 // about one wave of CTAs
+    if (want > kMaxCluster) want = kMaxCluster;
+    if (want < 1) want = 1;
+    int chunk = ceil_div(max_entries, kTile) * kTile;
+    for (int c = want; c >= 2; --c) {
+        const int ch = ceil_div(ceil_div(max_entries, c), kTile) * kTile;
+        const size_t smem = umma_smem_bytes(hd, ch);
+        const int n = hd == 128 ? max_active<128>(c, smem) : max_active<64>(c, smem);
+        if (n > 0 && n >= pairs) {                       // every cluster resident at once
+            chunk = ch;
+            break;
+        }
+    }
+    a.chunk = chunk;
+    a.max_splits = ceil_div(max_entries, chunk);         // one cluster of this many CTAs per (request, kv head)
+    a.ws_floats = 0;
+    a.tickets = 0;
+    (void)K;
+    (void)nq;
+    return a;
+}
+
+int launch_attention_umma(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                          cudaStream_t s, bool pdl) {
+    if (p.hd == 128) return launch_hd<128>(tq, tk, tv, p, s, pdl);
+    if (p.hd == 64) return launch_hd<64>(tq, tk, tv, p, s, pdl);
+    set_error("attention: head_dim must be 64 or 128");
+    return PE_ERR_UNSUPPORTED;
+}
+
+}  // namespace pe

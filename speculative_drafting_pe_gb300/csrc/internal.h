@@ -139,6 +139,11 @@ int launch_attention(int dtype, const AttnParams& p, cudaStream_t s, bool pdl);
 AttnPlan plan_attention_tc(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms);
 int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, cudaStream_t s, bool pdl);
 int encode_tmap_kv(CUtensorMap* map, const void* cache, int hd, int nkv, int num_pages);
+// tcgen05 variant; tq is a 3-D map {hd, nq, rows} over q with box {64, nq/nkv, K}
+AttnPlan plan_attention_umma(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms);
+int launch_attention_umma(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                          cudaStream_t s, bool pdl);
+int encode_tmap_q(CUtensorMap* map, const void* q, int hd, int nq, int rows, int G, int K);
 
 // ---------------------------------------------------------------- verify
 

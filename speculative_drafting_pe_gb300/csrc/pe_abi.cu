@@ -138,6 +138,29 @@ int encode_tmap_kv(CUtensorMap* map, const void* cache, int hd, int nkv, int num
     return PE_OK;
 }
 
+// bf16 query rows q [rows][nq][hd] as a 3-D tensor {hd, nq, rows}; box = the
+// nq/nkv heads of one kv head for the K rows of one request, 64 dims wide.
+int encode_tmap_q(CUtensorMap* map, const void* q, int hd, int nq, int rows, int G, int K) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (fn == nullptr) {
+        set_error("cuTensorMapEncodeTiled entry point not available");
+        return PE_ERR_CUDA;
+    }
+    const uint64_t e = 2;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(hd), static_cast<cuuint64_t>(nq), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {hd * e, static_cast<cuuint64_t>(nq) * hd * e};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(K)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled (q) failed with code " + std::to_string(static_cast<int>(r)));
+        return PE_ERR_CUDA;
+    }
+    return PE_OK;
+}
+
 }  // namespace pe
 
 using namespace pe;
@@ -398,7 +421,7 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     const GemmPlan p_down = plan_gemm(H, R, F, EPI_RESID, eb, h->num_sms, true);
     const GemmPlan p_lm = plan_gemm(V, R, H, EPI_ARGMAX, eb, h->num_sms, true);
     const bool attn_tc = dt == PE_DTYPE_BF16;
-    const AttnPlan p_at = attn_tc ? plan_attention_tc(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms)
+    const AttnPlan p_at = attn_tc ? plan_attention_umma(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms)
                                   : plan_attention(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms);
     if (p_at.ws_floats > h->attn_ws_floats) { set_error("attention scratch too small for this max_pages"); return PE_ERR_ARG; }
 
@@ -409,10 +432,11 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     if ((rc = act_map(h, &tm_xn, h->xn, R, H, bn_rows)) != PE_OK) return rc;
     if ((rc = act_map(h, &tm_attn, h->attn, R, qd, bn_rows)) != PE_OK) return rc;
     if ((rc = act_map(h, &tm_act, h->act, R, F, bn_rows)) != PE_OK) return rc;
-    CUtensorMap tm_kc, tm_vc;
+    CUtensorMap tm_kc, tm_vc, tm_q;
     if (attn_tc) {
         if ((rc = encode_tmap_kv(&tm_kc, k_cache, hd, nkv, num_pages)) != PE_OK) return rc;
         if ((rc = encode_tmap_kv(&tm_vc, v_cache, hd, nkv, num_pages)) != PE_OK) return rc;
+        if ((rc = encode_tmap_q(&tm_q, h->q, hd, nq, R, nq / nkv, K)) != PE_OK) return rc;
     }
 
     GemmParams base{};
@@ -486,7 +510,7 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
             ap.status = status; ap.out = h->attn; ap.ws = h->attn_ws; ap.tickets = h->attn_tickets; ap.err = h->err;
             ap.layer_page0 = l * num_pages;
             rc = run(PE_KERNEL_ATTENTION, [&] {
-                return attn_tc ? launch_attention_tc(tm_kc, tm_vc, ap, s, pdl) : launch_attention(dt, ap, s, pdl);
+                return attn_tc ? launch_attention_umma(tm_q, tm_kc, tm_vc, ap, s, pdl) : launch_attention(dt, ap, s, pdl);
             });
             if (rc != PE_OK) return rc;
         }
