@@ -49,7 +49,7 @@ struct Layout {
     static constexpr int kVt = kV + kStages * kKVBytes;
     static constexpr int kP = kVt + 2 * kVtBytes;
     static constexpr int kBar = kP + 2 * kPBytes;
-    static constexpr int kNumBars = 12;   // q_full, kv_full[3], kv_empty[3], s_full[2], p_full[2], o_done
+    static constexpr int kNumBars = 13;   // q_full, kv_full[3], kv_empty[3], s_full[2], p_full[2], o_done[2]
     static constexpr int kTmem = kBar + kNumBars * 8;
     static constexpr int kPages = kTmem + 16;
 };
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* kv_empty = bars + 4;
     uint64_t* s_full = bars + 7;
     uint64_t* p_full = bars + 9;
-    uint64_t* o_done = bars + 11;
+    uint64_t* o_done = bars + 11;          // [2]: P.V of tiles with this parity complete
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmem);
     int* s_pages = reinterpret_cast<int*>(sm + L::kPages);
     __shared__ float s_m[kRows], s_l[kRows];   // this split's per-row running max (log2) and sum
@@ -127,7 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&s_full[s], 1);
             mbar_init(&p_full[s], 128);
         }
-        mbar_init(o_done, 1);
+        mbar_init(&o_done[0], 1);
+        mbar_init(&o_done[1], 1);
         fence_mbar_init();
     }
     // page coordinates of this CTA's tiles; pages past the request's last
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     UmmaKind<__nv_bfloat16>::mma(t_o, umma_desc_sw128(p_addr + kk * 32),
                                                  umma_desc_sw128(vt_addr + kk * 32), idesc_o,
                                                  (t > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(o_done);
+                umma_commit(&o_done[t & 1]);
                 umma_commit(&kv_empty[t % kStages]);
             }
         }
@@ -244,7 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_used = -INFINITY, l = 0.f;
         for (int t = 0; t < n_tiles; ++t) {
             const int st = t % kStages;
-            if (t >= 1 && !mbar_wait(o_done, static_cast<uint32_t>((t - 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT)) ok = false;
+            // P / V^T buffers (t & 1) were last read by the P.V of tile t-2
+            if (t >= 2 && !mbar_wait(&o_done[t & 1], static_cast<uint32_t>(((t >> 1) - 1) & 1), p.err,
+                                     PE_DEVERR_ATTN_TIMEOUT))
+                ok = false;
             if (ok && !mbar_wait(&kv_full[st], static_cast<uint32_t>((t / kStages) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT))
                 ok = false;
             ok = __all_sync(0xffffffffu, ok);   // keep the warp converged for the .aligned instructions
@@ -307,8 +311,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_used = tmax;
             }
             if (t > 0 && __any_sync(0xffffffffu, need)) {
-                // O holds tiles < t (their PV is complete): scale the rows in
-                // TMEM, the whole warp together (rows that need none use f = 1)
+                // scale the rows of O in TMEM once the P.V of tile t-1 is
+                // complete, the whole warp together (rows that need none use f = 1)
+                bool w_ok = mbar_wait(&o_done[(t - 1) & 1], static_cast<uint32_t>(((t - 1) >> 1) & 1), p.err,
+                                      PE_DEVERR_ATTN_TIMEOUT);
+                w_ok = __all_sync(0xffffffffu, w_ok);
+                if (!w_ok) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
 #pragma unroll
                 for (int c = 0; c < HD / 16; ++c) {
                     float o16[16];
@@ -339,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&p_full[t & 1]);
         }
         if (ok && n_tiles > 0 &&
-            !mbar_wait(o_done, static_cast<uint32_t>((n_tiles - 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT))
+            !mbar_wait(&o_done[(n_tiles - 1) & 1], static_cast<uint32_t>(((n_tiles - 1) >> 1) & 1), p.err,
+                       PE_DEVERR_ATTN_TIMEOUT))
             ok = false;
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after_sync();
