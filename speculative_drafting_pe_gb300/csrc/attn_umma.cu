@@ -28,7 +28,7 @@
 namespace pe {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;      // warps 0-3 softmax, 4 TMA, 5 MMA, 6-9 V transpose
 constexpr int kTile = 64;           // cache entries per tile
 constexpr int kStages = 3;
 constexpr int kRows = 128;          // MMA M (query rows, zero padded)
@@ -49,7 +49,7 @@ struct Layout {
     static constexpr int kVt = kV + kStages * kKVBytes;
     static constexpr int kP = kVt + 2 * kVtBytes;
     static constexpr int kBar = kP + 2 * kPBytes;
-    static constexpr int kNumBars = 13;   // q_full, kv_full[3], kv_empty[3], s_full[2], p_full[2], o_done[2]
+    static constexpr int kNumBars = 15;   // q_full, kv_full[3], kv_empty[3], s_full[2], p_full[2], o_done[2], vt_full[2]
     static constexpr int kTmem = kBar + kNumBars * 8;
     static constexpr int kPages = kTmem + 16;
 };
@@ -64,6 +64,12 @@ __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
 }
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+// 2^x with the hardware approximation (ex2.approx.ftz.f32): 2^-inf = 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -84,6 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* s_full = bars + 7;
     uint64_t* p_full = bars + 9;
     uint64_t* o_done = bars + 11;          // [2]: P.V of tiles with this parity complete
+    uint64_t* vt_full = bars + 13;         // [2]: V^T of tiles with this parity written
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmem);
     int* s_pages = reinterpret_cast<int*>(sm + L::kPages);
     __shared__ float s_m[kRows], s_l[kRows];   // this split's per-row running max (log2) and sum
@@ -129,6 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&o_done[0], 1);
         mbar_init(&o_done[1], 1);
+        mbar_init(&vt_full[0], 128);
+        mbar_init(&vt_full[1], 128);
         fence_mbar_init();
     }
     // page coordinates of this CTA's tiles; pages past the request's last
@@ -218,7 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after_sync();
                     issue_s(t + 1);
                 }
-                if (!mbar_wait(&p_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT)) {
+                if (!mbar_wait(&p_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT) ||
+                    !mbar_wait(&vt_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT)) {
                     ok = false;
                     break;
                 }
@@ -235,6 +245,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (warp >= 6) {
+        // ------------------------------------------------ V transpose warps
+        const int tw = warp - 6;
+        const int mi = lane >> 3, r8 = lane & 7;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t % kStages;
+            // the V^T buffer (t & 1) was last read by the P.V of tile t-2
+            if (t >= 2 && !mbar_wait(&o_done[t & 1], static_cast<uint32_t>(((t >> 1) - 1) & 1), p.err,
+                                     PE_DEVERR_ATTN_TIMEOUT))
+                ok = false;
+            if (ok && !mbar_wait(&kv_full[st], static_cast<uint32_t>((t / kStages) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT))
+                ok = false;
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            // V_t [entries x dims] -> V^T [dims x entries] (K-major for the P.V MMA);
+            // this warp writes dims [tw*hd/4, (tw+1)*hd/4)
+            const uint32_t v_addr = smem_u32(sm + L::kV + st * L::kKVBytes);
+            const uint32_t vt = smem_u32(sm + L::kVt + (t & 1) * L::kVtBytes);
+#pragma unroll
+            for (int db = 0; db < HD / 32; ++db) {
+                const int d0 = tw * (HD / 4) + db * 8;
+                const int c = d0 >> 3;
+#pragma unroll
+                for (int eg = 0; eg < 2; ++eg) {
+                    const int e = eg * 32 + mi * 8 + r8;
+                    const uint32_t addr =
+                        v_addr + static_cast<uint32_t>((c >> 3) * kTile * 128 + e * 128 + (((c & 7) ^ (e & 7)) << 4));
+                    uint32_t rr[4];
+                    ldsm_x4_t(addr, rr[0], rr[1], rr[2], rr[3]);
+                    const int d = d0 + (lane >> 2);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int ee = eg * 32 + q4 * 8 + 2 * (lane & 3);
+                        sts32(vt + static_cast<uint32_t>(d * 128 + ((((ee >> 3) ^ (d & 7))) << 4) + (ee & 7) * 2),
+                              rr[q4]);
+                    }
+                }
+            }
+            fence_proxy_async_smem();     // generic-proxy writes -> visible to the tensor core
+            mbar_arrive(&vt_full[t & 1]);
+        }
     } else {
         // ------------------------------------------------ softmax warps: thread = query row = TMEM lane
         const int row = tid;
@@ -242,48 +293,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = row < Rq;
         const int lim = S + row / G;          // last visible entry of this row
         const float sl2 = rsqrtf(static_cast<float>(HD)) * 1.4426950408889634f;
-        float m_used = -INFINITY, l = 0.f;
+        float m_used = -INFINITY, l = 0.f;    // m_used: running max of the scaled (log2) scores
         for (int t = 0; t < n_tiles; ++t) {
-            const int st = t % kStages;
-            // P / V^T buffers (t & 1) were last read by the P.V of tile t-2
+            // the P buffer (t & 1) was last read by the P.V of tile t-2
             if (t >= 2 && !mbar_wait(&o_done[t & 1], static_cast<uint32_t>(((t >> 1) - 1) & 1), p.err,
                                      PE_DEVERR_ATTN_TIMEOUT))
                 ok = false;
-            if (ok && !mbar_wait(&kv_full[st], static_cast<uint32_t>((t / kStages) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT))
+            if (ok && !mbar_wait(&s_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT))
                 ok = false;
             ok = __all_sync(0xffffffffu, ok);   // keep the warp converged for the .aligned instructions
-            if (!ok) break;
-            tc_fence_after_sync();
-            // V_t -> V^T tile (K-major for the PV MMA); warp w handles dims [w*hd/4, (w+1)*hd/4)
-            {
-                const uint32_t v_addr = smem_u32(sm + L::kV + st * L::kKVBytes);
-                const uint32_t vt = smem_u32(sm + L::kVt + (t & 1) * L::kVtBytes);
-                const int mi = lane >> 3, r8 = lane & 7;
-#pragma unroll
-                for (int db = 0; db < HD / 32; ++db) {
-                    const int d0 = warp * (HD / 4) + db * 8;
-                    const int c = d0 >> 3;
-#pragma unroll
-                    for (int eg = 0; eg < 2; ++eg) {
-                        const int e = eg * 32 + mi * 8 + r8;
-                        const uint32_t addr =
-                            v_addr + static_cast<uint32_t>((c >> 3) * kTile * 128 + e * 128 + (((c & 7) ^ (e & 7)) << 4));
-                        uint32_t rr[4];
-                        ldsm_x4_t(addr, rr[0], rr[1], rr[2], rr[3]);
-                        const int d = d0 + (lane >> 2);
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const int ee = eg * 32 + q4 * 8 + 2 * (lane & 3);
-                            const uint32_t byte =
-                                static_cast<uint32_t>(d * 128 + ((((ee >> 3) ^ (d & 7))) << 4) + (ee & 7) * 2);
-                            sts32(vt + byte, rr[q4]);
-                        }
-                    }
-                }
-            }
-            // S_t row from TMEM
-            if (!mbar_wait(&s_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT)) ok = false;
-            ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after_sync();
             float sv[kTile];
@@ -295,18 +313,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 16; ++i) sv[c * 16 + i] = v16[i];
             }
             const int tbase = e0 + t * kTile;
+            // interior tile: every entry is visible to every row (CTA-uniform)
+            const bool interior = tbase + kTile <= e1 && tbase + kTile <= S + 1;
             float tmax = -INFINITY;
+            if (interior) {
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) {
-                const int e = tbase + i;
-                const bool vis = row_ok && e < e1 && e <= lim;
-                sv[i] = vis ? sv[i] * sl2 : -INFINITY;
-                tmax = fmaxf(tmax, sv[i]);
+                for (int i = 0; i < kTile; ++i) tmax = fmaxf(tmax, sv[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < kTile; ++i) {
+                    const int e = tbase + i;
+                    if (!(row_ok && e < e1 && e <= lim)) sv[i] = -INFINITY;
+                    tmax = fmaxf(tmax, sv[i]);
+                }
             }
+            tmax *= sl2;
             const bool need = tmax > -INFINITY && (m_used == -INFINITY || tmax > m_used + kRescaleLog2);
             float f = 1.f;
             if (need) {
-                f = m_used == -INFINITY ? 0.f : exp2f(m_used - tmax);
+                f = m_used == -INFINITY ? 0.f : ex2_approx(m_used - tmax);
                 l *= f;
                 m_used = tmax;
             }
@@ -330,7 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st16(t_o + lane_off + static_cast<uint32_t>(c * 16), o16);
                 }
             }
-            // P_t row (bf16) into the K-major P tile
+            // P_t row (bf16) into the K-major P tile: p = 2^(s * scale - m)
+            const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
             const uint32_t prow = smem_u32(sm + L::kP + (t & 1) * L::kPBytes) + static_cast<uint32_t>(row * 128);
             float psum = 0.f;
 #pragma unroll
@@ -338,15 +364,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float pv[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float x = sv[c * 8 + i];
-                    pv[i] = (m_used == -INFINITY || x == -INFINITY) ? 0.f : exp2f(x - m_used);
+                    pv[i] = ex2_approx(fmaf(sv[c * 8 + i], sl2, neg_m));
                     psum += pv[i];
                 }
                 sts128(prow + static_cast<uint32_t>((c ^ (row & 7)) << 4), pack_bf16(pv[0], pv[1]),
                        pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
             }
             l += psum;
-            fence_proxy_async_smem();     // generic-proxy writes (V^T, P) -> visible to the tensor core
+            fence_proxy_async_smem();     // generic-proxy writes (P) -> visible to the tensor core
             tc_fence_before_sync();
             mbar_arrive(&p_full[t & 1]);
         }
