@@ -135,11 +135,9 @@ struct AttnPlan {
 };
 AttnPlan plan_attention(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms);
 int launch_attention(int dtype, const AttnParams& p, cudaStream_t s, bool pdl);
-// bf16 tensor-core variant; tk / tv are 4-D maps {hd, 16, nkv, 4 * num_pages}
-AttnPlan plan_attention_tc(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms);
-int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, cudaStream_t s, bool pdl);
+// tk / tv are 4-D maps {hd, 16, nkv, 4 * num_pages} over the paged caches
 int encode_tmap_kv(CUtensorMap* map, const void* cache, int hd, int nkv, int num_pages);
-// tcgen05 variant; tq is a 3-D map {hd, nq, rows} over q with box {64, nq/nkv, K}
+// bf16 tcgen05 attention; tq is a 3-D map {hd, nq, rows} over q with box {64, nq/nkv, K}
 AttnPlan plan_attention_umma(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms);
 int launch_attention_umma(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                           cudaStream_t s, bool pdl);

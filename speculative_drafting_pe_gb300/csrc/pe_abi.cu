@@ -420,8 +420,8 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     const GemmPlan p_gu = plan_gemm(F, R, H, EPI_SWIGLU, eb, h->num_sms, true);
     const GemmPlan p_down = plan_gemm(H, R, F, EPI_RESID, eb, h->num_sms, true);
     const GemmPlan p_lm = plan_gemm(V, R, H, EPI_ARGMAX, eb, h->num_sms, true);
-    const bool attn_tc = dt == PE_DTYPE_BF16;
-    const AttnPlan p_at = attn_tc ? plan_attention_umma(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms)
+    const bool attn_umma = dt == PE_DTYPE_BF16;
+    const AttnPlan p_at = attn_umma ? plan_attention_umma(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms)
                                   : plan_attention(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms);
     if (p_at.ws_floats > h->attn_ws_floats) { set_error("attention scratch too small for this max_pages"); return PE_ERR_ARG; }
 
@@ -433,7 +433,7 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     if ((rc = act_map(h, &tm_attn, h->attn, R, qd, bn_rows)) != PE_OK) return rc;
     if ((rc = act_map(h, &tm_act, h->act, R, F, bn_rows)) != PE_OK) return rc;
     CUtensorMap tm_kc, tm_vc, tm_q;
-    if (attn_tc) {
+    if (attn_umma) {
         if ((rc = encode_tmap_kv(&tm_kc, k_cache, hd, nkv, num_pages)) != PE_OK) return rc;
         if ((rc = encode_tmap_kv(&tm_vc, v_cache, hd, nkv, num_pages)) != PE_OK) return rc;
         if ((rc = encode_tmap_q(&tm_q, h->q, hd, nq, R, nq / nkv, K)) != PE_OK) return rc;
@@ -510,7 +510,7 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
             ap.status = status; ap.out = h->attn; ap.ws = h->attn_ws; ap.tickets = h->attn_tickets; ap.err = h->err;
             ap.layer_page0 = l * num_pages;
             rc = run(PE_KERNEL_ATTENTION, [&] {
-                return attn_tc ? launch_attention_umma(tm_q, tm_kc, tm_vc, ap, s, pdl) : launch_attention(dt, ap, s, pdl);
+                return attn_umma ? launch_attention_umma(tm_q, tm_kc, tm_vc, ap, s, pdl) : launch_attention(dt, ap, s, pdl);
             });
             if (rc != PE_OK) return rc;
         }
