@@ -30,10 +30,9 @@ constexpr int kChunk = 16;                   // accumulator columns per tcgen05.
 constexpr int kPitch = kBM + 4;              // epilogue staging row pitch (floats)
 constexpr int kMaxClusterSplits = 8;         // cluster split-K: at most 8 CTAs per tile
 
-__host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn, bool fused, int bfull_bytes) {
-    size_t off = static_cast<size_t>(stages) * (kABytes + (fused ? 0 : static_cast<size_t>(bn) * kRowBytes));
-    off += static_cast<size_t>(bfull_bytes);
-    off += static_cast<size_t>(2 * stages + 5) * 8;   // mbarriers
+__host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn) {
+    size_t off = static_cast<size_t>(stages) * (kABytes + static_cast<size_t>(bn) * kRowBytes);
+    off += static_cast<size_t>(2 * stages + 4) * 8;   // mbarriers
     off += 16;                                        // TMEM base + flags
     off = (off + 15) & ~static_cast<size_t>(15);
     off += static_cast<size_t>(kChunk) * kPitch * 4;  // epilogue staging tile
@@ -286,59 +285,6 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile
     }
 }
 
-// Fused RMSNorm of the token operand (bf16, token tile <= 16 rows): the 128
-// epilogue threads compute each row's 1/rms from the fp32 residual, then
-// write X[n, k] = bf16(x * inv_rms[n] * gain[k]) for k-blocks kb0..kb1-1
-// in the 128-byte-swizzled K-major layout the MMA reads (rows past N = 0).
-__device__ __forceinline__ void build_normed_operand(const GemmParams& p, uint8_t* sBfull, float* s_inv, int kb0,
-                                                     int kb1, int ew, int lane) {
-    const int N = p.N, Kd = p.Kd, bn = p.bn;
-    // 1. row scales (warp ew takes rows ew, ew+4, ...)
-    for (int n = ew; n < N; n += 4) {
-        const float4* xr = reinterpret_cast<const float4*>(p.norm_x + static_cast<size_t>(n) * Kd);
-        float ss = 0.f;
-        for (int i = lane; i < Kd / 4; i += 32) {
-            const float4 v = xr[i];
-            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        if (lane == 0) s_inv[n] = rsqrtf(ss / static_cast<float>(Kd) + p.norm_eps);
-    }
-    named_bar_sync(1, 128);
-    // 2. the operand: items (k-block, row, 16-byte chunk of 8 elements)
-    const int t = ew * 32 + lane;
-    const int nkb = kb1 - kb0;
-    const __nv_bfloat16* gain = static_cast<const __nv_bfloat16*>(p.norm_gain);
-    for (int item = t; item < nkb * bn * 8; item += 128) {
-        const int c = item & 7;
-        const int n = (item >> 3) % bn;
-        const int kbl = (item >> 3) / bn;
-        const int k = (kb0 + kbl) * 64 + c * 8;
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (n < N && k < Kd) {
-            const float4 x0 = *reinterpret_cast<const float4*>(p.norm_x + static_cast<size_t>(n) * Kd + k);
-            const float4 x1 = *reinterpret_cast<const float4*>(p.norm_x + static_cast<size_t>(n) * Kd + k + 4);
-            const uint4 gr = *reinterpret_cast<const uint4*>(gain + k);
-            const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gr.x));
-            const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gr.y));
-            const float2 g2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gr.z));
-            const float2 g3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gr.w));
-            const float inv = s_inv[n];
-            __nv_bfloat162 o0 = __floats2bfloat162_rn(x0.x * inv * g0.x, x0.y * inv * g0.y);
-            __nv_bfloat162 o1 = __floats2bfloat162_rn(x0.z * inv * g1.x, x0.w * inv * g1.y);
-            __nv_bfloat162 o2 = __floats2bfloat162_rn(x1.x * inv * g2.x, x1.y * inv * g2.y);
-            __nv_bfloat162 o3 = __floats2bfloat162_rn(x1.z * inv * g3.x, x1.w * inv * g3.y);
-            w.x = *reinterpret_cast<uint32_t*>(&o0);
-            w.y = *reinterpret_cast<uint32_t*>(&o1);
-            w.z = *reinterpret_cast<uint32_t*>(&o2);
-            w.w = *reinterpret_cast<uint32_t*>(&o3);
-        }
-        *reinterpret_cast<uint4*>(sBfull + static_cast<size_t>(kbl) * bn * kRowBytes + n * kRowBytes +
-                                  ((c ^ (n & 7)) << 4)) = w;
-    }
-}
-
 // ------------------------------------------------------------ kernel
 
 template <typename T, int EPI>
@@ -349,17 +295,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stages = p.stages;
     const int bn = p.bn;
-    const bool fused = p.norm_x != nullptr;
-    const uint32_t b_bytes = fused ? 0u : static_cast<uint32_t>(bn) * kRowBytes;   // token tile per ring stage
+    const uint32_t b_bytes = static_cast<uint32_t>(bn) * kRowBytes;
     uint8_t* sA = smem;
     uint8_t* sB = smem + static_cast<size_t>(stages) * kABytes;
-    uint8_t* sBfull = sB + static_cast<size_t>(stages) * b_bytes;   // fused-norm token operand
-    uint64_t* full = reinterpret_cast<uint64_t*>(sBfull + p.bfull_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + static_cast<size_t>(stages) * b_bytes);
     uint64_t* empty = full + stages;
     uint64_t* tfull = empty + stages;      // [2] accumulator ready
     uint64_t* tempty = tfull + 2;          // [2] accumulator drained by the epilogue
-    uint64_t* bready = tempty + 2;         // fused-norm token operand written
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bready + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
     int* sflag = reinterpret_cast<int*>(tmem_slot + 1);
     float* stile = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(sflag + 3) + 15) & ~uintptr_t(15));
 
@@ -393,7 +336,6 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], 128);
         }
-        mbar_init(bready, 128);
         sflag[0] = 0;
         sflag[1] = 0;
         fence_mbar_init();
@@ -433,9 +375,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 };
                 auto load_b = [&](int st, int kb) {
-                    if (!fused)
-                        tma_load_2d(sB + static_cast<size_t>(st) * b_bytes, &tmB, &full[st], kb * kBK, n_tile * bn,
-                                    pol_x);
+                    tma_load_2d(sB + static_cast<size_t>(st) * b_bytes, &tmB, &full[st], kb * kBK, n_tile * bn,
+                                pol_x);
                 };
                 int kb = kb0;
                 if (first) {
@@ -477,7 +418,6 @@ __global__ void __launch_bounds__(kThreads, 2)
             uint32_t ph = 0;
             int it = 0;
             bool ok = true;
-            if (fused && !mbar_wait(bready, 0, p.err, PE_DEVERR_GEMM_TIMEOUT)) ok = false;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
                 int m_tile, n_tile, split, kb0, kb1;
                 decode(u, m_tile, n_tile, split, kb0, kb1);
@@ -497,9 +437,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                     tc_fence_after_sync();
                     const uint32_t a_addr = smem_u32(sA + static_cast<size_t>(s) * kABytes);
-                    const uint32_t b_addr =
-                        fused ? smem_u32(sBfull + static_cast<size_t>(kb - kb0) * bn * kRowBytes)
-                              : smem_u32(sB + static_cast<size_t>(s) * b_bytes);
+                    const uint32_t b_addr = smem_u32(sB + static_cast<size_t>(s) * b_bytes);
 #pragma unroll
                     for (int kk = 0; kk < kRowBytes / 32; ++kk) {
                         UmmaKind<T>::mma(d_tmem, umma_desc_sw128(a_addr + kk * 32), umma_desc_sw128(b_addr + kk * 32),
@@ -516,15 +454,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncwarp();
     } else {
-        if constexpr (sizeof(T) == 2) {
-            if (fused) {
-                int m_tile, n_tile, split, kb0, kb1;
-                decode(blockIdx.x, m_tile, n_tile, split, kb0, kb1);
-                build_normed_operand(p, sBfull, stile, kb0, kb1, warp - 2, lane);
-                fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor core
-                mbar_arrive(bready);
-            }
-        }
         int it = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
             int m_tile, n_tile, split, kb0, kb1;
@@ -620,7 +549,7 @@ inline int round_up(int a, int b) { return ceil_div(a, b) * b; }
 
 }  // namespace
 
-GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster, bool fused_norm) {
+GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster) {
     GemmPlan g{};
     const int bk = kRowBytes / elem_bytes;
     g.kb_total = ceil_div(Kd, bk);
@@ -639,7 +568,7 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     const size_t budget = g.bn <= 64 ? 100 * 1024 : 190 * 1024;
     int st = static_cast<int>(budget / stage);
     g.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
-    g.smem_bytes = gemm_smem_bytes(g.stages, g.bn, false, 0);
+    g.smem_bytes = gemm_smem_bytes(g.stages, g.bn);
     const int ctas_per_sm = g.smem_bytes <= 113 * 1024 ? 2 : 1;
     int splits = 1;
     if (epi != EPI_ARGMAX) {
@@ -669,17 +598,6 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
         g.splits = 1;
         g.cluster = false;
     }
-    // Fused RMSNorm: narrow bf16 token tiles with the whole token operand of
-    // the CTA's k-range held in shared memory; the ring then carries weights only.
-    g.fused_norm = fused_norm && elem_bytes == 2 && g.bn == 16 && g.n_tiles == 1;
-    g.bfull_bytes = 0;
-    if (g.fused_norm) {
-        g.bfull_bytes = g.kb_per_split * g.bn * kRowBytes;
-        // ring + operand <= 100 KB keeps two CTAs per SM (with the staging tile)
-        int st2 = static_cast<int>((100 * 1024 - g.bfull_bytes) / kABytes);
-        g.stages = st2 < 2 ? 2 : (st2 > 8 ? 8 : st2);
-        g.smem_bytes = gemm_smem_bytes(g.stages, g.bn, true, g.bfull_bytes);
-    }
     g.units = g.tiles * g.splits;
     // Without split-K the kernel is persistent: one CTA per resident slot
     // walks the tiles with a double-buffered TMEM accumulator, so the
@@ -701,8 +619,6 @@ int launch_gemm(int dtype, int epi, const CUtensorMap& A, const CUtensorMap& A2,
     p.stages = plan.stages;
     p.cluster = plan.cluster ? 1 : 0;
     p.persistent = plan.persistent ? 1 : 0;
-    p.bfull_bytes = plan.bfull_bytes;
-    if (!plan.fused_norm) p.norm_x = nullptr;
     if (dtype == PE_DTYPE_BF16) return launch_dispatch<__nv_bfloat16>(epi, A, A2, B, plan, p, stream, pdl);
     return launch_dispatch<float>(epi, A, A2, B, plan, p, stream, pdl);
 }

@@ -59,14 +59,6 @@ struct GemmParams {
     // otherwise partials go through ws and the tile's ticket
     int cluster;
     int persistent;     // walk units with stride gridDim.x, double-buffered accumulator
-    // Fused RMSNorm of the token operand (narrow token tiles, bf16): when
-    // norm_x is set, each CTA builds X = bf16(norm_x[n] * rsqrt(mean(norm_x[n]^2)
-    // + norm_eps) * norm_gain) for its own k-range in shared memory instead
-    // of loading X through TMA.
-    const float* norm_x;     // [N, Kd] fp32
-    const void* norm_gain;   // [Kd]
-    float norm_eps;
-    int bfull_bytes;         // shared-memory bytes of that operand
     float* ws;
     int* tickets;
     unsigned* err;
@@ -81,11 +73,9 @@ struct GemmPlan {
     bool cluster;       // splits of a tile form one thread-block cluster
     bool persistent;    // grid < units: CTAs loop over tiles
     int grid;           // CTAs launched
-    bool fused_norm;    // token operand normalised in shared memory (see GemmParams::norm_x)
-    int bfull_bytes;
 };
 
-GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster, bool fused_norm = false);
+GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster);
 int launch_gemm(int dtype, int epi, const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B,
                 const GemmPlan& plan, GemmParams p, cudaStream_t stream, bool pdl);
 

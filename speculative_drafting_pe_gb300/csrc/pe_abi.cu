@@ -415,11 +415,9 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     // GEMM plans (bn depends only on the row count)
     const GemmPlan p_fc = plan_gemm(H, B, 3 * H, EPI_STORE, eb, h->num_sms, true);
     const GemmPlan p_qkv0 = plan_gemm(qkv_rows, R, 2 * H, EPI_QKV, eb, h->num_sms, true);
-    // narrow bf16 token tiles: RMSNorm fused into the consuming GEMMs
-    const bool fuse_norm = dt == PE_DTYPE_BF16 && R <= 16;
-    const GemmPlan p_qkv = plan_gemm(qkv_rows, R, H, EPI_QKV, eb, h->num_sms, true, fuse_norm);
+    const GemmPlan p_qkv = plan_gemm(qkv_rows, R, H, EPI_QKV, eb, h->num_sms, true);
     const GemmPlan p_o = plan_gemm(H, R, qd, EPI_RESID, eb, h->num_sms, true);
-    const GemmPlan p_gu = plan_gemm(F, R, H, EPI_SWIGLU, eb, h->num_sms, true, fuse_norm);
+    const GemmPlan p_gu = plan_gemm(F, R, H, EPI_SWIGLU, eb, h->num_sms, true);
     const GemmPlan p_down = plan_gemm(H, R, F, EPI_RESID, eb, h->num_sms, true);
     const GemmPlan p_lm = plan_gemm(V, R, H, EPI_ARGMAX, eb, h->num_sms, true);
     const bool attn_umma = dt == PE_DTYPE_BF16;
@@ -486,7 +484,7 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         const pe_layer_weights& L = h->w.layer[l];
         char* kc = static_cast<char*>(k_cache) + l * layer_elems * h->elem;
         char* vc = static_cast<char*>(v_cache) + l * layer_elems * h->elem;
-        if (l > 0 && !p_qkv.fused_norm) {
+        if (l > 0) {
             rc = run(PE_KERNEL_RMSNORM,
                      [&] { return launch_rmsnorm(dt, h->resid, L.attn_norm, h->xn, R, H, c.rms_eps, s, pdl); });
             if (rc != PE_OK) return rc;
@@ -497,9 +495,6 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
             p.out_act = h->q; p.ld_act = qd;
             p.k_cache = kc; p.v_cache = vc; p.nq_hd = qd; p.nkv = nkv; p.hd = hd;
             p.row_slot = h->row_slot; p.rope_cs = h->rope_cs;
-            if (l > 0 && p_qkv.fused_norm) {
-                p.norm_x = h->resid; p.norm_gain = L.attn_norm; p.norm_eps = c.rms_eps;
-            }
             rc = run(PE_KERNEL_QKV, [&] {
                 return launch_gemm(dt, EPI_QKV, h->tm_qkv[l], h->tm_qkv[l], l == 0 ? tm_u : tm_xn,
                                    l == 0 ? p_qkv0 : p_qkv, p, s, pdl);
@@ -526,17 +521,12 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
                      [&] { return launch_gemm(dt, EPI_RESID, h->tm_o[l], h->tm_o[l], tm_attn, p_o, p, s, pdl); });
             if (rc != PE_OK) return rc;
         }
-        if (!p_gu.fused_norm) {
-            rc = run(PE_KERNEL_RMSNORM,
-                     [&] { return launch_rmsnorm(dt, h->resid, L.mlp_norm, h->xn, R, H, c.rms_eps, s, pdl); });
-            if (rc != PE_OK) return rc;
-        }
+        rc = run(PE_KERNEL_RMSNORM,
+                 [&] { return launch_rmsnorm(dt, h->resid, L.mlp_norm, h->xn, R, H, c.rms_eps, s, pdl); });
+        if (rc != PE_OK) return rc;
         {   // a6: gate/up + SwiGLU, then down + residual
             GemmParams p = base;
             p.M = F; p.Kd = H; p.out_act = h->act; p.ld_act = F;
-            if (p_gu.fused_norm) {
-                p.norm_x = h->resid; p.norm_gain = L.mlp_norm; p.norm_eps = c.rms_eps;
-            }
             rc = run(PE_KERNEL_GATE_UP,
                      [&] { return launch_gemm(dt, EPI_SWIGLU, h->tm_gate[l], h->tm_up[l], tm_xn, p_gu, p, s, pdl); });
             if (rc != PE_OK) return rc;
