@@ -88,16 +88,14 @@ def algorithmic_work(kind, wl, seq_lens):
         kv = ctx * nkv * hd * 2 * e
         flops = sum(4 * nq * hd * (int(S) + j + 1) for S in seq_lens for j in range(K))
         return kv + 2 * R * qd * e, flops
-    if kind == "o_proj":
-        return H * qd * e + R * qd * e + 2 * R * H * 4, 2 * R * H * qd
+    if kind == "o_proj":   # + the folded RMSNorm's gain * r output
+        return H * qd * e + R * qd * e + 2 * R * H * 4 + R * H * e, 2 * R * H * qd
     if kind == "gate_up":
         return 2 * F * H * e + R * H * e + R * F * e, 2 * R * 2 * F * H
     if kind == "down":
-        return H * F * e + R * F * e + 2 * R * H * 4, 2 * R * H * F
+        return H * F * e + R * F * e + 2 * R * H * 4 + R * H * e, 2 * R * H * F
     if kind == "lm_head":
         return V * H * e + R * H * e + R * 8, 2 * R * V * H
-    if kind == "rmsnorm":
-        return R * H * 4 + H * e + R * H * e, 4 * R * H
     if kind == "row_build":
         return R * (3 * H * e + H * 4) + B * H * 4, 8 * R * H
     return R * 12, R
@@ -454,6 +452,7 @@ def bench_ours(args):
         "direct_launch_ms_per_step": direct_ms,
         "roofline": roof,
         "kernel_share": {k: round(v / total_share, 4) for k, v in sorted(shares.items(), key=lambda x: -x[1])},
+        "kernel_ms_per_step": {k: round(v, 4) for k, v in sorted(shares.items(), key=lambda x: -x[1])},
         "clocks": clocks,
         "e2e": {"value": whole_job_steps_per_s(world, args.steps, e2e_ms), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

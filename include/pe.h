@@ -220,7 +220,7 @@ int pe_device_errors(pe_handle* h, void* stream, uint32_t* out_bits);
 /* Kernel kinds of the draft pass, for launch accounting and profiling. */
 #define PE_KERNEL_FC         0
 #define PE_KERNEL_ROW_BUILD  1
-#define PE_KERNEL_RMSNORM    2
+#define PE_KERNEL_RMSNORM    2   /* reserved: RMSNorm is folded into the GEMM epilogues and never launched */
 #define PE_KERNEL_QKV        3
 #define PE_KERNEL_ATTENTION  4
 #define PE_KERNEL_O_PROJ     5

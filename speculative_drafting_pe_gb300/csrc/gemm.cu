@@ -29,13 +29,20 @@ constexpr int kABytes = kBM * kRowBytes;     // 16 KB weight tile per stage
 constexpr int kChunk = 16;                   // accumulator columns per tcgen05.ld
 constexpr int kPitch = kBM + 4;              // epilogue staging row pitch (floats)
 constexpr int kMaxClusterSplits = 8;         // cluster split-K: at most 8 CTAs per tile
+constexpr int kMaxBn = 256;                  // widest token tile
+constexpr int kMaxInvAll = 4096;             // folded-norm scales of up to this many token rows stay in smem
 
-__host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn) {
+// Folded-norm scale slots: every token row of the launch when there are at
+// most kMaxInvAll of them, else two tiles' worth (double-buffered per tile).
+__host__ __device__ inline int inv_slots(int N) { return N <= kMaxInvAll ? ((N + 3) & ~3) : 2 * kMaxBn; }
+
+__host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn, int inv_floats) {
     size_t off = static_cast<size_t>(stages) * (kABytes + static_cast<size_t>(bn) * kRowBytes);
     off += static_cast<size_t>(2 * stages + 4) * 8;   // mbarriers
     off += 16;                                        // TMEM base + flags
     off = (off + 15) & ~static_cast<size_t>(15);
     off += static_cast<size_t>(kChunk) * kPitch * 4;  // epilogue staging tile
+    off += static_cast<size_t>(inv_floats) * 4;       // folded-norm column scales
     return off + 1024;                                // base alignment slack
 }
 
@@ -45,29 +52,73 @@ __host__ __device__ inline uint32_t tmem_cols_for(int bn) {
 
 // ------------------------------------------------------------ epilogues
 
-// Columns i of the chunk with bit i of `colmask` clear are skipped (another
-// CTA of the cluster owns them).
+// The 16 columns of an epilogue chunk: column i is token row n0 + i * cs,
+// valid when i < cnt and the row exists. `slot0` numbers the chunk's columns
+// within the tile's epilogue (the folded-norm partials are kept per slot).
+struct ColMap {
+    int n0, cs, cnt, slot0;
+    __device__ __forceinline__ int col(int i) const { return n0 + i * cs; }
+};
+
 template <typename T, int EPI>
 __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v)[kChunk], int ml, int m_tile,
-                                            int n0, float* stile, uint32_t colmask) {
-    auto col_ok = [&](int i) { return n0 + i < p.N && ((colmask >> i) & 1u); };
+                                            const ColMap& cm, float* stile, float xg_g) {
+    auto col_ok = [&](int i) { return i < cm.cnt && cm.col(i) < p.N; };
     if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
         // all loads of the chunk first, then all stores (the destinations of
         // different columns never alias, but the compiler cannot know that)
         const int m = m_tile * kBM + ml;
+        float r[kChunk];
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) r[i] = 0.f;
         if (m < p.M) {
             float* __restrict__ base = p.out_f32 + m;
-            float old[kChunk];
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) {
-                old[i] = 0.f;
                 if constexpr (EPI == EPI_RESID) {
-                    if (col_ok(i)) old[i] = base[static_cast<size_t>(n0 + i) * p.ld_out];
+                    if (col_ok(i)) r[i] = base[static_cast<size_t>(cm.col(i)) * p.ld_out];
                 }
             }
 #pragma unroll
-            for (int i = 0; i < kChunk; ++i)
-                if (col_ok(i)) base[static_cast<size_t>(n0 + i) * p.ld_out] = old[i] + v[i];
+            for (int i = 0; i < kChunk; ++i) {
+                r[i] += v[i];
+                if (col_ok(i)) base[static_cast<size_t>(cm.col(i)) * p.ld_out] = r[i];
+            }
+        }
+        if constexpr (EPI == EPI_RESID) {
+            if (p.xg != nullptr) {
+                // The next RMSNorm, folded: its consumer reads g * r and
+                // scales by 1/rms after the GEMM, so only the per-row sums of
+                // squares are needed here (this tile's 128 features).
+                const bool mv = m < p.M;
+                T* __restrict__ xg = static_cast<T*>(p.xg) + m;
+                float q[kChunk];
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i) {
+                    const bool ok = mv && col_ok(i);
+                    if (ok) xg[static_cast<size_t>(cm.col(i)) * p.ld_xg] = Elem<T>::from_f(xg_g * r[i]);
+                    q[i] = ok ? r[i] * r[i] : 0.f;
+                }
+                // transpose-reduce over the warp's 32 rows (fixed order), as
+                // in the argmax epilogue: lanes 2c, 2c+1 end with column c
+                const int lane = ml & 31;
+#pragma unroll
+                for (int rd = 0; rd < 4; ++rd) {
+                    const int half = 8 >> rd;
+                    const int bit = 16 >> rd;
+                    const bool upper = (lane & bit) != 0;
+#pragma unroll
+                    for (int j = 0; j < half; ++j) {
+                        const float send = upper ? q[j] : q[j + half];
+                        const float keep = upper ? q[j + half] : q[j];
+                        q[j] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+                    }
+                }
+                q[0] += __shfl_xor_sync(0xffffffffu, q[0], 1);
+                // this warp's partial for chunk column c, in a slot of its own
+                // (the four warps' slots are added by finish_norm_partials)
+                if ((lane & 1) == 0) stile[(ml >> 5) * kMaxBn + cm.slot0 + ((lane >> 1) & 15)] = q[0];
+            }
         }
     } else if constexpr (EPI == EPI_ARGMAX) {
         const int m = m_tile * kBM + ml;
@@ -75,7 +126,7 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
         unsigned long long k[kChunk];
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
-            if (p.logits != nullptr && valid && col_ok(i)) p.logits[static_cast<size_t>(n0 + i) * p.ld_logits + m] = v[i];
+            if (p.logits != nullptr && valid && col_ok(i)) p.logits[static_cast<size_t>(cm.col(i)) * p.ld_logits + m] = v[i];
             k[i] = valid ? argmax_key(v[i], static_cast<uint32_t>(m)) : 0ull;
         }
         // Transpose-reduce over the warp's 32 rows: each round halves the
@@ -100,7 +151,7 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
             k[0] = k[0] > recv ? k[0] : recv;
         }
         const int c = (lane >> 1) & 15;
-        if ((lane & 1) == 0 && col_ok(c) && k[0] != 0ull) atomicMax(p.amax + n0 + c, k[0]);
+        if ((lane & 1) == 0 && col_ok(c) && k[0] != 0ull) atomicMax(p.amax + cm.col(c), k[0]);
     } else if constexpr (EPI == EPI_SWIGLU) {
         // rows 0..63 of the tile are gate rows, 64..127 the matching up rows
         named_bar_sync(1, 128);
@@ -121,7 +172,7 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
 #pragma unroll
             for (int i = 0; i < kChunk / 2; ++i)
                 if (col_ok(ibeg + i))
-                    out[static_cast<size_t>(n0 + ibeg + i) * p.ld_act] = Elem<T>::from_f(silu_f(g[i]) * u[i]);
+                    out[static_cast<size_t>(cm.col(ibeg + i)) * p.ld_act] = Elem<T>::from_f(silu_f(g[i]) * u[i]);
         }
     } else if constexpr (EPI == EPI_QKV) {
         // A 128-row tile holds whole heads of exactly one of q, k, v.
@@ -133,7 +184,7 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
         // loads first: slots of the chunk's rows, RoPE factors, partner values
         int slot[kChunk];
 #pragma unroll
-        for (int i = 0; i < kChunk; ++i) slot[i] = (region > 0 && col_ok(i)) ? p.row_slot[n0 + i] : -1;
+        for (int i = 0; i < kChunk; ++i) slot[i] = (region > 0 && col_ok(i)) ? p.row_slot[cm.col(i)] : -1;
         float outv[kChunk];
         if (region < 2) {
             const int d = ml % hd;
@@ -143,7 +194,7 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
             float2 cs[kChunk];
 #pragma unroll
             for (int i = 0; i < kChunk; ++i)
-                cs[i] = col_ok(i) ? p.rope_cs[static_cast<size_t>(n0 + i) * half + fi] : make_float2(1.f, 0.f);
+                cs[i] = col_ok(i) ? p.rope_cs[static_cast<size_t>(cm.col(i)) * half + fi] : make_float2(1.f, 0.f);
             named_bar_sync(1, 128);
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) stile[i * kPitch + ml] = v[i];
@@ -162,7 +213,7 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
                 T* __restrict__ q = static_cast<T*>(p.out_act) + m;
 #pragma unroll
                 for (int i = 0; i < kChunk; ++i)
-                    if (col_ok(i)) q[static_cast<size_t>(n0 + i) * p.ld_act] = Elem<T>::from_f(outv[i]);
+                    if (col_ok(i)) q[static_cast<size_t>(cm.col(i)) * p.ld_act] = Elem<T>::from_f(outv[i]);
             } else {
                 const int r = m - p.nq_hd - (region == 2 ? p.nkv * hd : 0);
                 const int kvh = r / hd;
@@ -181,9 +232,94 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
     }
 }
 
+// Folded RMSNorm, consumer side: inv[j] = 1/rms of token row n0 + j for
+// j < count, from the producer's partial sums of squares (row n's partials
+// are contiguous, zero-padded to a multiple of 4). Thread t of the 128
+// epilogue threads takes j = t, t + 128, ...; the loads of four such rows are
+// in flight together, and each sum runs in partial order.
+__device__ __forceinline__ void fold_norm_scales(const GemmParams& p, float* inv, int n0, int count, int t) {
+    constexpr int kCols = 4;
+    constexpr int kVec = 4;   // float4 loads per row per round
+    const int nvec = p.ss_ld >> 2;
+    for (int j0 = t; j0 < count; j0 += 128 * kCols) {
+        float ss[kCols];
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) ss[c] = 0.f;
+        for (int v0 = 0; v0 < nvec; v0 += kVec) {
+            float4 x[kCols][kVec];
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) {
+                const int j = j0 + c * 128;
+                const bool ok = j < count && n0 + j < p.N;
+                const float4* src = reinterpret_cast<const float4*>(p.ss_in + static_cast<size_t>(n0 + j) * p.ss_ld);
+#pragma unroll
+                for (int u = 0; u < kVec; ++u)
+                    x[c][u] = (ok && v0 + u < nvec) ? __ldcg(src + v0 + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) {
+#pragma unroll
+                for (int u = 0; u < kVec; ++u) {
+                    ss[c] += x[c][u].x;
+                    ss[c] += x[c][u].y;
+                    ss[c] += x[c][u].z;
+                    ss[c] += x[c][u].w;
+                }
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) {
+            const int j = j0 + c * 128;
+            if (j < count) inv[j] = n0 + j < p.N ? rsqrtf(ss[c] * p.ss_scale + p.ss_eps) : 1.f;
+        }
+    }
+}
+
+// Whether the epilogue scales accumulator columns by the folded norm's
+// 1/rms: only QKV and gate/up, whose epilogues are not linear in a column.
+// The residual GEMMs produce the norm's inputs and never consume them. The
+// LM head's argmax needs no scaling, because 1/rms of a token row is positive
+// and so cannot change which vocabulary entry is largest in that row (its
+// optional logits output is scaled by a separate kernel).
+template <int EPI>
+constexpr bool epi_norm_scaled() { return EPI == EPI_QKV || EPI == EPI_SWIGLU; }
+template <int EPI>
+__device__ __forceinline__ bool norm_scaled(const GemmParams& p) {
+    if constexpr (epi_norm_scaled<EPI>()) return p.ss_in != nullptr;
+    else return false;
+}
+
+// Folded RMSNorm of the B operand: chunk column i (tile column c0 + i * cs,
+// valid for i < cnt) times inv[c0 + i * cs].
+__device__ __forceinline__ void scale_cols(float (&v)[kChunk], const float* inv, int c0, int cs, int cnt) {
+    if (inv == nullptr) return;
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i)
+        if (i < cnt) v[i] *= inv[c0 + i * cs];
+}
+
+// Folded RMSNorm, producer side, after all chunks of a tile: the partial sum
+// of squares of each of the tile's `count` columns (token row n0 + j * cs) is
+// the four warps' slot values added in warp order.
+template <int EPI>
+__device__ __forceinline__ void finish_norm_partials(const GemmParams& p, const float* stile, int m_tile, int n0,
+                                                     int cs, int count, int ml) {
+    if constexpr (EPI == EPI_RESID) {
+        if (p.xg == nullptr) return;
+        named_bar_sync(1, 128);
+        for (int j = ml; j < count; j += 128) {
+            const int n = n0 + j * cs;
+            if (n < p.N)
+                p.ss_out[static_cast<size_t>(n) * p.ss_ld + m_tile] =
+                    ((stile[j] + stile[kMaxBn + j]) + stile[2 * kMaxBn + j]) + stile[3 * kMaxBn + j];
+        }
+    }
+}
+
 template <typename T, int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_acc, float* stile, int* sflag,
-                                              float* part, int m_tile, int n_tile, int split, int warp, int lane) {
+                                              float* part, const float* inv, float xg_g, int m_tile, int n_tile,
+                                              int split, int warp, int lane) {
     const int quad = warp & 3;               // TMEM lane quadrant this warp may read
     const int ml = quad * 32 + lane;         // tile row = TMEM lane
     const uint32_t t_row = t_acc + (static_cast<uint32_t>(quad * 32) << 16);
@@ -244,45 +380,52 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_ac
                     }
                 }
             }
-            apply_chunk<T, EPI>(p, v, ml, m_tile, n_base + c0, stile, 0xFFFFu);
+            scale_cols(v, inv, c0, 1, kChunk);
+            apply_chunk<T, EPI>(p, v, ml, m_tile, ColMap{n_base + c0, 1, kChunk, c0}, stile, xg_g);
         }
+        finish_norm_partials<EPI>(p, stile, m_tile, n_base, 1, bn, ml);
     } else {
         for (int c0 = 0; c0 < bn; c0 += kChunk) {
             float v[kChunk];
             tmem_ld16(t_row + c0, v);
-            apply_chunk<T, EPI>(p, v, ml, m_tile, n_base + c0, stile, 0xFFFFu);
+            scale_cols(v, inv, c0, 1, kChunk);
+            apply_chunk<T, EPI>(p, v, ml, m_tile, ColMap{n_base + c0, 1, kChunk, c0}, stile, xg_g);
         }
+        finish_norm_partials<EPI>(p, stile, m_tile, n_base, 1, bn, ml);
     }
 }
 
 // Cluster split-K, second half: after a cluster barrier, CTA `rank` sums the
-// columns c with c % splits == rank over all peers' partial tiles (read through
-// distributed shared memory, in split order) and applies the epilogue to them.
+// columns c = rank + j * splits over all peers' partial tiles (read through
+// distributed shared memory, in split order) and applies the epilogue to
+// them, 16 of its own columns per chunk.
 template <typename T, int EPI>
-__device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile, const float* part, int m_tile,
-                                               int n_tile, int warp, int lane) {
+__device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile, const float* part,
+                                               const float* inv, float xg_g, int m_tile, int n_tile, int warp,
+                                               int lane) {
     const int ml = (warp & 3) * 32 + lane;
     const int bn = p.bn;
     const int C = p.splits;
     const uint32_t rank = cluster_ctarank();
     const uint32_t base = smem_u32(part);
-    for (int c0 = 0; c0 < bn; c0 += kChunk) {
+    const int first = static_cast<int>(rank);
+    const int owned = first < bn ? (bn - first + C - 1) / C : 0;
+    for (int j0 = 0; j0 < owned; j0 += kChunk) {
+        const int cnt = min(kChunk, owned - j0);
+        const int c0 = first + j0 * C;     // tile column of chunk column 0
         float v[kChunk];
-        uint32_t mask = 0;
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
             v[i] = 0.f;
-            if ((c0 + i) % C == static_cast<int>(rank)) mask |= 1u << i;
-        }
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            if ((mask >> i) & 1u) {
-                const uint32_t a = base + 4u * static_cast<uint32_t>((c0 + i) * kBM + ml);
+            if (i < cnt) {
+                const uint32_t a = base + 4u * static_cast<uint32_t>((c0 + i * C) * kBM + ml);
                 for (int sp = 0; sp < C; ++sp) v[i] += dsmem_ld(dsmem_addr(a, sp));
             }
         }
-        apply_chunk<T, EPI>(p, v, ml, m_tile, n_tile * bn + c0, stile, mask);
+        scale_cols(v, inv, c0, C, cnt);
+        apply_chunk<T, EPI>(p, v, ml, m_tile, ColMap{n_tile * bn + c0, C, cnt, j0}, stile, xg_g);
     }
+    finish_norm_partials<EPI>(p, stile, m_tile, n_tile * bn + first, C, owned, ml);
 }
 
 // ------------------------------------------------------------ kernel
@@ -305,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
     int* sflag = reinterpret_cast<int*>(tmem_slot + 1);
     float* stile = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(sflag + 3) + 15) & ~uintptr_t(15));
+    float* s_inv = stile + kChunk * kPitch;   // [inv_slots(N)] in the QKV and gate/up GEMMs
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -321,6 +465,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         kb1 = min(p.kb_total, kb0 + p.kb_per_split);
     };
     const int nacc = p.persistent ? 2 : 1;           // double-buffered accumulator when persistent
+    const bool inv_all = norm_scaled<EPI>(p) && p.N <= kMaxInvAll;
+    float xg_g = 0.f;                                // folded RMSNorm gain of this epilogue thread's row
     const uint32_t acc_cols = tmem_cols_for(bn);
     const uint32_t tmem_cols = acc_cols * static_cast<uint32_t>(nacc);
 
@@ -454,19 +600,41 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncwarp();
     } else {
+        // Folded RMSNorm: the scales of every token row, computed once while
+        // the first mainloop runs (published by the barrier after the first
+        // accumulator wait), unless there are too many rows for shared memory.
+        if constexpr (epi_norm_scaled<EPI>()) {
+            if (inv_all) fold_norm_scales(p, s_inv, 0, p.N, threadIdx.x - 64);
+        }
         int it = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
             int m_tile, n_tile, split, kb0, kb1;
             decode(u, m_tile, n_tile, split, kb0, kb1);
             const int acc = it % nacc;
             const int use = it / nacc;
+            const float* inv = nullptr;
+            if (inv_all) {
+                inv = s_inv + n_tile * bn;
+            } else if (norm_scaled<EPI>(p)) {
+                if constexpr (epi_norm_scaled<EPI>()) {
+                    // double-buffered: the previous tile's epilogue may still read the other half
+                    float* buf = s_inv + (it & 1) * kMaxBn;
+                    fold_norm_scales(p, buf, n_tile * bn, bn, threadIdx.x - 64);
+                    inv = buf;
+                }
+            }
+            if constexpr (EPI == EPI_RESID) {
+                // gain of this thread's output row for the folded RMSNorm
+                const int m = m_tile * kBM + (warp & 3) * 32 + lane;
+                xg_g = (p.xg != nullptr && m < p.M) ? Elem<T>::to_f(static_cast<const T*>(p.xg_gain)[m]) : 0.f;
+            }
             const bool ok = mbar_wait(&tfull[acc], static_cast<uint32_t>(use & 1), p.err, PE_DEVERR_GEMM_TIMEOUT);
             tc_fence_after_sync();
             if (!ok) sflag[0] = 1;
             named_bar_sync(1, 128);
             if (sflag[0]) break;
             epilogue_tile<T, EPI>(p, tmem_base + static_cast<uint32_t>(acc) * acc_cols, stile, sflag,
-                                  reinterpret_cast<float*>(smem), m_tile, n_tile, split, warp, lane);
+                                  reinterpret_cast<float*>(smem), inv, xg_g, m_tile, n_tile, split, warp, lane);
             tc_fence_before_sync();
             mbar_arrive(&tempty[acc]);
         }
@@ -477,8 +645,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         decode(blockIdx.x, m_tile, n_tile, split, kb0, kb1);
         __syncthreads();              // this CTA's partial is in shared memory
         cluster_sync_all();           // ... and so are the peers'
-        if (warp >= 2 && !sflag[0])
-            cluster_reduce<T, EPI>(p, stile, reinterpret_cast<const float*>(smem), m_tile, n_tile, warp, lane);
+        if (warp >= 2 && !sflag[0]) {
+            const float* inv = inv_all ? s_inv + n_tile * bn : (norm_scaled<EPI>(p) ? s_inv : nullptr);
+            cluster_reduce<T, EPI>(p, stile, reinterpret_cast<const float*>(smem), inv, xg_g, m_tile, n_tile, warp,
+                                   lane);
+        }
         cluster_sync_all();           // peers are done reading this CTA's partial
     }
 
@@ -568,7 +739,7 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     const size_t budget = g.bn <= 64 ? 100 * 1024 : 190 * 1024;
     int st = static_cast<int>(budget / stage);
     g.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
-    g.smem_bytes = gemm_smem_bytes(g.stages, g.bn);
+    g.smem_bytes = gemm_smem_bytes(g.stages, g.bn, (epi == EPI_QKV || epi == EPI_SWIGLU) ? inv_slots(N) : 0);
     const int ctas_per_sm = g.smem_bytes <= 113 * 1024 ? 2 : 1;
     int splits = 1;
     if (epi != EPI_ARGMAX) {

@@ -55,6 +55,22 @@ struct GemmParams {
     unsigned long long* amax;   // [N]
     float* logits;              // [N, ld_logits] or null
     int ld_logits;
+    // Folded RMSNorm, producer side (RESID): besides the residual, write
+    // xg[n, m] = gain[m] * r[n, m] in the activation dtype [N, ld_xg] and this
+    // m tile's partial sum of r[n, :]^2 to ss_out[n * ss_ld + m_tile].
+    void* xg;
+    const void* xg_gain;
+    int ld_xg;
+    float* ss_out;
+    // Folded RMSNorm, consumer side: the B operand is xg; column n of the
+    // accumulator is scaled by rsqrt(sum_q ss_in[n * ss_ld + q] * ss_scale + ss_eps)
+    // (q in order; ss_ld a multiple of 4 and the entries past the producer's
+    // m tiles zero) before the epilogue.
+    const float* ss_in;
+    int ss_parts;
+    int ss_ld;
+    float ss_scale;
+    float ss_eps;
     // split-K: cluster != 0 reduces through distributed shared memory;
     // otherwise partials go through ws and the tile's ticket
     int cluster;
@@ -104,8 +120,10 @@ struct RowBuildParams {
 };
 int launch_row_build(int dtype, const RowBuildParams& p, cudaStream_t s, bool pdl);
 
-int launch_rmsnorm(int dtype, const float* x, const void* gain, void* out, int rows, int H, float eps,
-                   cudaStream_t s, bool pdl);
+// logits[n, :V] *= 1/rms of token row n, from the folded norm's partial sums
+// of squares ss[n * ss_ld + q] (the LM head's optional logits output)
+int launch_logits_rms_scale(float* logits, int rows, int V, int ld, const float* ss, int ss_ld, float scale,
+                            float eps, cudaStream_t s, bool pdl);
 
 int launch_argmax_finalize(const unsigned long long* amax, const int32_t* status, int B, int K, int32_t* drafts,
                            cudaStream_t s, bool pdl);

@@ -34,7 +34,9 @@ struct pe_handle {
     float* h = nullptr;           // [max_batch, H]
     float* resid = nullptr;       // [max_rows, H]
     void* u = nullptr;            // [max_rows, 2H]
-    void* xn = nullptr;           // [max_rows, H]
+    void* xn = nullptr;           // [max_rows, H] gain * residual (folded RMSNorm input)
+    float* ss = nullptr;          // [max_rows, ss_ld] per-128-feature partial sums of squares of the residual
+    int ss_ld = 0;                // ceil(H/128) rounded up to a multiple of 4 (the padding stays zero)
     void* q = nullptr;            // [max_rows, nq*hd]
     void* attn = nullptr;         // [max_rows, nq*hd]
     void* act = nullptr;          // [max_rows, F]
@@ -186,7 +188,7 @@ int act_map(const pe_handle* h, CUtensorMap* m, const void* x, int rows, int col
 void free_handle(pe_handle* h) {
     if (h == nullptr) return;
     for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
-    void* ptrs[] = {h->h,    h->resid,    h->u,        h->xn,         h->q,       h->attn,         h->act,
+    void* ptrs[] = {h->h,    h->resid,    h->u,        h->xn,         h->ss,      h->q,            h->attn,      h->act,
                     h->amax, h->row_slot, h->rope_cs, h->inv_freq, h->gemm_ws, h->gemm_tickets, h->attn_ws,
                     h->attn_tickets, h->err};
     for (void* p : ptrs)
@@ -316,6 +318,8 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
     if (a == PE_OK) a = dev_alloc(&h->resid, R * H * 4);
     if (a == PE_OK) a = dev_alloc(&h->u, R * 2 * H * E);
     if (a == PE_OK) a = dev_alloc(&h->xn, R * H * E);
+    h->ss_ld = (((H + 127) / 128) + 3) / 4 * 4;
+    if (a == PE_OK) a = dev_alloc(&h->ss, static_cast<size_t>(h->ss_ld) * R * 4);
     if (a == PE_OK) a = dev_alloc(&h->q, R * qd * E);
     if (a == PE_OK) a = dev_alloc(&h->attn, R * qd * E);
     if (a == PE_OK) a = dev_alloc(&h->act, R * F * E);
@@ -338,7 +342,8 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
                cudaMemset(h->attn_tickets, 0, static_cast<size_t>(h->attn_tickets_n) * 4) == cudaSuccess &&
                cudaMemset(h->err, 0, 16) == cudaSuccess && cudaMemset(h->u, 0, R * 2 * H * E) == cudaSuccess &&
                cudaMemset(h->xn, 0, R * H * E) == cudaSuccess && cudaMemset(h->attn, 0, R * qd * E) == cudaSuccess &&
-               cudaMemset(h->act, 0, R * F * E) == cudaSuccess;
+               cudaMemset(h->act, 0, R * F * E) == cudaSuccess &&
+               cudaMemset(h->ss, 0, static_cast<size_t>(h->ss_ld) * R * 4) == cudaSuccess;
     std::vector<double> inv(hd / 2);
     for (int i = 0; i < hd / 2; ++i) inv[i] = std::pow(static_cast<double>(cfg->rope_theta), -2.0 * i / hd);
     zok = zok && cudaMemcpy(h->inv_freq, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice) == cudaSuccess;
@@ -445,6 +450,19 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     base.tickets = h->gemm_tickets;
     base.err = h->err;
 
+    // RMSNorm folded into the GEMMs around it: the residual-producing GEMM
+    // (O, down) also writes gain * r and per-tile sums of r^2; the consuming
+    // GEMM (QKV of the next layer, gate/up, LM head) reads gain * r as its B
+    // operand and scales accumulator column n by 1/rms(r[n]), which is the
+    // same product because the GEMM is linear in each token row.
+    auto fold_norm_out = [&](GemmParams& p, const void* gain) {
+        p.xg = h->xn; p.xg_gain = gain; p.ld_xg = H; p.ss_out = h->ss; p.ss_ld = h->ss_ld;
+    };
+    auto fold_norm_in = [&](GemmParams& p) {
+        p.ss_in = h->ss; p.ss_parts = (H + 127) / 128; p.ss_ld = h->ss_ld;
+        p.ss_scale = 1.0f / static_cast<float>(H); p.ss_eps = c.rms_eps;
+    };
+
     // Every launch goes through `run`, which counts it and, when the kernel
     // kind is being profiled, brackets it with CUDA events on stream s.
     auto run = [&](int kind, auto&& fn) -> int {
@@ -484,17 +502,13 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         const pe_layer_weights& L = h->w.layer[l];
         char* kc = static_cast<char*>(k_cache) + l * layer_elems * h->elem;
         char* vc = static_cast<char*>(v_cache) + l * layer_elems * h->elem;
-        if (l > 0) {
-            rc = run(PE_KERNEL_RMSNORM,
-                     [&] { return launch_rmsnorm(dt, h->resid, L.attn_norm, h->xn, R, H, c.rms_eps, s, pdl); });
-            if (rc != PE_OK) return rc;
-        }
         {   // a3: QKV + RoPE + paged KV write
             GemmParams p = base;
             p.M = qkv_rows; p.Kd = l == 0 ? 2 * H : H;
             p.out_act = h->q; p.ld_act = qd;
             p.k_cache = kc; p.v_cache = vc; p.nq_hd = qd; p.nkv = nkv; p.hd = hd;
             p.row_slot = h->row_slot; p.rope_cs = h->rope_cs;
+            if (l > 0) fold_norm_in(p);   // attention RMSNorm of layer l
             rc = run(PE_KERNEL_QKV, [&] {
                 return launch_gemm(dt, EPI_QKV, h->tm_qkv[l], h->tm_qkv[l], l == 0 ? tm_u : tm_xn,
                                    l == 0 ? p_qkv0 : p_qkv, p, s, pdl);
@@ -517,36 +531,41 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         {   // a5: O projection + residual
             GemmParams p = base;
             p.M = H; p.Kd = qd; p.out_f32 = h->resid; p.ld_out = H;
+            fold_norm_out(p, L.mlp_norm);
             rc = run(PE_KERNEL_O_PROJ,
                      [&] { return launch_gemm(dt, EPI_RESID, h->tm_o[l], h->tm_o[l], tm_attn, p_o, p, s, pdl); });
             if (rc != PE_OK) return rc;
         }
-        rc = run(PE_KERNEL_RMSNORM,
-                 [&] { return launch_rmsnorm(dt, h->resid, L.mlp_norm, h->xn, R, H, c.rms_eps, s, pdl); });
-        if (rc != PE_OK) return rc;
         {   // a6: gate/up + SwiGLU, then down + residual
             GemmParams p = base;
             p.M = F; p.Kd = H; p.out_act = h->act; p.ld_act = F;
+            fold_norm_in(p);   // MLP RMSNorm
             rc = run(PE_KERNEL_GATE_UP,
                      [&] { return launch_gemm(dt, EPI_SWIGLU, h->tm_gate[l], h->tm_up[l], tm_xn, p_gu, p, s, pdl); });
             if (rc != PE_OK) return rc;
             GemmParams d = base;
             d.M = H; d.Kd = F; d.out_f32 = h->resid; d.ld_out = H;
+            fold_norm_out(d, l < 3 ? h->w.layer[l + 1].attn_norm : h->w.final_norm);
             rc = run(PE_KERNEL_DOWN,
                      [&] { return launch_gemm(dt, EPI_RESID, h->tm_down[l], h->tm_down[l], tm_act, p_down, d, s, pdl); });
             if (rc != PE_OK) return rc;
         }
     }
-    // a7: final norm, LM head + fused argmax
-    rc = run(PE_KERNEL_RMSNORM,
-             [&] { return launch_rmsnorm(dt, h->resid, h->w.final_norm, h->xn, R, H, c.rms_eps, s, pdl); });
-    if (rc != PE_OK) return rc;
+    // a7: final norm (folded), LM head + fused argmax
     {
         GemmParams p = base;
         p.M = V; p.Kd = H; p.amax = h->amax; p.logits = logits_dbg; p.ld_logits = V;
+        // the argmax is taken on W_lm (g * r): 1/rms(r) > 0 does not move it
         rc = run(PE_KERNEL_LM_HEAD,
                  [&] { return launch_gemm(dt, EPI_ARGMAX, h->tm_lm, h->tm_lm, tm_xn, p_lm, p, s, pdl); });
         if (rc != PE_OK) return rc;
+        if (logits_dbg != nullptr) {
+            rc = run(PE_KERNEL_LM_HEAD, [&] {
+                return launch_logits_rms_scale(logits_dbg, R, V, V, h->ss, h->ss_ld, 1.0f / static_cast<float>(H),
+                                               c.rms_eps, s, pdl);
+            });
+            if (rc != PE_OK) return rc;
+        }
     }
     rc = run(PE_KERNEL_ARGMAX, [&] { return launch_argmax_finalize(h->amax, status, B, K, drafts, s, pdl); });
     if (rc != PE_OK) return rc;

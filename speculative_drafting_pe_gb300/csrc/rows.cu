@@ -1,4 +1,4 @@
-// Row construction, RMSNorm and argmax finalisation.
+// Row construction and argmax finalisation.
 //
 // k_row_build builds the K input rows of every request (P-EAGLE post,
 // "Solution overview / step-by-step drafting", Step 2): row 0 from the real
@@ -157,38 +157,19 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
     }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kRowThreads)
-    k_rmsnorm(const float* __restrict__ x, const T* __restrict__ gain, T* __restrict__ out, int H, float eps) {
-    __shared__ float red[32];
-    const int r = blockIdx.x;
-    const int ng = H / 4;
-    const int tid = threadIdx.x;
-    float4 g4[kMaxG], x4[kMaxG];
-#pragma unroll
-    for (int i = 0; i < kMaxG; ++i) {
-        const int g = tid + i * kRowThreads;
-        if (g < ng) g4[i] = load4(gain + 4 * g);      // weights: before the dependency wait
-    }
+// Debug logits of the LM head (written from the un-normalised operand g * r)
+// scaled to the final RMSNorm: row n times 1/rms(r[n]), the partial sums of
+// squares added in partial order as the folding GEMMs do.
+__global__ void k_logits_rms_scale(float* __restrict__ logits, int V, int ld, const float* __restrict__ ss, int ss_ld,
+                                   float scale, float eps) {
     pdl_launch_dependents();
     pdl_wait();
-    const float* xr = x + static_cast<size_t>(r) * H;
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < kMaxG; ++i) {
-        const int g = tid + i * kRowThreads;
-        if (g < ng) {
-            x4[i] = load4(xr + 4 * g);
-            ss += dot4(x4[i]);
-        }
-    }
-    const float inv = rsqrtf(block_sum(ss, red) / H + eps);
-    T* o = out + static_cast<size_t>(r) * H;
-#pragma unroll
-    for (int i = 0; i < kMaxG; ++i) {
-        const int g = tid + i * kRowThreads;
-        if (g < ng) store4(o + 4 * g, scale4(x4[i], inv, g4[i]));
-    }
+    const int n = blockIdx.y;
+    float sum = 0.f;
+    for (int q = 0; q < ss_ld; ++q) sum += ss[static_cast<size_t>(n) * ss_ld + q];
+    const float inv = rsqrtf(sum * scale + eps);
+    float* row = logits + static_cast<size_t>(n) * ld;
+    for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < V; v += gridDim.x * blockDim.x) row[v] *= inv;
 }
 
 __global__ void k_argmax_finalize(const unsigned long long* __restrict__ amax, const int32_t* __restrict__ status,
@@ -211,15 +192,10 @@ int launch_row_build(int dtype, const RowBuildParams& p, cudaStream_t s, bool pd
     return PE_OK;
 }
 
-int launch_rmsnorm(int dtype, const float* x, const void* gain, void* out, int rows, int H, float eps,
-                   cudaStream_t s, bool pdl) {
-    const dim3 grid(rows), block(kRowThreads);
-    if (dtype == PE_DTYPE_BF16)
-        PE_CUDA_TRY(launch_ex(k_rmsnorm<__nv_bfloat16>, grid, block, 0, s, pdl, x,
-                              static_cast<const __nv_bfloat16*>(gain), static_cast<__nv_bfloat16*>(out), H, eps));
-    else
-        PE_CUDA_TRY(launch_ex(k_rmsnorm<float>, grid, block, 0, s, pdl, x, static_cast<const float*>(gain),
-                              static_cast<float*>(out), H, eps));
+int launch_logits_rms_scale(float* logits, int rows, int V, int ld, const float* ss, int ss_ld, float scale,
+                            float eps, cudaStream_t s, bool pdl) {
+    PE_CUDA_TRY(launch_ex(k_logits_rms_scale, dim3(16, rows), dim3(256), 0, s, pdl, logits, V, ld, ss, ss_ld, scale,
+                          eps));
     return PE_OK;
 }
 
