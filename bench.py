@@ -69,33 +69,60 @@ def workload_desc(wl):
             f"V={s.vocab}, 4 layers, {s.dtype}), B={wl.B}, K={wl.K}, prefix {prefix} in 16-token pages")
 
 
-def algorithmic_work(kind, wl, seq_lens):
+def algorithmic_work(kind, wl, seq_lens, chained=False):
     """Algorithmic HBM bytes and FLOPs of ONE launch of a kernel kind,
-    averaged over that kind's launches in a step."""
+    averaged over that kind's launches in a step. `chained`: the step runs
+    O, gate/up, down and the next QKV (or the LM head) as one persistent
+    layer-chain launch per layer."""
     s = wl.shape
     e = 2 if s.dtype == "bf16" else 4
     H, F, V, hd, nq, nkv = s.hidden, s.ffn, s.vocab, s.head_dim, s.n_q_heads, s.n_kv_heads
     B, K = wl.B, wl.K
     R = B * K
     qd, qkv = nq * hd, s.qkv_rows
+
+    def qkv_work(kin):       # + q out and the new K/V rows
+        return qkv * kin * e + R * kin * e + R * qd * e + R * 2 * nkv * hd * e, 2 * R * qkv * kin
+
+    def o_work():            # + residual read/write and the folded RMSNorm's gain * r output
+        return H * qd * e + R * qd * e + 2 * R * H * 4 + R * H * e, 2 * R * H * qd
+
+    def gu_work():
+        return 2 * F * H * e + R * H * e + R * F * e, 2 * R * 2 * F * H
+
+    def down_work():
+        return H * F * e + R * F * e + 2 * R * H * 4 + R * H * e, 2 * R * H * F
+
+    def lm_work():
+        return V * H * e + R * H * e + R * 8, 2 * R * V * H
+
+    def add(*ws):
+        return sum(w[0] for w in ws), sum(w[1] for w in ws)
+
     if kind == "fc":
         return 3 * H * H * e + B * 3 * H * e + B * H * 4, 2 * B * 3 * H * H
     if kind == "qkv":
-        kin = (2 * H + 3 * H) / 4.0
-        return (qkv * kin * e + R * kin * e + R * qd * e + R * 2 * nkv * hd * e), 2 * R * qkv * kin
+        if chained:          # only layer 0's QKV (2H inputs) runs on its own
+            return qkv_work(2 * H)
+        b, f = add(qkv_work(2 * H), qkv_work(H), qkv_work(H), qkv_work(H))
+        return b / 4.0, f / 4.0
     if kind == "attention":
         ctx = sum(int(S) + K for S in seq_lens)
         kv = ctx * nkv * hd * 2 * e
         flops = sum(4 * nq * hd * (int(S) + j + 1) for S in seq_lens for j in range(K))
         return kv + 2 * R * qd * e, flops
-    if kind == "o_proj":   # + the folded RMSNorm's gain * r output
-        return H * qd * e + R * qd * e + 2 * R * H * 4 + R * H * e, 2 * R * H * qd
+    if kind == "o_proj":
+        return o_work()
     if kind == "gate_up":
-        return 2 * F * H * e + R * H * e + R * F * e, 2 * R * 2 * F * H
+        return gu_work()
     if kind == "down":
-        return H * F * e + R * F * e + 2 * R * H * 4 + R * H * e, 2 * R * H * F
+        return down_work()
     if kind == "lm_head":
-        return V * H * e + R * H * e + R * 8, 2 * R * V * H
+        return lm_work()
+    if kind == "layer_chain":   # three launches end with a QKV, the last with the LM head
+        mid = add(o_work(), gu_work(), down_work(), qkv_work(H))
+        last = add(o_work(), gu_work(), down_work(), lm_work())
+        return (3 * mid[0] + last[0]) / 4.0, (3 * mid[1] + last[1]) / 4.0
     if kind == "row_build":
         return R * (3 * H * e + H * 4) + B * H * 4, 8 * R * H
     return R * 12, R
@@ -410,7 +437,7 @@ def bench_ours(args):
         return
 
     peaks, peaks_src = load_peaks()
-    dom_bytes, dom_flops = algorithmic_work(dominant, wl, seq_np)
+    dom_bytes, dom_flops = algorithmic_work(dominant, wl, seq_np, chained=shares.get("layer_chain", 0.0) > 0.0)
     dom_avg_s = (dom_ms / 1e3) / max(dom_n, 1)
     t_hbm = dom_bytes / (peaks["hbm_gbs"] * 1e9)
     t_tc = dom_flops / (peaks["bf16_tflops_sustained"] * 1e12)

@@ -54,6 +54,7 @@ extern "C" {
 /* bits of the device error word (pe_device_errors) */
 #define PE_DEVERR_GEMM_TIMEOUT  1u
 #define PE_DEVERR_ATTN_TIMEOUT  2u
+#define PE_DEVERR_CHAIN_TIMEOUT 4u   /* the persistent layer-chain kernel */
 
 #define PE_DTYPE_BF16 0         /* bf16 weights/activations/KV, fp32 accumulate */
 #define PE_DTYPE_FP32 1         /* fp32 everything; GEMMs run as tf32 */
@@ -228,7 +229,8 @@ int pe_device_errors(pe_handle* h, void* stream, uint32_t* out_bits);
 #define PE_KERNEL_DOWN       7
 #define PE_KERNEL_LM_HEAD    8
 #define PE_KERNEL_ARGMAX     9
-#define PE_KERNEL_COUNT      10
+#define PE_KERNEL_LAYER_CHAIN 10  /* O, gate/up, down and the next QKV (or the LM head) in one persistent launch */
+#define PE_KERNEL_COUNT      11
 
 /* Measurement hook: after pe_profile_start, every launch of `kernel_kind`
  * made by pe_draft (up to max_launches of them) is bracketed by CUDA events

@@ -24,7 +24,8 @@ EXPORTS = (
     "pe_step_graph_create", "pe_step_graph_launch", "pe_step_graph_launch_count", "pe_step_graph_destroy",
     "pe_linear_noalloc",
 )
-KERNEL_KINDS = ("fc", "row_build", "rmsnorm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "argmax")
+KERNEL_KINDS = ("fc", "row_build", "rmsnorm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "argmax",
+                "layer_chain")
 
 _i32 = ctypes.c_int32
 _vp = ctypes.c_void_p

@@ -101,6 +101,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
     }
 }
 
+// Like mbar_wait, but also gives up as soon as *abort is set (another role of
+// this CTA already gave up, so the phase may never complete).
+__device__ __forceinline__ bool mbar_wait_ab(uint64_t* bar, uint32_t parity, unsigned* err, unsigned err_bit,
+                                             const volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (err) atomicOr(err, err_bit);
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- global flags (GPU scope)
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's generic-proxy global accesses with its later (or, on
+// the writing side, other threads' later) async-proxy accesses such as TMA.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

@@ -95,6 +95,54 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
 int launch_gemm(int dtype, int epi, const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B,
                 const GemmPlan& plan, GemmParams p, cudaStream_t stream, bool pdl);
 
+// ---------------------------------------------------------------- persistent layer chain
+
+// Several weight-streaming GEMMs of one draft pass (O, gate/up, down and the
+// next layer's QKV, or the LM head) in one cooperative launch with one CTA per
+// SM. Each phase's k-blocks are split evenly over the CTAs (a tile shared by
+// several CTAs is summed in CTA order by the last to arrive); the weight ring
+// runs ahead across phases, and a phase's activations are loaded once the
+// previous phase's per-tile completion counter is full.
+constexpr int kMaxChainPhases = 4;
+constexpr int kMaxChainBn = 64;
+
+struct ChainPhase {
+    CUtensorMap tmA;     // weights; SWIGLU: gate rows (64-row boxes)
+    CUtensorMap tmA2;    // SWIGLU: up rows
+    CUtensorMap tmB;     // activations [N, Kd], box rows = bn
+    GemmParams gp;       // epilogue parameters (M, N, Kd, outputs, folded norm)
+    int epi;
+    int m_tiles;         // weight tiles (128 rows; SWIGLU: 64 gate + 64 up)
+    int kb_total;        // 64-element k-blocks per tile
+    int max_segs;        // most CTAs sharing one tile (stride of the partial buffer)
+    long long ws_off;    // this phase's region of the partial buffer (floats)
+    int ticket_off;      // this phase's tickets
+};
+
+struct ChainParams {
+    ChainPhase ph[kMaxChainPhases];
+    int nphases;
+    int bn, stages;
+    unsigned* counters;  // [kMaxChainPhases + 1]: tiles finished per phase, then CTAs finished; zero between launches
+    float* ws;           // partial tiles of shared tiles
+    int* tickets;        // per-tile arrival counts, zero between launches
+    unsigned* err;
+};
+
+struct ChainPlan {
+    int bn, stages, grid;
+    size_t smem_bytes;
+    size_t ws_floats;    // partial buffer of all phases given to chain_plan (one region each)
+    int tickets;         // tickets of all phases (one run each)
+};
+
+// Plan for token rows N and the phases' (m_tiles, kb_total); ok = false when
+// the chain does not apply (N > kMaxChainBn or no co-resident CTA per SM).
+ChainPlan chain_plan(int N, const int* m_tiles, const int* kb_total, int nphases, int num_sms, bool* ok);
+int chain_max_segs(int m_tiles, int kb_total, int grid);
+int launch_chain(const ChainParams& p, const ChainPlan& plan, cudaStream_t s, bool pdl);
+bool chain_supported(int device);
+
 // ---------------------------------------------------------------- small kernels
 
 struct RowBuildParams {

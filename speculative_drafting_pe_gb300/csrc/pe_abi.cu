@@ -53,6 +53,13 @@ struct pe_handle {
     int* attn_tickets = nullptr;
     int attn_tickets_n = 0;
     unsigned* err = nullptr;
+    // persistent layer chain (bf16, up to kMaxChainBn token rows)
+    bool chain = false;
+    unsigned* chain_ctr = nullptr;   // [kMaxChainPhases + 1]
+    float* chain_ws = nullptr;
+    size_t chain_ws_floats = 0;
+    int* chain_tickets = nullptr;
+    int chain_tickets_n = 0;
     // weight tensor maps
     CUtensorMap tm_fc, tm_lm;
     CUtensorMap tm_qkv[4], tm_o[4], tm_gate[4], tm_up[4], tm_down[4];
@@ -190,7 +197,7 @@ void free_handle(pe_handle* h) {
     for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
     void* ptrs[] = {h->h,    h->resid,    h->u,        h->xn,         h->ss,      h->q,            h->attn,      h->act,
                     h->amax, h->row_slot, h->rope_cs, h->inv_freq, h->gemm_ws, h->gemm_tickets, h->attn_ws,
-                    h->attn_tickets, h->err};
+                    h->attn_tickets, h->err, h->chain_ctr, h->chain_ws, h->chain_tickets};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     delete h;
@@ -312,6 +319,24 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
     const size_t pairs_max = static_cast<size_t>(max_batch) * nkv;
     h->attn_ws_floats = (2 * static_cast<size_t>(h->num_sms) + 2 * pairs_max) * (cfg->k_max * G) * (hd + 2);
     h->attn_tickets_n = static_cast<int>(pairs_max);
+    // persistent layer chain: the partial buffer of its two phase lists
+    // (O, gate/up, down, QKV and O, gate/up, down, LM head) at the widest
+    // token tile it serves
+    const char* chain_env = std::getenv("PE_LAYER_CHAIN");
+    h->chain = cfg->dtype == PE_DTYPE_BF16 && chain_env != nullptr && chain_env[0] == '1' &&
+               chain_supported(device);
+    if (h->chain) {
+        const int n_top = h->max_rows < kMaxChainBn ? h->max_rows : kMaxChainBn;
+        const int mt_mid[4] = {(H + 127) / 128, F / 64, (H + 127) / 128, qkv_rows / 128};
+        const int mt_last[4] = {(H + 127) / 128, F / 64, (H + 127) / 128, (V + 127) / 128};
+        const int kb[4] = {qd / 64, H / 64, F / 64, H / 64};
+        bool ok1 = false, ok2 = false;
+        const ChainPlan c1 = chain_plan(n_top, mt_mid, kb, 4, h->num_sms, &ok1);
+        const ChainPlan c2 = chain_plan(n_top, mt_last, kb, 4, h->num_sms, &ok2);
+        h->chain = ok1 && ok2;
+        h->chain_ws_floats = c1.ws_floats > c2.ws_floats ? c1.ws_floats : c2.ws_floats;
+        h->chain_tickets_n = c1.tickets > c2.tickets ? c1.tickets : c2.tickets;
+    }
 
     int a = PE_OK;
     if (a == PE_OK) a = dev_alloc(&h->h, static_cast<size_t>(max_batch) * H * 4);
@@ -332,6 +357,11 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
     if (a == PE_OK) a = dev_alloc(&h->attn_ws, h->attn_ws_floats * 4);
     if (a == PE_OK) a = dev_alloc(&h->attn_tickets, static_cast<size_t>(h->attn_tickets_n) * 4);
     if (a == PE_OK) a = dev_alloc(&h->err, 16);
+    if (h->chain) {
+        if (a == PE_OK) a = dev_alloc(&h->chain_ctr, (kMaxChainPhases + 1) * sizeof(unsigned));
+        if (a == PE_OK) a = dev_alloc(&h->chain_ws, h->chain_ws_floats * 4);
+        if (a == PE_OK) a = dev_alloc(&h->chain_tickets, static_cast<size_t>(h->chain_tickets_n) * 4);
+    }
     if (a != PE_OK) {
         free_handle(h);
         return a;
@@ -343,7 +373,10 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
                cudaMemset(h->err, 0, 16) == cudaSuccess && cudaMemset(h->u, 0, R * 2 * H * E) == cudaSuccess &&
                cudaMemset(h->xn, 0, R * H * E) == cudaSuccess && cudaMemset(h->attn, 0, R * qd * E) == cudaSuccess &&
                cudaMemset(h->act, 0, R * F * E) == cudaSuccess &&
-               cudaMemset(h->ss, 0, static_cast<size_t>(h->ss_ld) * R * 4) == cudaSuccess;
+               cudaMemset(h->ss, 0, static_cast<size_t>(h->ss_ld) * R * 4) == cudaSuccess &&
+               (!h->chain ||
+                (cudaMemset(h->chain_ctr, 0, (kMaxChainPhases + 1) * sizeof(unsigned)) == cudaSuccess &&
+                 cudaMemset(h->chain_tickets, 0, static_cast<size_t>(h->chain_tickets_n) * 4) == cudaSuccess));
     std::vector<double> inv(hd / 2);
     for (int i = 0; i < hd / 2; ++i) inv[i] = std::pow(static_cast<double>(cfg->rope_theta), -2.0 * i / hd);
     zok = zok && cudaMemcpy(h->inv_freq, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice) == cudaSuccess;
@@ -498,17 +531,92 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         if ((rc = run(PE_KERNEL_ROW_BUILD, [&] { return launch_row_build(dt, rp, s, pdl); })) != PE_OK) return rc;
     }
     const size_t layer_elems = static_cast<size_t>(num_pages) * nkv * c.page_size * hd;
+    auto kcache = [&](int l) { return static_cast<char*>(k_cache) + l * layer_elems * h->elem; };
+    auto vcache = [&](int l) { return static_cast<char*>(v_cache) + l * layer_elems * h->elem; };
+    // epilogue parameters of each GEMM of the pass
+    auto gp_qkv = [&](int l) {
+        GemmParams p = base;
+        p.M = qkv_rows; p.Kd = l == 0 ? 2 * H : H;
+        p.out_act = h->q; p.ld_act = qd;
+        p.k_cache = kcache(l); p.v_cache = vcache(l); p.nq_hd = qd; p.nkv = nkv; p.hd = hd;
+        p.row_slot = h->row_slot; p.rope_cs = h->rope_cs;
+        if (l > 0) fold_norm_in(p);   // attention RMSNorm of layer l
+        return p;
+    };
+    auto gp_o = [&](int l) {      // a5: O projection + residual
+        GemmParams p = base;
+        p.M = H; p.Kd = qd; p.out_f32 = h->resid; p.ld_out = H;
+        fold_norm_out(p, h->w.layer[l].mlp_norm);
+        return p;
+    };
+    auto gp_gu = [&](int) {       // a6: gate/up + SwiGLU
+        GemmParams p = base;
+        p.M = F; p.Kd = H; p.out_act = h->act; p.ld_act = F;
+        fold_norm_in(p);   // MLP RMSNorm
+        return p;
+    };
+    auto gp_down = [&](int l) {   // a6: down + residual
+        GemmParams p = base;
+        p.M = H; p.Kd = F; p.out_f32 = h->resid; p.ld_out = H;
+        fold_norm_out(p, l < 3 ? h->w.layer[l + 1].attn_norm : h->w.final_norm);
+        return p;
+    };
+    auto gp_lm = [&]() {          // a7: LM head + fused argmax on W_lm (g * r): 1/rms(r) > 0 does not move it
+        GemmParams p = base;
+        p.M = V; p.Kd = H; p.amax = h->amax; p.logits = logits_dbg; p.ld_logits = V;
+        return p;
+    };
+    // O, gate/up, down of layer l and then the next layer's QKV (or the LM
+    // head) as one persistent launch
+    const bool use_chain = h->chain && R <= kMaxChainBn;
+    auto launch_layer_chain = [&](int l) -> int {
+        ChainParams cp{};
+        cp.nphases = 4;
+        const CUtensorMap* a1[4] = {&h->tm_o[l], &h->tm_gate[l], &h->tm_down[l], l < 3 ? &h->tm_qkv[l + 1] : &h->tm_lm};
+        const CUtensorMap* a2[4] = {&h->tm_o[l], &h->tm_up[l], &h->tm_down[l], l < 3 ? &h->tm_qkv[l + 1] : &h->tm_lm};
+        const CUtensorMap* bm[4] = {&tm_attn, &tm_xn, &tm_act, &tm_xn};
+        const GemmParams gps[4] = {gp_o(l), gp_gu(l), gp_down(l), l < 3 ? gp_qkv(l + 1) : gp_lm()};
+        const int epis[4] = {EPI_RESID, EPI_SWIGLU, EPI_RESID, l < 3 ? EPI_QKV : EPI_ARGMAX};
+        const int mt[4] = {(H + 127) / 128, F / 64, (H + 127) / 128, l < 3 ? qkv_rows / 128 : (V + 127) / 128};
+        const int kb[4] = {qd / 64, H / 64, F / 64, H / 64};
+        bool ok = false;
+        const ChainPlan plan = chain_plan(R, mt, kb, 4, h->num_sms, &ok);
+        if (!ok || plan.ws_floats > h->chain_ws_floats || plan.tickets > h->chain_tickets_n) {
+            set_error("layer chain: plan exceeds the handle's scratch");
+            return PE_ERR_ARG;
+        }
+        long long ws_off = 0;
+        int ticket_off = 0;
+        for (int i = 0; i < 4; ++i) {
+            ChainPhase& ph = cp.ph[i];
+            ph.tmA = *a1[i];
+            ph.tmA2 = *a2[i];
+            ph.tmB = *bm[i];
+            ph.gp = gps[i];
+            ph.gp.bn = plan.bn;
+            ph.epi = epis[i];
+            ph.m_tiles = mt[i];
+            ph.kb_total = kb[i];
+            ph.max_segs = chain_max_segs(mt[i], kb[i], plan.grid);
+            ph.ws_off = ws_off;
+            ph.ticket_off = ticket_off;
+            ws_off += static_cast<long long>(mt[i]) * ph.max_segs * plan.bn * 128;
+            ticket_off += mt[i];
+        }
+        cp.bn = plan.bn;
+        cp.stages = plan.stages;
+        cp.counters = h->chain_ctr;
+        cp.ws = h->chain_ws;
+        cp.tickets = h->chain_tickets;
+        cp.err = h->err;
+        return run(PE_KERNEL_LAYER_CHAIN, [&] { return launch_chain(cp, plan, s, pdl); });
+    };
+
     for (int l = 0; l < 4; ++l) {
-        const pe_layer_weights& L = h->w.layer[l];
-        char* kc = static_cast<char*>(k_cache) + l * layer_elems * h->elem;
-        char* vc = static_cast<char*>(v_cache) + l * layer_elems * h->elem;
-        {   // a3: QKV + RoPE + paged KV write
-            GemmParams p = base;
-            p.M = qkv_rows; p.Kd = l == 0 ? 2 * H : H;
-            p.out_act = h->q; p.ld_act = qd;
-            p.k_cache = kc; p.v_cache = vc; p.nq_hd = qd; p.nkv = nkv; p.hd = hd;
-            p.row_slot = h->row_slot; p.rope_cs = h->rope_cs;
-            if (l > 0) fold_norm_in(p);   // attention RMSNorm of layer l
+        char* kc = kcache(l);
+        char* vc = vcache(l);
+        if (!use_chain || l == 0) {   // a3: QKV + RoPE + paged KV write
+            GemmParams p = gp_qkv(l);
             rc = run(PE_KERNEL_QKV, [&] {
                 return launch_gemm(dt, EPI_QKV, h->tm_qkv[l], h->tm_qkv[l], l == 0 ? tm_u : tm_xn,
                                    l == 0 ? p_qkv0 : p_qkv, p, s, pdl);
@@ -528,44 +636,40 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
             });
             if (rc != PE_OK) return rc;
         }
-        {   // a5: O projection + residual
-            GemmParams p = base;
-            p.M = H; p.Kd = qd; p.out_f32 = h->resid; p.ld_out = H;
-            fold_norm_out(p, L.mlp_norm);
+        if (use_chain) {
+            if ((rc = launch_layer_chain(l)) != PE_OK) return rc;
+            continue;
+        }
+        {
+            GemmParams p = gp_o(l);
             rc = run(PE_KERNEL_O_PROJ,
                      [&] { return launch_gemm(dt, EPI_RESID, h->tm_o[l], h->tm_o[l], tm_attn, p_o, p, s, pdl); });
             if (rc != PE_OK) return rc;
         }
-        {   // a6: gate/up + SwiGLU, then down + residual
-            GemmParams p = base;
-            p.M = F; p.Kd = H; p.out_act = h->act; p.ld_act = F;
-            fold_norm_in(p);   // MLP RMSNorm
+        {
+            GemmParams p = gp_gu(l);
             rc = run(PE_KERNEL_GATE_UP,
                      [&] { return launch_gemm(dt, EPI_SWIGLU, h->tm_gate[l], h->tm_up[l], tm_xn, p_gu, p, s, pdl); });
             if (rc != PE_OK) return rc;
-            GemmParams d = base;
-            d.M = H; d.Kd = F; d.out_f32 = h->resid; d.ld_out = H;
-            fold_norm_out(d, l < 3 ? h->w.layer[l + 1].attn_norm : h->w.final_norm);
+            GemmParams d = gp_down(l);
             rc = run(PE_KERNEL_DOWN,
                      [&] { return launch_gemm(dt, EPI_RESID, h->tm_down[l], h->tm_down[l], tm_act, p_down, d, s, pdl); });
             if (rc != PE_OK) return rc;
         }
     }
-    // a7: final norm (folded), LM head + fused argmax
-    {
-        GemmParams p = base;
-        p.M = V; p.Kd = H; p.amax = h->amax; p.logits = logits_dbg; p.ld_logits = V;
-        // the argmax is taken on W_lm (g * r): 1/rms(r) > 0 does not move it
+    // a7: final norm (folded), LM head + fused argmax (inside the last chain launch when chained)
+    if (!use_chain) {
+        GemmParams p = gp_lm();
         rc = run(PE_KERNEL_LM_HEAD,
                  [&] { return launch_gemm(dt, EPI_ARGMAX, h->tm_lm, h->tm_lm, tm_xn, p_lm, p, s, pdl); });
         if (rc != PE_OK) return rc;
-        if (logits_dbg != nullptr) {
-            rc = run(PE_KERNEL_LM_HEAD, [&] {
-                return launch_logits_rms_scale(logits_dbg, R, V, V, h->ss, h->ss_ld, 1.0f / static_cast<float>(H),
-                                               c.rms_eps, s, pdl);
-            });
-            if (rc != PE_OK) return rc;
-        }
+    }
+    if (logits_dbg != nullptr) {
+        rc = run(PE_KERNEL_LM_HEAD, [&] {
+            return launch_logits_rms_scale(logits_dbg, R, V, V, h->ss, h->ss_ld, 1.0f / static_cast<float>(H),
+                                           c.rms_eps, s, pdl);
+        });
+        if (rc != PE_OK) return rc;
     }
     rc = run(PE_KERNEL_ARGMAX, [&] { return launch_argmax_finalize(h->amax, status, B, K, drafts, s, pdl); });
     if (rc != PE_OK) return rc;
@@ -609,7 +713,8 @@ int pe_profile_stop(pe_handle* h, float* total_ms, int32_t* launches) {
 const char* pe_kernel_name(int32_t kind) {
     static const char* names[PE_KERNEL_COUNT] = {"fc_gemm", "row_build", "rmsnorm", "qkv_rope_kv_gemm",
                                                  "paged_attention", "o_proj_resid_gemm", "gate_up_swiglu_gemm",
-                                                 "down_resid_gemm", "lm_head_argmax_gemm", "argmax_finalize"};
+                                                 "down_resid_gemm", "lm_head_argmax_gemm", "argmax_finalize",
+                                                 "layer_chain"};
     return (kind >= 0 && kind < PE_KERNEL_COUNT) ? names[kind] : "unknown";
 }
 
