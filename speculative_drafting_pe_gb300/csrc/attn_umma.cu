@@ -5,7 +5,8 @@
 // 0 .. S_b + j; scores are scaled by 1/sqrt(hd); softmax is online in fp32
 // (base-2 exponent).
 //
-// One CTA per (request, kv head, entry split); a tile is 64 cache entries
+// One CTA per (request, kv head, entry split), requests issued longest
+// first (an order the row build computes); a tile is 64 cache entries
 // (4 pages). Roles (192 threads):
 //   warp 4   TMA: the packed query rows once (3-D map over q), then K and V
 //            pages of every tile (4-D map over the paged cache) into a
@@ -96,8 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float s_m[kRows], s_l[kRows];   // this split's per-row running max (log2) and sum
 
     const int pair = blockIdx.x;
-    const int b = pair / p.nkv;
-    const int kvh = pair - b * p.nkv;
+    const int kvh = pair % p.nkv;
     const int split = blockIdx.y;
     const int C = gridDim.y;                   // cluster size = entry splits per (request, kv head)
     const int G = p.nq / p.nkv;
@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     pdl_launch_dependents();
     pdl_wait();
+    // the request of this CTA: longest first when an order is given
+    const int b = p.order != nullptr ? p.order[pair / p.nkv] : pair / p.nkv;
 
     // Every CTA of a cluster runs to the end (cluster barriers); CTAs without
     // work contribute an empty partial.

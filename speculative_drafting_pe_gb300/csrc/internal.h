@@ -165,6 +165,7 @@ struct RowBuildParams {
     const double* inv_freq;    // [hd/2]
     unsigned long long* amax;  // OUT [R] zeroed
     int32_t* status;           // OUT [B]
+    int32_t* order;            // OUT [B] or null: requests by decreasing seq_len (ties by index)
 };
 int launch_row_build(int dtype, const RowBuildParams& p, cudaStream_t s, bool pdl);
 
@@ -189,6 +190,7 @@ struct AttnParams {
     const int32_t* page_table;
     const int32_t* seq_lens;
     const int32_t* status;
+    const int32_t* order;     // [B] or null: CTA pair i serves request order[i / nkv] (longest first)
     void* out;                // [R, nq*hd] T
     float* ws;                // split partials
     int* tickets;             // [B*nkv]

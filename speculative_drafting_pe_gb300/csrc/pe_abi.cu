@@ -42,6 +42,7 @@ struct pe_handle {
     void* act = nullptr;          // [max_rows, F]
     unsigned long long* amax = nullptr;
     int* row_slot = nullptr;
+    int32_t* attn_order = nullptr;   // [max_batch] requests by decreasing seq_len
     float2* rope_cs = nullptr;
     double* inv_freq = nullptr;
     float* gemm_ws = nullptr;
@@ -196,7 +197,7 @@ void free_handle(pe_handle* h) {
     if (h == nullptr) return;
     for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
     void* ptrs[] = {h->h,    h->resid,    h->u,        h->xn,         h->ss,      h->q,            h->attn,      h->act,
-                    h->amax, h->row_slot, h->rope_cs, h->inv_freq, h->gemm_ws, h->gemm_tickets, h->attn_ws,
+                    h->amax, h->row_slot, h->attn_order, h->rope_cs, h->inv_freq, h->gemm_ws, h->gemm_tickets, h->attn_ws,
                     h->attn_tickets, h->err, h->chain_ctr, h->chain_ws, h->chain_tickets};
     for (void* p : ptrs)
         if (p) cudaFree(p);
@@ -350,6 +351,7 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
     if (a == PE_OK) a = dev_alloc(&h->act, R * F * E);
     if (a == PE_OK) a = dev_alloc(&h->amax, R * 8);
     if (a == PE_OK) a = dev_alloc(&h->row_slot, R * 4);
+    if (a == PE_OK) a = dev_alloc(&h->attn_order, static_cast<size_t>(max_batch) * 4);
     if (a == PE_OK) a = dev_alloc(&h->rope_cs, R * (hd / 2) * sizeof(float2));
     if (a == PE_OK) a = dev_alloc(&h->inv_freq, (hd / 2) * sizeof(double));
     if (a == PE_OK) a = dev_alloc(&h->gemm_ws, h->gemm_ws_floats * 4);
@@ -528,6 +530,7 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         rp.norm_e = h->w.layer[0].norm_e; rp.norm_h = h->w.layer[0].norm_h; rp.eps = c.rms_eps;
         rp.u = h->u; rp.resid = h->resid; rp.row_slot = h->row_slot; rp.rope_cs = h->rope_cs;
         rp.inv_freq = h->inv_freq; rp.amax = h->amax; rp.status = status;
+        rp.order = attn_umma && B <= 1024 ? h->attn_order : nullptr;
         if ((rc = run(PE_KERNEL_ROW_BUILD, [&] { return launch_row_build(dt, rp, s, pdl); })) != PE_OK) return rc;
     }
     const size_t layer_elems = static_cast<size_t>(num_pages) * nkv * c.page_size * hd;
@@ -629,7 +632,8 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
             ap.max_pages = max_pages; ap.num_pages = num_pages; ap.page_size = c.page_size;
             ap.chunk = p_at.chunk; ap.max_splits = p_at.max_splits;
             ap.q = h->q; ap.k_cache = kc; ap.v_cache = vc; ap.page_table = page_table; ap.seq_lens = seq_lens;
-            ap.status = status; ap.out = h->attn; ap.ws = h->attn_ws; ap.tickets = h->attn_tickets; ap.err = h->err;
+            ap.status = status; ap.out = h->attn;
+            ap.order = attn_umma && B <= 1024 ? h->attn_order : nullptr; ap.ws = h->attn_ws; ap.tickets = h->attn_tickets; ap.err = h->err;
             ap.layer_page0 = l * num_pages;
             rc = run(PE_KERNEL_ATTENTION, [&] {
                 return attn_umma ? launch_attention_umma(tm_q, tm_kc, tm_vc, ap, s, pdl) : launch_attention(dt, ap, s, pdl);

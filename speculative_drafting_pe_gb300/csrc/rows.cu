@@ -99,6 +99,19 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
     const bool ok = st == PE_REQ_OK;
     if (j == 0 && tid == 0) p.status[b] = st;
     if (tid == 0) p.amax[r] = 0ull;
+    if (r == 0 && p.order != nullptr) {
+        // requests by decreasing length (ties by index, so a permutation):
+        // the attention issues its longest (request, kv head) CTAs first
+        for (int q = tid; q < p.B; q += blockDim.x) {
+            const int sq = p.seq_lens[q];
+            int rank = 0;
+            for (int o = 0; o < p.B; ++o) {
+                const int so = p.seq_lens[o];
+                rank += (so > sq || (so == sq && o < q)) ? 1 : 0;
+            }
+            p.order[rank] = q;
+        }
+    }
     if (j == 0) {
         const T* emb = static_cast<const T*>(p.embed) + static_cast<size_t>(ok ? p.last_token[b] : 0) * H;
         const float* h0 = p.h + static_cast<size_t>(b) * H;
