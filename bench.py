@@ -129,13 +129,17 @@ def algorithmic_work(kind, wl, seq_lens, chained=False):
 
 
 def step_bytes(wl, seq_lens):
-    """Algorithmic HBM bytes of one whole step (weights once + KV traffic)."""
+    """Algorithmic HBM bytes of one whole step: every weight matrix once,
+    except the token embedding, of which only the B gathered rows are read;
+    plus the KV cache read (prefix and new entries) and the new entries
+    written."""
     s = wl.shape
     e = 2 if s.dtype == "bf16" else 4
     R = wl.B * wl.K
+    weights = (s.param_count() - s.vocab * s.hidden + wl.B * s.hidden) * e
     kv_read = sum(int(S) + wl.K for S in seq_lens) * s.n_kv_heads * s.head_dim * 2 * e * s.n_layers
     kv_write = R * s.n_kv_heads * s.head_dim * 2 * e * s.n_layers
-    return s.param_count() * e + kv_read + kv_write
+    return weights + kv_read + kv_write
 
 
 class ClockSampler:
