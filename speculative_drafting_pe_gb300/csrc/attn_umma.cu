@@ -10,7 +10,8 @@
 // (4 pages). Roles (192 threads):
 //   warp 4   TMA: the packed query rows once (3-D map over q), then K and V
 //            pages of every tile (4-D map over the paged cache) into a
-//            3-stage ring, 128-byte swizzle.
+//            3-stage ring, 128-byte swizzle. A stage is refilled as soon as
+//            S_t has read K and V_t has been transposed (not after P.V).
 //   warp 5   TMEM allocation; lane 0 issues  S_t = Q K_t^T  (M=128, N=64,
 //            K=hd) into one of two TMEM score buffers, and  O += P_t V_t
 //            (M=128, N=hd, K=64) into the TMEM output accumulator.
@@ -130,7 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(q_full, 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            // free once S = Q K^T has read K (one MMA commit) and the 128
+            // transpose threads have copied V into V^T
+            mbar_init(&kv_empty[s], 1 + 128);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&s_full[s], 1);
@@ -211,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&s_full[t & 1]);
+                umma_commit(&kv_empty[t % kStages]);   // K of this stage is read
             };
             if (!mbar_wait(q_full, 0, p.err, PE_DEVERR_ATTN_TIMEOUT) ||
                 !mbar_wait(&kv_full[0], 0, p.err, PE_DEVERR_ATTN_TIMEOUT)) {
@@ -243,7 +247,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  umma_desc_sw128(vt_addr + kk * 32), idesc_o,
                                                  (t > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(&o_done[t & 1]);
-                umma_commit(&kv_empty[t % kStages]);
             }
         }
         __syncwarp();
@@ -287,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();     // generic-proxy writes -> visible to the tensor core
             mbar_arrive(&vt_full[t & 1]);
+            mbar_arrive(&kv_empty[st]);   // V of this stage is copied
         }
     } else {
         // ------------------------------------------------ softmax warps: thread = query row = TMEM lane
