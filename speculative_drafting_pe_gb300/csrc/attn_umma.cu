@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        __syncwarp();   // reconverge before the CTA-wide barriers below
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0 && n_tiles > 0) {
@@ -481,11 +482,31 @@ size_t umma_smem_bytes(int hd, int chunk) {
     return base + pages + 1024;
 }
 
+// The dynamic shared-memory limit currently set on k_attn_umma<HD> per
+// device: the occupancy queries below change it too, so every launch sets it
+// again whenever it differs.
+template <int HD>
+size_t& smem_attr(int dev) {
+    static size_t now[64] = {};
+    return now[dev >= 0 && dev < 64 ? dev : 0];
+}
+
+template <int HD>
+cudaError_t set_smem_attr(size_t smem) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (smem_attr<HD>(dev) == smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(k_attn_umma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e == cudaSuccess) smem_attr<HD>(dev) = smem;
+    return e;
+}
+
 template <int HD>
 int max_active(int C, size_t smem) {
     static int cache[kMaxCluster + 1] = {};
     if (cache[C] != 0) return cache[C];
-    cudaFuncSetAttribute(k_attn_umma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    set_smem_attr<HD>(smem);
     cudaFuncSetAttribute(k_attn_umma<HD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C, C);
@@ -512,14 +533,8 @@ int launch_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& t
               cudaStream_t s, bool pdl) {
     const size_t smem = umma_smem_bytes(HD, p.chunk);
     auto kern = k_attn_umma<HD>;
-    static size_t smem_set[64] = {};
-    int dev = 0;
-    PE_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= 64 || smem > smem_set[dev]) {
-        PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
-        PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
-        if (dev >= 0 && dev < 64) smem_set[dev] = smem;
-    }
+    PE_CUDA_TRY(set_smem_attr<HD>(smem));
+    PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.B * p.nkv, p.max_splits);
     cfg.blockDim = dim3(kThreads);

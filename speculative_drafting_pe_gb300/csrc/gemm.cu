@@ -463,10 +463,12 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     int splits = 1;
     if (epi != EPI_ARGMAX) {
         if (cluster) {
-            // the splits of a tile form one cluster of <= 8 CTAs; aim at one wave
-            // that leaves room on each SM for the next kernel's CTAs to start
-            // streaming their weights early (programmatic dependent launch)
-            const int target = ctas_per_sm == 2 ? (num_sms * 3) / 2 : num_sms;
+            // the splits of a tile form one cluster of <= 8 CTAs; aim at about
+            // one CTA per SM, which leaves room on each SM for the next
+            // kernel's CTAs to start streaming their weights early
+            // (programmatic dependent launch). The QKV GEMM (RoPE and cache
+            // scatter in its epilogue) measured faster with ~1.5 per SM.
+            const int target = (epi == EPI_QKV && ctas_per_sm == 2) ? (num_sms * 3) / 2 : num_sms;
             const int max_c = kMaxClusterSplits;
             splits = target / g.tiles;
             splits = splits > max_c ? max_c : splits;

@@ -164,6 +164,7 @@ def test_qwen_b1_full_size(K):
 
 
 @pytest.mark.parametrize("name,samples", [("qwen-b128-k11", (0, 77, 127)), ("qwen-b8-k7", (3,)),
+                                          ("qwen-b32-k11", (0, 17, 31)),   # one wave of (request, kv head) attention CTAs
                                           ("gptoss-b64-k10", (0, 63))])
 def test_batched_full_size_sampled(name, samples):
     wl = synth.WORKLOADS[name]
