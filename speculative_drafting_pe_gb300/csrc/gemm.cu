@@ -453,9 +453,12 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     const int rows_per_tile = epi == EPI_SWIGLU ? 64 : kBM;
     g.m_tiles = ceil_div(M, rows_per_tile);
     g.tiles = g.m_tiles * g.n_tiles;
-    // shared-memory ring: ~100 KB (two CTAs per SM) for narrow token tiles
+    // shared-memory ring: ~100 KB (two CTAs per SM, so the next kernel's CTAs
+    // can start their weight loads beside this one) for token tiles up to
+    // 128 rows; ~190 KB above that (at 96 rows the small ring measured 17%
+    // faster per step, at 176 rows its two stages were much slower)
     const size_t stage = kABytes + static_cast<size_t>(g.bn) * kRowBytes;
-    const size_t budget = g.bn <= 64 ? 100 * 1024 : 190 * 1024;
+    const size_t budget = g.bn <= 128 ? 100 * 1024 : 190 * 1024;
     int st = static_cast<int>(budget / stage);
     g.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
     g.smem_bytes = gemm_smem_bytes(g.stages, g.bn, (epi == EPI_QKV || epi == EPI_SWIGLU) ? inv_slots(N) : 0);
