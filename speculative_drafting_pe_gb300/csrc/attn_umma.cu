@@ -447,17 +447,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int item = tid; item < my_rows * (HD / 2); item += kThreads) {
             const int r = static_cast<int>(rank) + (item / (HD / 2)) * C;
             const int d = (item - (item / (HD / 2)) * (HD / 2)) * 2;
+            // every peer's max, sum and output pair in flight at once, then
+            // combined in split order
+            float mv[kMaxCluster], lv[kMaxCluster];
+            float2 ov[kMaxCluster];
+#pragma unroll
+            for (int sp = 0; sp < kMaxCluster; ++sp) {
+                if (sp < C) {
+                    mv[sp] = dsmem_ld(dsmem_addr(m_base + 4u * r, static_cast<uint32_t>(sp)));
+                    lv[sp] = dsmem_ld(dsmem_addr(l_base + 4u * r, static_cast<uint32_t>(sp)));
+                    ov[sp] = dsmem_ld2(dsmem_addr(o_base + 4u * (r * HD + d), static_cast<uint32_t>(sp)));
+                }
+            }
             float M = -INFINITY;
-            for (int sp = 0; sp < C; ++sp) M = fmaxf(M, dsmem_ld(dsmem_addr(m_base + 4u * r, sp)));
+#pragma unroll
+            for (int sp = 0; sp < kMaxCluster; ++sp)
+                if (sp < C) M = fmaxf(M, mv[sp]);
             float den = 0.f, n0 = 0.f, n1 = 0.f;
-            for (int sp = 0; sp < C; ++sp) {
-                const float ls = dsmem_ld(dsmem_addr(l_base + 4u * r, sp));
-                if (ls <= 0.f) continue;
-                const float w = exp2f(dsmem_ld(dsmem_addr(m_base + 4u * r, sp)) - M);
-                const float2 ov = dsmem_ld2(dsmem_addr(o_base + 4u * (r * HD + d), sp));
-                den = fmaf(ls, w, den);
-                n0 = fmaf(w, ov.x, n0);
-                n1 = fmaf(w, ov.y, n1);
+#pragma unroll
+            for (int sp = 0; sp < kMaxCluster; ++sp) {
+                if (sp < C && lv[sp] > 0.f) {
+                    const float w = exp2f(mv[sp] - M);
+                    den = fmaf(lv[sp], w, den);
+                    n0 = fmaf(w, ov[sp].x, n0);
+                    n1 = fmaf(w, ov[sp].y, n1);
+                }
             }
             const float inv = (req_ok && den > 0.f) ? 1.f / den : 0.f;
             const int j = r / G, g = r - (r / G) * G;
