@@ -133,11 +133,26 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile
         const int c0 = first + j0 * C;     // tile column of chunk column 0
         float v[kChunk];
 #pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            v[i] = 0.f;
-            if (i < cnt) {
-                const uint32_t a = base + 4u * static_cast<uint32_t>((c0 + i * C) * kBM + ml);
-                for (int sp = 0; sp < C; ++sp) v[i] += dsmem_ld(dsmem_addr(a, sp));
+        for (int i = 0; i < kChunk; ++i) v[i] = 0.f;
+        // four columns at a time: all their peers' values in flight together,
+        // then added in split order
+#pragma unroll
+        for (int i0 = 0; i0 < kChunk; i0 += 4) {
+            if (i0 < cnt) {
+                float t[4][kMaxClusterSplits];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t a = base + 4u * static_cast<uint32_t>((c0 + (i0 + u) * C) * kBM + ml);
+#pragma unroll
+                    for (int sp = 0; sp < kMaxClusterSplits; ++sp)
+                        if (i0 + u < cnt && sp < C) t[u][sp] = dsmem_ld(dsmem_addr(a, static_cast<uint32_t>(sp)));
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+#pragma unroll
+                    for (int sp = 0; sp < kMaxClusterSplits; ++sp)
+                        if (i0 + u < cnt && sp < C) v[i0 + u] += t[u][sp];
+                }
             }
         }
         scale_cols(v, inv, c0, C, cnt);
