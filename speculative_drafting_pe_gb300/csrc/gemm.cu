@@ -236,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_keep = l2_policy_evict_last();   // weight tiles kept in L2 across steps
             const uint64_t pol_x = l2_policy_evict_last();
             constexpr int kBK = kRowBytes / static_cast<int>(sizeof(T));
             int s = 0;
@@ -250,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                         tma_load_2d(a_dst, &tmA, &full[st], kb * kBK, m_tile * 64, pol_w);
                         tma_load_2d(a_dst + kABytes / 2, &tmA2, &full[st], kb * kBK, m_tile * 64, pol_w);
                     } else {
-                        tma_load_2d(a_dst, &tmA, &full[st], kb * kBK, m_tile * kBM, pol_w);
+                        tma_load_2d(a_dst, &tmA, &full[st], kb * kBK, m_tile * kBM,
+                                    m_tile < p.keep_tiles ? pol_keep : pol_w);
                     }
                 };
                 auto load_b = [&](int st, int kb) {

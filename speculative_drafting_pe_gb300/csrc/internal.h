@@ -78,6 +78,9 @@ struct GemmParams {
     float* ws;
     int* tickets;
     unsigned* err;
+    // weight tiles m_tile < keep_tiles are loaded evict-last (they stay in L2
+    // across steps); the rest evict-first
+    int keep_tiles;
 };
 
 struct GemmPlan {

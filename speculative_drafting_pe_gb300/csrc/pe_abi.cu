@@ -567,6 +567,9 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     auto gp_lm = [&]() {          // a7: LM head + fused argmax on W_lm (g * r): 1/rms(r) > 0 does not move it
         GemmParams p = base;
         p.M = V; p.Kd = H; p.amax = h->amax; p.logits = logits_dbg; p.ld_logits = V;
+        // the LM head's first ~40 MB of weights stay in L2 between steps
+        // (measured: 40 MB faster, 80 and 100 MB slower than none at B=1, B=4)
+        p.keep_tiles = static_cast<int>((40LL << 20) / (128LL * H * static_cast<long long>(h->elem)));
         return p;
     };
     // O, gate/up, down of layer l and then the next layer's QKV (or the LM
