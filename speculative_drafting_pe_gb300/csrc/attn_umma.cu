@@ -10,16 +10,18 @@
 // (4 pages). Roles (192 threads):
 //   warp 4   TMA: the packed query rows once (3-D map over q), then K and V
 //            pages of every tile (4-D map over the paged cache) into a
-//            3-stage ring, 128-byte swizzle. A stage is refilled as soon as
-//            S_t has read K and V_t has been transposed (not after P.V).
+//            4-stage ring, 128-byte swizzle. A stage is refilled once the
+//            P.V of its tile has completed.
 //   warp 5   TMEM allocation; lane 0 issues  S_t = Q K_t^T  (M=128, N=64,
-//            K=hd) into one of two TMEM score buffers, and  O += P_t V_t
-//            (M=128, N=hd, K=64) into the TMEM output accumulator.
-//   warps 0-3  one thread per query row (= TMEM lane): transpose V_t into
-//            a K-major tile with ldmatrix.trans, read the row of S_t from
-//            TMEM, mask, keep the running max, write P_t = exp2(S - m) as
-//            bf16 into shared memory, and rescale the TMEM output row only
-//            when the running max grows by more than 2^8.
+//            K=hd, both operands K-major) into one of two TMEM score
+//            buffers, and  O += P_t V_t  (M=128, N=hd, K=64) into the TMEM
+//            output accumulator. V_t is read where TMA put it, as an
+//            MN-major operand (entries are the reduction dimension, the
+//            64-dim rows the N dimension), so it is never transposed.
+//   warps 0-3  one thread per query row (= TMEM lane): read the row of S_t
+//            from TMEM, mask, keep the running max, write P_t = exp2(S - m)
+//            as bf16 into shared memory, and rescale the TMEM output row
+//            only when the running max grows by more than 2^8.
 // The entry splits of one (request, kv head) form one thread-block cluster
 // and are combined through distributed shared memory in split order.
 #include <cfloat>
@@ -30,9 +32,9 @@
 namespace pe {
 namespace {
 
-constexpr int kThreads = 320;      // warps 0-3 softmax, 4 TMA, 5 MMA, 6-9 V transpose
+constexpr int kThreads = 192;      // warps 0-3 softmax, 4 TMA, 5 MMA
 constexpr int kTile = 64;           // cache entries per tile
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kRows = 128;          // MMA M (query rows, zero padded)
 constexpr int kBoxBytes = 16 * 128; // one page of one kv head, 64 dims
 constexpr float kRescaleLog2 = 8.f;
@@ -43,27 +45,17 @@ struct Layout {
     static constexpr int kSub = HD / 64;                    // 128-byte sub-tiles per row
     static constexpr int kQBytes = kSub * kRows * 128;      // Q: kSub x [128 rows x 128 B]
     static constexpr int kKVBytes = kSub * kTile * 128;     // K or V tile: kSub x [64 entries x 128 B]
-    static constexpr int kVtBytes = HD * 128;               // V^T: [hd rows x 64 entries]
     static constexpr int kPBytes = kRows * 128;             // P: [128 rows x 64 entries]
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kQBytes;
     static constexpr int kV = kK + kStages * kKVBytes;
-    static constexpr int kVt = kV + kStages * kKVBytes;
-    static constexpr int kP = kVt + 2 * kVtBytes;
+    static constexpr int kP = kV + kStages * kKVBytes;
     static constexpr int kBar = kP + 2 * kPBytes;
-    static constexpr int kNumBars = 15;   // q_full, kv_full[3], kv_empty[3], s_full[2], p_full[2], o_done[2], vt_full[2]
+    static constexpr int kNumBars = 1 + 2 * kStages + 6;   // q_full, kv_full[], kv_empty[], s_full[2], p_full[2], o_done[2]
     static constexpr int kTmem = kBar + kNumBars * 8;
     static constexpr int kPages = kTmem + 16;
 };
 
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -88,11 +80,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
     uint64_t* q_full = bars;
     uint64_t* kv_full = bars + 1;
-    uint64_t* kv_empty = bars + 4;
-    uint64_t* s_full = bars + 7;
-    uint64_t* p_full = bars + 9;
-    uint64_t* o_done = bars + 11;          // [2]: P.V of tiles with this parity complete
-    uint64_t* vt_full = bars + 13;         // [2]: V^T of tiles with this parity written
+    uint64_t* kv_empty = kv_full + kStages;
+    uint64_t* s_full = kv_empty + kStages;
+    uint64_t* p_full = s_full + 2;
+    uint64_t* o_done = p_full + 2;         // [2]: P.V of tiles with this parity complete
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmem);
     int* s_pages = reinterpret_cast<int*>(sm + L::kPages);
     __shared__ float s_m[kRows], s_l[kRows];   // this split's per-row running max (log2) and sum
@@ -131,9 +122,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(q_full, 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&kv_full[s], 1);
-            // free once S = Q K^T has read K (one MMA commit) and the 128
-            // transpose threads have copied V into V^T
-            mbar_init(&kv_empty[s], 1 + 128);
+            // free once the P.V of the stage's tile has completed (one MMA
+            // commit; it is issued after the S that read K)
+            mbar_init(&kv_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&s_full[s], 1);
@@ -141,8 +132,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&o_done[0], 1);
         mbar_init(&o_done[1], 1);
-        mbar_init(&vt_full[0], 128);
-        mbar_init(&vt_full[1], 128);
         fence_mbar_init();
     }
     // page coordinates of this CTA's tiles; pages past the request's last
@@ -202,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ MMA issuer
         if (lane == 0 && n_tiles > 0) {
             const uint32_t idesc_s = umma_idesc(1, kRows, kTile);
-            const uint32_t idesc_o = umma_idesc(1, kRows, HD);
+            const uint32_t idesc_o = umma_idesc(1, kRows, HD) | kIdescBMnMajor;
             const uint32_t q_addr = smem_u32(sm + L::kQ);
             auto issue_s = [&](int t) {
                 const uint32_t k_addr = smem_u32(sm + L::kK + (t % kStages) * L::kKVBytes);
@@ -215,7 +204,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&s_full[t & 1]);
-                umma_commit(&kv_empty[t % kStages]);   // K of this stage is read
             };
             if (!mbar_wait(q_full, 0, p.err, PE_DEVERR_ATTN_TIMEOUT) ||
                 !mbar_wait(&kv_full[0], 0, p.err, PE_DEVERR_ATTN_TIMEOUT)) {
@@ -234,65 +222,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after_sync();
                     issue_s(t + 1);
                 }
-                if (!mbar_wait(&p_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT) ||
-                    !mbar_wait(&vt_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT)) {
+                if (!mbar_wait(&p_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t p_addr = smem_u32(sm + L::kP + (t & 1) * L::kPBytes);
-                const uint32_t vt_addr = smem_u32(sm + L::kVt + (t & 1) * L::kVtBytes);
+                const uint32_t v_addr = smem_u32(sm + L::kV + (t % kStages) * L::kKVBytes);
+                // V_t as the MN-major B operand: 16 entries (two 8-row swizzle
+                // atoms, 1024 B apart) per MMA, 64-dim blocks kTile*128 B apart
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
                     UmmaKind<__nv_bfloat16>::mma(t_o, umma_desc_sw128(p_addr + kk * 32),
-                                                 umma_desc_sw128(vt_addr + kk * 32), idesc_o,
+                                                 umma_desc_sw128_mn(v_addr + kk * 16 * 128, kTile * 128), idesc_o,
                                                  (t > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(&o_done[t & 1]);
+                umma_commit(&kv_empty[t % kStages]);   // K and V of this stage are read
             }
         }
         __syncwarp();
-    } else if (warp >= 6) {
-        // ------------------------------------------------ V transpose warps
-        const int tw = warp - 6;
-        const int mi = lane >> 3, r8 = lane & 7;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int st = t % kStages;
-            // the V^T buffer (t & 1) was last read by the P.V of tile t-2
-            if (t >= 2 && !mbar_wait(&o_done[t & 1], static_cast<uint32_t>(((t >> 1) - 1) & 1), p.err,
-                                     PE_DEVERR_ATTN_TIMEOUT))
-                ok = false;
-            if (ok && !mbar_wait(&kv_full[st], static_cast<uint32_t>((t / kStages) & 1), p.err, PE_DEVERR_ATTN_TIMEOUT))
-                ok = false;
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            // V_t [entries x dims] -> V^T [dims x entries] (K-major for the P.V MMA);
-            // this warp writes dims [tw*hd/4, (tw+1)*hd/4)
-            const uint32_t v_addr = smem_u32(sm + L::kV + st * L::kKVBytes);
-            const uint32_t vt = smem_u32(sm + L::kVt + (t & 1) * L::kVtBytes);
-#pragma unroll
-            for (int db = 0; db < HD / 32; ++db) {
-                const int d0 = tw * (HD / 4) + db * 8;
-                const int c = d0 >> 3;
-#pragma unroll
-                for (int eg = 0; eg < 2; ++eg) {
-                    const int e = eg * 32 + mi * 8 + r8;
-                    const uint32_t addr =
-                        v_addr + static_cast<uint32_t>((c >> 3) * kTile * 128 + e * 128 + (((c & 7) ^ (e & 7)) << 4));
-                    uint32_t rr[4];
-                    ldsm_x4_t(addr, rr[0], rr[1], rr[2], rr[3]);
-                    const int d = d0 + (lane >> 2);
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const int ee = eg * 32 + q4 * 8 + 2 * (lane & 3);
-                        sts32(vt + static_cast<uint32_t>(d * 128 + ((((ee >> 3) ^ (d & 7))) << 4) + (ee & 7) * 2),
-                              rr[q4]);
-                    }
-                }
-            }
-            fence_proxy_async_smem();     // generic-proxy writes -> visible to the tensor core
-            mbar_arrive(&vt_full[t & 1]);
-            mbar_arrive(&kv_empty[st]);   // V of this stage is copied
-        }
     } else {
         // ------------------------------------------------ softmax warps: thread = query row = TMEM lane
         const int row = tid;

@@ -197,6 +197,24 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
     return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major operand in the same 128-byte
+// swizzle: each 128-byte row holds 64 consecutive MN elements of one K index,
+// 8 rows (one 1024-byte atom) cover 8 K indices; `mn_stride` bytes separate
+// consecutive 64-element MN blocks (leading byte offset) and atoms of the K
+// dimension follow at 1024 bytes (stride byte offset).
+__device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t smem_addr, uint32_t mn_stride) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction-descriptor bit that reads B as MN-major (16-bit formats only).
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
+
 // Instruction descriptor: dense, D = f32, A/B format (1 = bf16, 2 = tf32),
 // both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
 __host__ __device__ constexpr uint32_t umma_idesc(uint32_t ab_fmt, int M, int N) {
