@@ -39,6 +39,10 @@ constexpr int kRows = 128;          // MMA M (query rows, zero padded)
 constexpr int kBoxBytes = 16 * 128; // one page of one kv head, 64 dims
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxCluster = 16;
+constexpr int kPiecePairs = 16;      // (request, kv head) pairs from which length-aware pieces are used
+constexpr int kPieceMaxBatch = 256;  // requests the row build's piece list serves
+constexpr int kPieceMinTiles = 4;
+
 
 template <int HD>
 struct Layout {
@@ -88,9 +92,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* s_pages = reinterpret_cast<int*>(sm + L::kPages);
     __shared__ float s_m[kRows], s_l[kRows];   // this split's per-row running max (log2) and sum
 
-    const int pair = blockIdx.x;
-    const int kvh = pair % p.nkv;
-    const int split = blockIdx.y;
     const int C = gridDim.y;                   // cluster size = entry splits per (request, kv head)
     const int G = p.nq / p.nkv;
     const int K = p.K;
@@ -101,16 +102,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     pdl_launch_dependents();
     pdl_wait();
-    // the request of this CTA: longest first when an order is given
-    const int b = p.order != nullptr ? p.order[pair / p.nkv] : pair / p.nkv;
+    int b, kvh, e0, e_end;
+    bool single;                               // this CTA alone covers its (request, kv head)
+    if (p.items != nullptr) {
+        // length-aware piece; CTAs past the item count have none
+        if (static_cast<int>(blockIdx.x) >= p.plan[0]) return;
+        const int4 it = p.items[blockIdx.x];
+        b = it.x;
+        kvh = it.y;
+        e0 = it.z;
+        e_end = it.w;
+        single = p.plan[1 + b] <= 1;
+    } else {
+        // the request of this CTA: longest first when an order is given
+        const int pair = blockIdx.x;
+        kvh = pair % p.nkv;
+        b = p.order != nullptr ? p.order[pair / p.nkv] : pair / p.nkv;
+        e0 = static_cast<int>(blockIdx.y) * p.chunk;
+        e_end = e0 + p.chunk;
+        single = C == 1;
+    }
 
     // Every CTA of a cluster runs to the end (cluster barriers); CTAs without
     // work contribute an empty partial.
     const bool req_ok = p.status[b] == PE_REQ_OK;
     const int S = req_ok ? p.seq_lens[b] : 0;
     const int total = S + K;
-    const int e0 = split * p.chunk;
-    const int e1 = req_ok ? min(total, e0 + p.chunk) : e0;
+    const int e1 = req_ok ? min(total, e_end) : e0;
     const int n_tiles = e1 > e0 ? (e1 - e0 + kTile - 1) / kTile : 0;
     const int32_t* pt = p.page_table + static_cast<size_t>(b) * p.max_pages;
     const int last_page = (total - 1) >> 4;
@@ -339,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) l = 0.f;
         const bool have_o = ok && n_tiles > 0;   // warp-uniform
 
-        if (C == 1) {
+        if (single) {
             const int j = row / G, g = row - (row / G) * G;
             __nv_bfloat16* dst = out + static_cast<size_t>(b * K + j) * row_stride + static_cast<size_t>(kvh * G + g) * HD;
             const float inv = (req_ok && have_o && l > 0.f) ? 1.f / l : 0.f;
@@ -362,6 +380,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4*>(dst + c * 16) = w0;
                     *reinterpret_cast<uint4*>(dst + c * 16 + 8) = w1;
                 }
+            }
+        } else if (p.items != nullptr) {
+            // piece partial to global scratch: O [Rq][hd], then the running
+            // max (log2) and sum of each row, for k_attn_merge
+            float* w = p.ws + static_cast<size_t>(blockIdx.x) * attn_piece_floats(Rq, HD);
+#pragma unroll
+            for (int c = 0; c < HD / 16; ++c) {
+                float o16[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o16[i] = 0.f;
+                if (have_o) tmem_ld16(t_o + lane_off + static_cast<uint32_t>(c * 16), o16);
+                if (row_ok) {
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4)
+                        *reinterpret_cast<float4*>(w + row * HD + c * 16 + i) =
+                            make_float4(o16[i], o16[i + 1], o16[i + 2], o16[i + 3]);
+                }
+            }
+            if (row_ok) {
+                w[Rq * HD + row] = m_used;
+                w[Rq * HD + ((Rq + 3) & ~3) + row] = l;
             }
         } else {
             // split partial into this CTA's shared memory (the K stage ring is free)
@@ -436,6 +475,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Combines the pieces of each (request, kv head) that has more than one:
+// with M the largest running max of the pieces, a row's output is
+// sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i. One thread per (query row,
+// pair of dims); the pieces are read eight at a time (all loads of a batch in
+// flight) and folded in piece order with a running max.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeBatch = 8;
+
+template <int HD>
+__global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const AttnParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int b = static_cast<int>(blockIdx.x) / p.nkv;
+    const int kvh = static_cast<int>(blockIdx.x) - b * p.nkv;
+    const int n = p.plan[1 + b];
+    if (n <= 1) return;                        // written by its only piece
+    const int G = p.nq / p.nkv;
+    const int K = p.K;
+    const int Rq = K * G;
+    const int item = static_cast<int>(blockIdx.y) * kMergeThreads + static_cast<int>(threadIdx.x);
+    const int r = item / (HD / 2);
+    if (r >= Rq) return;
+    const int d = (item - r * (HD / 2)) * 2;
+    const int off = p.plan[1 + p.B + b];
+    const int Rq4 = (Rq + 3) & ~3;
+    const size_t pf = attn_piece_floats(Rq, HD);
+    float M = -INFINITY, den = 0.f, n0 = 0.f, n1 = 0.f;
+    for (int i0 = 0; i0 < n; i0 += kMergeBatch) {
+        float mv[kMergeBatch], lv[kMergeBatch];
+        float2 ov[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            mv[u] = -INFINITY;
+            lv[u] = 0.f;
+            ov[u] = make_float2(0.f, 0.f);
+            const int slot = p.nkv * (off + i0 + u) + kvh;
+            if (i0 + u < n && slot < p.grid) {
+                const float* w = p.ws + static_cast<size_t>(slot) * pf;
+                mv[u] = w[Rq * HD + r];
+                lv[u] = w[Rq * HD + Rq4 + r];
+                ov[u] = *reinterpret_cast<const float2*>(w + r * HD + d);
+            }
+        }
+        float bm = M;
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u)
+            if (lv[u] > 0.f) bm = fmaxf(bm, mv[u]);
+        if (bm > M) {
+            // earlier sums are relative to M: bring them to the new maximum
+            const float f = exp2f(M - bm);     // 0 while nothing has been added
+            den *= f;
+            n0 *= f;
+            n1 *= f;
+            M = bm;
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            if (lv[u] > 0.f) {
+                const float f = exp2f(mv[u] - M);
+                den = fmaf(lv[u], f, den);
+                n0 = fmaf(f, ov[u].x, n0);
+                n1 = fmaf(f, ov[u].y, n1);
+            }
+        }
+    }
+    const bool req_ok = p.status[b] == PE_REQ_OK;
+    const float inv = (req_ok && den > 0.f) ? 1.f / den : 0.f;
+    const int j = r / G, g = r - (r / G) * G;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(b * K + j) * p.nq * HD +
+                         static_cast<size_t>(kvh * G + g) * HD + d;
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(n0 * inv, n1 * inv);
+}
+
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 size_t umma_smem_bytes(int hd, int chunk) {
@@ -498,7 +610,7 @@ int launch_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& t
     PE_CUDA_TRY(set_smem_attr<HD>(smem));
     PE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.B * p.nkv, p.max_splits);
+    cfg.gridDim = p.items != nullptr ? dim3(p.grid, 1) : dim3(p.B * p.nkv, p.max_splits);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -507,7 +619,7 @@ int launch_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& t
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = 1;
-    attr[1].val.clusterDim.y = static_cast<unsigned>(p.max_splits);
+    attr[1].val.clusterDim.y = p.items != nullptr ? 1u : static_cast<unsigned>(p.max_splits);
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
@@ -521,6 +633,49 @@ AttnPlan plan_attention_umma(int B, int K, int nq, int nkv, int hd, int max_page
     AttnPlan a{};
     const int max_entries = max_pages * page_size;
     const int pairs = B * nkv;
+    if (pairs >= kPiecePairs && B <= kPieceMaxBatch) {
+        // length-aware pieces while the pairs are fewer than one wave:
+        // about total tiles / slots tiles each, where slots = the CTAs
+        // resident at once, less one per pair when that keeps the pieces to
+        // one wave
+        const int chunk = ceil_div(max_entries, kTile) * kTile;
+        const size_t smem = umma_smem_bytes(hd, chunk);
+        static size_t q_smem[2] = {0, 0};
+        static int q_per_sm[2] = {0, 0};
+        const int hi = hd == 128 ? 1 : 0;
+        if (q_smem[hi] != smem) {
+            int n = 0;
+            cudaError_t e;
+            if (hd == 128) {
+                set_smem_attr<128>(smem);
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_attn_umma<128>, kThreads, smem);
+            } else {
+                set_smem_attr<64>(smem);
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_attn_umma<64>, kThreads, smem);
+            }
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                n = 1;
+            }
+            q_smem[hi] = smem;
+            q_per_sm[hi] = n;
+        }
+        const int per_sm = q_per_sm[hi];
+        const int slots = num_sms * (per_sm > 0 ? per_sm : 1);
+        if (pairs < slots) {
+            a.pieces = true;
+            a.piece_slots = pairs <= slots / 2 ? slots - pairs : slots;
+            a.piece_min_tiles = kPieceMinTiles;
+            a.grid = a.piece_slots + pairs;
+            a.chunk = chunk;
+            a.max_splits = 1;
+            (void)K;
+            (void)nq;
+            return a;
+        }
+        // a wave or more of (request, kv head) CTAs: issuing the longest
+        // first already balances them
+    }
     int want = ceil_div(num_sms, pairs);                 // about one wave of CTAs
     if (want > kMaxCluster) want = kMaxCluster;
     if (want < 1) want = 1;
@@ -549,6 +704,23 @@ int launch_attention_umma(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     if (p.hd == 64) return launch_hd<64>(tq, tk, tv, p, s, pdl);
     set_error("attention: head_dim must be 64 or 128");
     return PE_ERR_UNSUPPORTED;
+}
+
+int launch_attention_merge(const AttnParams& p, cudaStream_t s, bool pdl) {
+    if (p.items == nullptr) return PE_OK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.B * p.nkv, ceil_div(p.K * (p.nq / p.nkv) * (p.hd / 2), kMergeThreads));
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (p.hd == 128) PE_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_attn_merge<128>, p));
+    else PE_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_attn_merge<64>, p));
+    return PE_OK;
 }
 
 }  // namespace pe

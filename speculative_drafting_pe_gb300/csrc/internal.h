@@ -169,6 +169,15 @@ struct RowBuildParams {
     unsigned long long* amax;  // OUT [R] zeroed
     int32_t* status;           // OUT [B]
     int32_t* order;            // OUT [B] or null: requests by decreasing seq_len (ties by index)
+    // Length-aware attention pieces (null: none). Block 0 cuts every
+    // request's S + K cache entries into n_b pieces of about the same tile
+    // count (total tiles / piece_slots, at least piece_min_tiles) and writes
+    // one item {b, kv head, first entry, end entry} per (piece, kv head),
+    // longest requests first; item (nkv * (off_b + i) + kv head) is piece i
+    // of request b. attn_plan: [0] item count, [1 + b] n_b, [1 + B + b] off_b.
+    int4* attn_items;
+    int* attn_plan;
+    int nkv, piece_slots, piece_min_tiles;
 };
 int launch_row_build(int dtype, const RowBuildParams& p, cudaStream_t s, bool pdl);
 
@@ -198,11 +207,22 @@ struct AttnParams {
     float* ws;                // split partials
     int* tickets;             // [B*nkv]
     unsigned* err;
+    // length-aware pieces (tcgen05 kernel; null: one cluster of max_splits
+    // CTAs per (request, kv head)): CTA i serves items[i] while i < plan[0];
+    // a piece of a request with several writes its partial (O, running max,
+    // sum) to ws[i] and k_attn_merge combines them
+    const int4* items;
+    const int* plan;
+    int grid;                 // CTAs launched (>= the item count)
 };
 struct AttnPlan {
     int chunk, max_splits;
     size_t ws_floats;
     int tickets;
+    bool pieces;              // length-aware pieces + merge kernel
+    int piece_slots;          // CTAs resident at once (SMs x CTAs per SM)
+    int piece_min_tiles;
+    int grid;                 // piece_slots + B * nkv
 };
 AttnPlan plan_attention(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms);
 int launch_attention(int dtype, const AttnParams& p, cudaStream_t s, bool pdl);
@@ -212,6 +232,13 @@ int encode_tmap_kv(CUtensorMap* map, const void* cache, int hd, int nkv, int num
 AttnPlan plan_attention_umma(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms);
 int launch_attention_umma(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                           cudaStream_t s, bool pdl);
+// combines the pieces of every (request, kv head) with more than one
+int launch_attention_merge(const AttnParams& p, cudaStream_t s, bool pdl);
+// floats of one piece partial in the attention scratch: O [Rq][hd], then the
+// running max [Rq] and sum [Rq], each block a multiple of 16 bytes
+__host__ __device__ inline size_t attn_piece_floats(int Rq, int hd) {
+    return static_cast<size_t>(Rq) * hd + 2 * static_cast<size_t>((Rq + 3) & ~3);
+}
 int encode_tmap_q(CUtensorMap* map, const void* q, int hd, int nq, int rows, int G, int K);
 
 // ---------------------------------------------------------------- verify

@@ -53,6 +53,9 @@ struct pe_handle {
     size_t attn_ws_floats = 0;
     int* attn_tickets = nullptr;
     int attn_tickets_n = 0;
+    int4* attn_items = nullptr;      // [attn_items_n] length-aware attention pieces
+    int attn_items_n = 0;
+    int* attn_plan = nullptr;        // [1 + 2 * max_batch] piece count, pieces and first piece per request
     unsigned* err = nullptr;
     // persistent layer chain (bf16, up to kMaxChainBn token rows)
     bool chain = false;
@@ -198,7 +201,8 @@ void free_handle(pe_handle* h) {
     for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
     void* ptrs[] = {h->h,    h->resid,    h->u,        h->xn,         h->ss,      h->q,            h->attn,      h->act,
                     h->amax, h->row_slot, h->attn_order, h->rope_cs, h->inv_freq, h->gemm_ws, h->gemm_tickets, h->attn_ws,
-                    h->attn_tickets, h->err, h->chain_ctr, h->chain_ws, h->chain_tickets};
+                    h->attn_tickets, h->err, h->chain_ctr, h->chain_ws, h->chain_tickets, h->attn_items,
+                    h->attn_plan};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     delete h;
@@ -320,6 +324,7 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
     const size_t pairs_max = static_cast<size_t>(max_batch) * nkv;
     h->attn_ws_floats = (2 * static_cast<size_t>(h->num_sms) + 2 * pairs_max) * (cfg->k_max * G) * (hd + 2);
     h->attn_tickets_n = static_cast<int>(pairs_max);
+    h->attn_items_n = 2 * h->num_sms + static_cast<int>(pairs_max);
     // persistent layer chain: the partial buffer of its two phase lists
     // (O, gate/up, down, QKV and O, gate/up, down, LM head) at the widest
     // token tile it serves
@@ -358,6 +363,8 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
     if (a == PE_OK) a = dev_alloc(&h->gemm_tickets, static_cast<size_t>(h->gemm_tickets_n) * 4);
     if (a == PE_OK) a = dev_alloc(&h->attn_ws, h->attn_ws_floats * 4);
     if (a == PE_OK) a = dev_alloc(&h->attn_tickets, static_cast<size_t>(h->attn_tickets_n) * 4);
+    if (a == PE_OK) a = dev_alloc(&h->attn_items, static_cast<size_t>(h->attn_items_n) * sizeof(int4));
+    if (a == PE_OK) a = dev_alloc(&h->attn_plan, (1 + 2 * static_cast<size_t>(max_batch)) * 4);
     if (a == PE_OK) a = dev_alloc(&h->err, 16);
     if (h->chain) {
         if (a == PE_OK) a = dev_alloc(&h->chain_ctr, (kMaxChainPhases + 1) * sizeof(unsigned));
@@ -464,6 +471,11 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     const AttnPlan p_at = attn_umma ? plan_attention_umma(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms)
                                   : plan_attention(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms);
     if (p_at.ws_floats > h->attn_ws_floats) { set_error("attention scratch too small for this max_pages"); return PE_ERR_ARG; }
+    if (p_at.pieces && (p_at.grid > h->attn_items_n ||
+                        static_cast<size_t>(p_at.grid) * attn_piece_floats(K * (nq / nkv), hd) > h->attn_ws_floats)) {
+        set_error("attention piece scratch too small");
+        return PE_ERR_ARG;
+    }
 
     CUtensorMap tm_th, tm_u, tm_xn, tm_attn, tm_act;
     const int bn_rows = p_qkv.bn;   // all row-count-R GEMMs share bn
@@ -500,11 +512,12 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
 
     // Every launch goes through `run`, which counts it and, when the kernel
     // kind is being profiled, brackets it with CUDA events on stream s.
-    auto run = [&](int kind, auto&& fn) -> int {
+    // `kernels`: launches fn makes (one profiled interval for all of them)
+    auto run = [&](int kind, auto&& fn, int kernels = 1) -> int {
         const bool prof = h->prof_kind == kind && h->prof_used + 2 <= static_cast<int>(h->prof_events.size());
         if (prof) cudaEventRecord(h->prof_events[h->prof_used], s);
         const int r = fn();
-        if (r == PE_OK) ++launches;
+        if (r == PE_OK) launches += kernels;
         if (prof) {
             cudaEventRecord(h->prof_events[h->prof_used + 1], s);
             h->prof_used += 2;
@@ -530,7 +543,12 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         rp.norm_e = h->w.layer[0].norm_e; rp.norm_h = h->w.layer[0].norm_h; rp.eps = c.rms_eps;
         rp.u = h->u; rp.resid = h->resid; rp.row_slot = h->row_slot; rp.rope_cs = h->rope_cs;
         rp.inv_freq = h->inv_freq; rp.amax = h->amax; rp.status = status;
-        rp.order = attn_umma && B <= 1024 ? h->attn_order : nullptr;
+        rp.order = attn_umma && B <= 1024 && !p_at.pieces ? h->attn_order : nullptr;
+        rp.attn_items = p_at.pieces ? h->attn_items : nullptr;
+        rp.attn_plan = h->attn_plan;
+        rp.nkv = nkv;
+        rp.piece_slots = p_at.piece_slots;
+        rp.piece_min_tiles = p_at.piece_min_tiles;
         if ((rc = run(PE_KERNEL_ROW_BUILD, [&] { return launch_row_build(dt, rp, s, pdl); })) != PE_OK) return rc;
     }
     const size_t layer_elems = static_cast<size_t>(num_pages) * nkv * c.page_size * hd;
@@ -638,9 +656,19 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
             ap.status = status; ap.out = h->attn;
             ap.order = attn_umma && B <= 1024 ? h->attn_order : nullptr; ap.ws = h->attn_ws; ap.tickets = h->attn_tickets; ap.err = h->err;
             ap.layer_page0 = l * num_pages;
-            rc = run(PE_KERNEL_ATTENTION, [&] {
-                return attn_umma ? launch_attention_umma(tm_q, tm_kc, tm_vc, ap, s, pdl) : launch_attention(dt, ap, s, pdl);
-            });
+            ap.items = p_at.pieces ? h->attn_items : nullptr;
+            ap.plan = h->attn_plan;
+            ap.grid = p_at.grid;
+            // with length-aware pieces the merge kernel follows in the same
+            // profiled interval (one attention per layer)
+            rc = run(
+                PE_KERNEL_ATTENTION,
+                [&] {
+                    if (!attn_umma) return launch_attention(dt, ap, s, pdl);
+                    const int r = launch_attention_umma(tm_q, tm_kc, tm_vc, ap, s, pdl);
+                    return (r == PE_OK && p_at.pieces) ? launch_attention_merge(ap, s, pdl) : r;
+                },
+                p_at.pieces ? 2 : 1);
             if (rc != PE_OK) return rc;
         }
         if (use_chain) {

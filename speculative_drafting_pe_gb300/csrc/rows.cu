@@ -17,6 +17,8 @@ namespace pe {
 namespace {
 
 constexpr int kRowThreads = 256;
+constexpr int kMaxPieceB = 256;   // requests the attention piece list serves
+constexpr int kPieceTile = 64;    // cache entries per attention tile
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
@@ -110,6 +112,85 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
                 rank += (so > sq || (so == sq && o < q)) ? 1 : 0;
             }
             p.order[rank] = q;
+        }
+    }
+    if (r == 0 && p.attn_items != nullptr) {
+        // Length-aware attention pieces. tiles_b = ceil((S_b + K) / 64) for a
+        // request whose entries fit its page table (none otherwise); a piece
+        // holds about tc = total tiles / piece_slots of them; pieces are
+        // listed largest first (requests ranked by piece size, ties by index),
+        // so the CTAs dispatched first carry the most work.
+        __shared__ int s_t[kMaxPieceB], s_sz[kMaxPieceB], s_req[kMaxPieceB], s_off[kMaxPieceB + 1];
+        __shared__ int s_total;
+        if (tid == 0) s_total = 0;
+        __syncthreads();
+        const long long cap = static_cast<long long>(p.max_pages) * p.page_size;
+        for (int q = tid; q < p.B; q += blockDim.x) {
+            const int sq = p.seq_lens[q];
+            const bool fits = sq >= 0 && static_cast<long long>(sq) + p.K <= cap;
+            const int tiles = fits ? (sq + p.K + kPieceTile - 1) / kPieceTile : 0;
+            s_t[q] = tiles;
+            atomicAdd(&s_total, tiles);
+        }
+        __syncthreads();
+        const long long all = static_cast<long long>(s_total) * p.nkv;
+        int tc = static_cast<int>((all + p.piece_slots - 1) / p.piece_slots);
+        tc = tc < p.piece_min_tiles ? p.piece_min_tiles : tc;
+        auto pieces_of = [&](int t) { return t > 0 ? (t + tc - 1) / tc : 1; };
+        for (int q = tid; q < p.B; q += blockDim.x) {
+            const int t = s_t[q];
+            s_sz[q] = t > 0 ? (t + pieces_of(t) - 1) / pieces_of(t) : 0;
+        }
+        __syncthreads();
+        for (int q = tid; q < p.B; q += blockDim.x) {
+            const int sq = s_sz[q];
+            int rank = 0;
+            for (int o = 0; o < p.B; ++o) {
+                const int so = s_sz[o];
+                rank += (so > sq || (so == sq && o < q)) ? 1 : 0;
+            }
+            s_req[rank] = q;
+        }
+        __syncthreads();
+        const int warp = tid >> 5, lane = tid & 31;
+        if (warp == 0) {
+            // exclusive prefix of the piece counts in rank order: each lane a
+            // contiguous run of ranks, then a warp scan of the run sums
+            const int per = (p.B + 31) / 32;
+            const int k0 = lane * per, k1 = min(p.B, k0 + per);
+            int sum = 0;
+            for (int k = k0; k < k1; ++k) sum += pieces_of(s_t[s_req[k]]);
+            int incl = sum;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            int run = incl - sum;
+            for (int k = k0; k < k1; ++k) {
+                s_off[k] = run;
+                run += pieces_of(s_t[s_req[k]]);
+            }
+            if (lane == 31) s_off[p.B] = incl;
+        }
+        __syncthreads();
+        const int max_items = p.piece_slots + p.B * p.nkv;
+        if (tid == 0) p.attn_plan[0] = min(s_off[p.B] * p.nkv, max_items);
+        for (int k = tid; k < p.B; k += blockDim.x) {
+            const int q = s_req[k];
+            const int t = s_t[q];
+            const int n = pieces_of(t);
+            const int per_piece = s_sz[q];
+            const int len = t > 0 ? p.seq_lens[q] + p.K : 0;
+            p.attn_plan[1 + q] = n;
+            p.attn_plan[1 + p.B + q] = s_off[k];
+            for (int i = 0; i < n; ++i) {
+                const int e0 = i * per_piece * kPieceTile;
+                const int e1 = min(len, (i + 1) * per_piece * kPieceTile);
+                for (int hh = 0; hh < p.nkv; ++hh) {
+                    const int idx = p.nkv * (s_off[k] + i) + hh;
+                    if (idx < max_items) p.attn_items[idx] = make_int4(q, hh, e0, e1);
+                }
+            }
         }
     }
     if (j == 0) {
