@@ -45,6 +45,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--max-prefix", type=int, default=0,
+                    help="cap the workload's prefix lengths (same GEMM shapes, smaller KV cache: for small ncu captures)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0, help="time box of the oracle CPU baseline")
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -291,6 +293,10 @@ def bench_ours(args):
     binding.load()
 
     wl = synth.WORKLOADS[args.workload]
+    if args.max_prefix > 0:
+        import dataclasses
+        cap = args.max_prefix
+        wl = dataclasses.replace(wl, prefix=(min(wl.prefix[0], cap), min(wl.prefix[1], cap)))
     K_max = max(wl.K, 11) if wl.B == 1 and wl.shape.name.startswith("qwen") else wl.K
     W = synth.make_weights(wl.shape, wl.seed, device=dev)
     inp = synth.make_step_inputs(wl, device=dev)
