@@ -469,6 +469,18 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     }
     const int rows_per_tile = epi == EPI_SWIGLU ? 64 : kBM;
     g.m_tiles = ceil_div(M, rows_per_tile);
+    if (epi == EPI_RESID && cluster && N > 256) {
+        // O and down have few weight tiles (H / 128): narrower token tiles,
+        // down to 128 rows, so that the tiles fill one wave of SMs
+        const int n_fill = num_sms / g.m_tiles;
+        if (n_fill > g.n_tiles) {
+            const int bn2 = round_up(ceil_div(N, n_fill), 16);
+            if (bn2 >= 128) {
+                g.bn = bn2;
+                g.n_tiles = ceil_div(N, bn2);
+            }
+        }
+    }
     g.tiles = g.m_tiles * g.n_tiles;
     // shared-memory ring: ~100 KB (two CTAs per SM, so the next kernel's CTAs
     // can start their weight loads beside this one) for token tiles up to

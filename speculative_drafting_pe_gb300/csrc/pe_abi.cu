@@ -478,12 +478,12 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     }
 
     CUtensorMap tm_th, tm_u, tm_xn, tm_attn, tm_act;
-    const int bn_rows = p_qkv.bn;   // all row-count-R GEMMs share bn
+    const int bn_rows = p_qkv.bn;   // the row-count-R GEMMs share bn, except O and down (their own token tiles)
     if ((rc = act_map(h, &tm_th, target_hidden, B, 3 * H, p_fc.bn)) != PE_OK) return rc;
     if ((rc = act_map(h, &tm_u, h->u, R, 2 * H, bn_rows)) != PE_OK) return rc;
     if ((rc = act_map(h, &tm_xn, h->xn, R, H, bn_rows)) != PE_OK) return rc;
-    if ((rc = act_map(h, &tm_attn, h->attn, R, qd, bn_rows)) != PE_OK) return rc;
-    if ((rc = act_map(h, &tm_act, h->act, R, F, bn_rows)) != PE_OK) return rc;
+    if ((rc = act_map(h, &tm_attn, h->attn, R, qd, p_o.bn)) != PE_OK) return rc;       // B operand of O
+    if ((rc = act_map(h, &tm_act, h->act, R, F, p_down.bn)) != PE_OK) return rc;       // B operand of down
     CUtensorMap tm_kc, tm_vc, tm_q;
     if (attn_umma) {
         if ((rc = encode_tmap_kv(&tm_kc, k_cache, hd, nkv, num_pages)) != PE_OK) return rc;
