@@ -469,9 +469,10 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     }
     const int rows_per_tile = epi == EPI_SWIGLU ? 64 : kBM;
     g.m_tiles = ceil_div(M, rows_per_tile);
-    if (epi == EPI_RESID && cluster && N > 256) {
-        // O and down have few weight tiles (H / 128): narrower token tiles,
-        // down to 128 rows, so that the tiles fill one wave of SMs
+    if ((epi == EPI_RESID || epi == EPI_QKV) && cluster && N > 256) {
+        // O, down and QKV have few weight tiles (16 and 40 at the Qwen
+        // shape): narrower token tiles, down to 128 rows, when that lets the
+        // tiles fill one wave of SMs
         const int n_fill = num_sms / g.m_tiles;
         if (n_fill > g.n_tiles) {
             const int bn2 = round_up(ceil_div(N, n_fill), 16);

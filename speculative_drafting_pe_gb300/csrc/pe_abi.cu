@@ -477,11 +477,14 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         return PE_ERR_ARG;
     }
 
-    CUtensorMap tm_th, tm_u, tm_xn, tm_attn, tm_act;
-    const int bn_rows = p_qkv.bn;   // the row-count-R GEMMs share bn, except O and down (their own token tiles)
+    // B-operand maps: the box height is the token tile of the GEMM that reads
+    // the map (QKV, O and down may take narrower tiles than gate/up and the LM head)
+    CUtensorMap tm_th, tm_u, tm_xq, tm_xn, tm_attn, tm_act;
+    if (p_qkv0.bn != p_qkv.bn || p_lm.bn != p_gu.bn) { set_error("GEMM token tiles disagree"); return PE_ERR_UNSUPPORTED; }
     if ((rc = act_map(h, &tm_th, target_hidden, B, 3 * H, p_fc.bn)) != PE_OK) return rc;
-    if ((rc = act_map(h, &tm_u, h->u, R, 2 * H, bn_rows)) != PE_OK) return rc;
-    if ((rc = act_map(h, &tm_xn, h->xn, R, H, bn_rows)) != PE_OK) return rc;
+    if ((rc = act_map(h, &tm_u, h->u, R, 2 * H, p_qkv.bn)) != PE_OK) return rc;      // layer 0's QKV
+    if ((rc = act_map(h, &tm_xq, h->xn, R, H, p_qkv.bn)) != PE_OK) return rc;       // QKV of layers 1-3
+    if ((rc = act_map(h, &tm_xn, h->xn, R, H, p_gu.bn)) != PE_OK) return rc;        // gate/up, LM head
     if ((rc = act_map(h, &tm_attn, h->attn, R, qd, p_o.bn)) != PE_OK) return rc;       // B operand of O
     if ((rc = act_map(h, &tm_act, h->act, R, F, p_down.bn)) != PE_OK) return rc;       // B operand of down
     CUtensorMap tm_kc, tm_vc, tm_q;
@@ -642,7 +645,7 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         if (!use_chain || l == 0) {   // a3: QKV + RoPE + paged KV write
             GemmParams p = gp_qkv(l);
             rc = run(PE_KERNEL_QKV, [&] {
-                return launch_gemm(dt, EPI_QKV, h->tm_qkv[l], h->tm_qkv[l], l == 0 ? tm_u : tm_xn,
+                return launch_gemm(dt, EPI_QKV, h->tm_qkv[l], h->tm_qkv[l], l == 0 ? tm_u : tm_xq,
                                    l == 0 ? p_qkv0 : p_qkv, p, s, pdl);
             });
             if (rc != PE_OK) return rc;
