@@ -533,13 +533,21 @@ def read_profile_traffic(kernel, workload):
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources (all of csrc) with comments and whitespace
+    removed: a comment edit does not change the kernels the profile counters
+    were taken on, any code edit does."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_drafting_pe_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
+            text = re.sub(r"\s+", " ", text).strip()
+            h.update(name.encode() + b"\0" + text.encode())
     return h.hexdigest()[:16]
 
 
