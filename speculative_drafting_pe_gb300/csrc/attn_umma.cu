@@ -5,9 +5,13 @@
 // 0 .. S_b + j; scores are scaled by 1/sqrt(hd); softmax is online in fp32
 // (base-2 exponent).
 //
-// One CTA per (request, kv head, entry split), requests issued longest
-// first (an order the row build computes); a tile is 64 cache entries
-// (4 pages). Roles (192 threads):
+// Work layouts (chosen by plan_attention_umma from the (request, kv head)
+// pair count): clusters - one CTA per (request, kv head, entry split),
+// requests issued longest first (an order the row build computes), the
+// splits of a pair combined through distributed shared memory; or
+// length-aware pieces - one CTA per item of the row build's piece list, no
+// cluster, a request with several pieces combined by k_attn_merge. A tile
+// is 64 cache entries (4 pages). Roles (192 threads):
 //   warp 4   TMA: the packed query rows once (3-D map over q), then K and V
 //            pages of every tile (4-D map over the paged cache) into a
 //            4-stage ring, 128-byte swizzle. A stage is refilled once the
@@ -22,8 +26,10 @@
 //            from TMEM, mask, keep the running max, write P_t = exp2(S - m)
 //            as bf16 into shared memory, and rescale the TMEM output row
 //            only when the running max grows by more than 2^8.
-// The entry splits of one (request, kv head) form one thread-block cluster
-// and are combined through distributed shared memory in split order.
+// In the cluster layout the entry splits of one (request, kv head) form one
+// thread-block cluster and are combined through distributed shared memory in
+// split order; a piece of a request with several writes its partial (O,
+// running max, sum) to scratch for k_attn_merge.
 #include <cfloat>
 
 #include "common.cuh"
