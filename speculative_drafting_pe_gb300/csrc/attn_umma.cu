@@ -46,7 +46,8 @@ constexpr int kBoxBytes = 16 * 128; // one page of one kv head, 64 dims
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxCluster = 16;
 constexpr int kPiecePairs = 16;      // (request, kv head) pairs from which length-aware pieces are used
-constexpr int kPieceMaxBatch = 256;  // requests the row build's piece list serves
+constexpr int kPieceMaxBatch = 256;  // requests the row build's piece list serves (= kMaxPieceB of
+                                     // rows.cu, the size of its shared arrays)
 constexpr int kPieceMinTiles = 4;
 
 

@@ -17,7 +17,8 @@ namespace pe {
 namespace {
 
 constexpr int kRowThreads = 256;
-constexpr int kMaxPieceB = 256;   // requests the attention piece list serves
+constexpr int kMaxPieceB = 256;   // requests the attention piece list serves (= kPieceMaxBatch of
+                                  // attn_umma.cu, whose planner uses pieces only up to it)
 constexpr int kPieceTile = 64;    // cache entries per attention tile
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
