@@ -532,14 +532,14 @@ def read_profile_traffic(kernel, workload):
         return None
 
 
-def kernel_source_hash():
+def kernel_source_hash(csrc=None):
     """Hash of the kernel sources (all of csrc) with comments and whitespace
     removed: a comment edit does not change the kernels the profile counters
     were taken on, any code edit does."""
     import hashlib
     import re
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "speculative_drafting_pe_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "speculative_drafting_pe_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
             with open(os.path.join(csrc, name), encoding="utf-8") as f:
