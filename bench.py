@@ -44,7 +44,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the K sweep, the cold-L2 line and the workload sweep")
     ap.add_argument("--max-prefix", type=int, default=0,
                     help="cap the workload's prefix lengths (same GEMM shapes, smaller KV cache: for small ncu captures)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0, help="time box of the oracle CPU baseline")
@@ -271,6 +271,96 @@ def cpu_baseline_obj(res, wl):
 
 # ------------------------------------------------------------------ our arm
 
+SWEEP_WORKLOADS = (["qwen-b1-k3", "qwen-b1-k7", "qwen-b1-k11"]
+                   + [f"qwen-b{B}-k{K}" for B in (4, 8, 32, 128) for K in (3, 7, 11)]
+                   + ["gptoss-b64-k10"])
+
+
+def roofline_of(kind, wl, seq_np, avg_launch_s, peaks, chained=False):
+    """Roofline of one kernel kind: its algorithmic bytes (or FLOPs) per
+    launch over its measured average launch time, against the measured peak
+    of whichever resource bounds it at these sizes."""
+    b, f = algorithmic_work(kind, wl, seq_np, chained=chained)
+    t_hbm = b / (peaks["hbm_gbs"] * 1e9)
+    t_tc = f / (peaks["bf16_tflops_sustained"] * 1e12)
+    if t_hbm >= t_tc:
+        a = b / avg_launch_s / 1e9
+        return {"bound": "hbm", "achieved": a, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": a / peaks["hbm_gbs"]}
+    a = f / avg_launch_s / 1e12
+    return {"bound": "tensor", "achieved": a, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+            "frac": a / peaks["bf16_tflops_sustained"]}
+
+
+def sweep_workload(name, dev, weights_cache, peaks, replays):
+    """Steps/s, draft tok/s, step HBM fraction and the dominant kernel's
+    roofline for one workload: per-kind CUDA events over three direct steps
+    (shares and per-launch times), then `replays` timed step-graph replays."""
+    import torch
+
+    from speculative_drafting_pe_gb300 import binding, synth
+
+    wl = synth.WORKLOADS[name]
+    key = (wl.shape.name, wl.seed)
+    if key not in weights_cache:
+        weights_cache.clear()
+        torch.cuda.empty_cache()
+        weights_cache[key] = synth.make_weights(wl.shape, wl.seed, device=dev)
+    W = weights_cache[key]
+    inp = synth.make_step_inputs(wl, device=dev)
+    seq_np = inp.seq_lens.cpu().numpy()
+    drafter = binding.Drafter(wl.shape, W, max_batch=wl.B, k_max=wl.K)
+    B, K = wl.B, wl.K
+    drafts = torch.empty(B, K, dtype=torch.int32, device=dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    drafter.draft(inp.last_token, inp.target_hidden, inp.positions, inp.seq_lens, inp.page_table, inp.num_pages,
+                  inp.k_cache, inp.v_cache, K, drafts=drafts, status=status)
+    torch.cuda.synchronize()
+    g = torch.as_tensor(synth.plant_targets(drafts.cpu().numpy(), inp.alpha, wl.shape.vocab, wl.seed), device=dev)
+    vout = {}
+
+    def step():
+        drafter.draft(inp.last_token, inp.target_hidden, inp.positions, inp.seq_lens, inp.page_table,
+                      inp.num_pages, inp.k_cache, inp.v_cache, K, drafts=drafts, status=status)
+        binding.verify_rebuild(drafts, g, inp.page_table, inp.num_pages, inp.positions, inp.seq_lens, out=vout)
+
+    for _ in range(3):
+        step()
+    per_kind = {}
+    for kind in binding.KERNEL_KINDS:
+        drafter.profile_start(kind, 64)
+        for _ in range(3):
+            step()
+        ms, n = drafter.profile_stop()
+        if n > 0:
+            per_kind[kind] = (ms / 3.0, (ms / 1e3) / n)
+    dominant = max(per_kind, key=lambda k: per_kind[k][0])
+    sg = drafter.step_graph(inp.last_token, inp.target_hidden, inp.positions, inp.seq_lens, inp.page_table,
+                            inp.num_pages, inp.k_cache, inp.v_cache, K, g)
+    for _ in range(3):
+        sg.launch()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    e0.record(stream)
+    for _ in range(replays):
+        sg.launch()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert drafter.device_errors() == 0
+    ms_step = e0.elapsed_time(e1) / replays
+    roof = roofline_of(dominant, wl, seq_np, per_kind[dominant][1], peaks)
+    out = {"steps_s": 1e3 / ms_step, "ms_per_step": ms_step, "draft_tok_s": 1e3 / ms_step * B * K,
+           "step_hbm_frac": step_bytes(wl, seq_np) / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"],
+           "dominant": dominant, "dominant_us_per_launch": per_kind[dominant][1] * 1e6,
+           "dominant_roofline": {k: roof[k] for k in ("bound", "achieved", "unit", "frac")},
+           "kernel_ms_per_step": {k: round(v[0], 4) for k, v in sorted(per_kind.items(), key=lambda x: -x[1][0])}}
+    sg.close()
+    drafter.close()
+    del inp
+    return out
+
+
+
 def bench_ours(args):
     import numpy as np
     import torch
@@ -379,7 +469,32 @@ def bench_ours(args):
     dom_ms, dom_n = drafter.profile_stop()
     assert drafter.device_errors() == 0
 
-    # ---------------- flatness in K at B=1 (step graphs of the draft pass + verify)
+    # ---------------- the same step with L2 cold: a buffer larger than L2 is
+    # written between timed steps (outside the events), so no weight or KV
+    # byte of the previous step is still cached when a step starts
+    cold = None
+    if not args.no_sweep:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        n_cold = max(args.steps, 20)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_cold)]
+        for _ in range(3):
+            flush.fill_(1)
+            sg.launch()
+        torch.cuda.synchronize()
+        for i in range(n_cold):
+            flush.fill_(i & 0xFF)
+            evs[i][0].record(stream)
+            sg.launch()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        cold_ms = sum(a.elapsed_time(b) for a, b in evs) / n_cold
+        cold = {"ms_per_step": cold_ms, "steps_s": 1e3 / cold_ms,
+                "step_hbm_frac": step_bytes(wl, seq_np) / (cold_ms / 1e3) / 1e9 / load_peaks()[0]["hbm_gbs"],
+                "steps": n_cold, "flush": "256 MB buffer written between timed steps, outside the timed events"}
+        del flush
+
+    # ---------------- flatness in K at B=1 (step graphs of the draft pass
+    # followed by the verify/rebuild, ~3 us of the step)
     k_sweep = None
     if not args.no_sweep and wl.B == 1 and wl.shape.name.startswith("qwen"):
         k_sweep = {}
@@ -440,6 +555,18 @@ def bench_ours(args):
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
+    # ---------------- every workload of the metric (C2, C3, C4): one line each
+    sweep = None
+    if not args.no_sweep and world == 1 and args.max_prefix == 0:
+        peaks0, _ = load_peaks()
+        del sg, sg_e
+        drafter.close()
+        cache = {(wl.shape.name, wl.seed): W}
+        sweep = {}
+        for name in SWEEP_WORKLOADS:
+            sweep[name] = sweep_workload(name, dev, cache, peaks0, max(args.steps, 50))
+        cache.clear()
+
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -496,8 +623,13 @@ def bench_ours(args):
         "gpu_launches": launches_per_step * args.steps,
     }
     if k_sweep:
-        line["k_sweep_draft_ms"] = k_sweep
+        line["k_sweep_step_ms"] = k_sweep
+        line["k_sweep_note"] = "ms per step-graph replay (draft pass + verify/rebuild) at B=1, K = 3 / 7 / 11"
         line["k11_over_k3"] = k_sweep["11"] / k_sweep["3"]
+    if cold:
+        line["cold_l2"] = cold
+    if sweep:
+        line["sweep"] = sweep
     if world == 1 and not args.no_cpu_baseline:
         try:
             res = run_oracle_subprocess(args.workload, args.cpu_seconds, 1000)

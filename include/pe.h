@@ -182,11 +182,16 @@ int pe_linear(int32_t dtype, int32_t M, int32_t N, int32_t Kd, const void* w, co
  * arguments minus ws / tickets) but keeps its split-K scratch in fixed arrays
  * inside the library: 8 MiB of partials and 4096 tickets per device, held
  * until the process exits. It allocates nothing.
- *  - Shapes whose plan needs more scratch than that return PE_ERR_ARG with a
- *    message giving the need and the maximum (pe_linear has no such limit).
+ *  - Shapes whose plan needs more scratch than that (pe_linear_scratch
+ *    reports the need: more than 2 Mi floats, or more than 4096 tickets
+ *    when it needs tickets at all) return PE_ERR_ARG with a message giving
+ *    the need and the maximum, before any launch (pe_linear has no limit).
  *  - The first call on each device looks up the arrays' device addresses
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture that should contain later calls.
+ *    (cudaGetSymbolAddress) with that device current and loads the kernel
+ *    of both dtypes; make that first call (in either dtype) before any
+ *    stream capture that should contain later calls, or that runs while
+ *    later calls are made. After cudaDeviceReset the cached addresses are
+ *    stale: do not call it on that device again in the same process.
  *  - Every call on a device shares the same arrays: calls that can overlap
  *    on the GPU (several streams or host threads) race and must be serialised
  *    by the caller. Each call clears the tickets it uses on its stream. */
@@ -217,6 +222,20 @@ void pe_step_graph_destroy(pe_step_graph* g);
 /* Synchronise `stream` and return (then clear) the device error word of h
  * (PE_DEVERR_* bits; 0 = no device-side wait gave up). */
 int pe_device_errors(pe_handle* h, void* stream, uint32_t* out_bits);
+
+/* Test support for the bounded-wait give-up path (no counterpart in the
+ * paper; host-side fault injection, nothing on the device is made to fault).
+ * Enqueues on `stream` a write that primes the arrival tickets of the first
+ * phase of the handle's persistent layer chain so that its shared tiles never
+ * complete. The next pe_draft's chain launches then wait for a phase that
+ * never finishes: each such wait gives up after its time limit (1 s), sets
+ * PE_DEVERR_CHAIN_TIMEOUT, and the kernel returns; its outputs for that call
+ * are meaningless. The chain resets its tickets and counters on the way out,
+ * so the handle is usable again once pe_device_errors has read and cleared
+ * the error word. Returns PE_ERR_UNSUPPORTED when the handle runs no chain
+ * (it runs one when created with PE_LAYER_CHAIN=1 in the environment, bf16,
+ * for draft passes of at most 64 rows). */
+int pe_test_stall_chain(pe_handle* h, void* stream);
 
 /* Kernel kinds of the draft pass, for launch accounting and profiling. */
 #define PE_KERNEL_FC         0

@@ -32,4 +32,5 @@ from .verify import (  # noqa: F401
     REQ_OK,
     REQ_CAPACITY,
     REQ_BAD_PAGE,
+    REQ_BAD_INPUT,
 )

@@ -29,11 +29,14 @@ Readings where the pages are silent (also listed in the design notes):
      page_table[b, (S_b'+j) // P] * P + (S_b'+j) % P for j < K.
  V4  Rolled-back slots are those of entries S_b' .. S_b+K-1
      (K - kept of them), padded with -1 to K.
- V5  A request whose next K entries do not fit its page table
-     (S_b' + K > max_pages * P) gets status REQ_CAPACITY; one whose needed
-     page index is outside [0, num_pages) gets REQ_BAD_PAGE. For such a
-     request seq_lens / positions are returned unchanged and the slot and
-     rollback rows are all -1; accepted length and bonus are still reported.
+ V5  A request whose length or position is outside [0, 2^31 - 1 - 2K]
+     (negative, or so large that the next step's entries or positions would
+     not fit a signed 32-bit integer) gets status REQ_BAD_INPUT; one whose
+     next K entries do not fit its page table (S_b' + K > max_pages * P)
+     gets REQ_CAPACITY; one whose needed page index is outside
+     [0, num_pages) gets REQ_BAD_PAGE. For such a request seq_lens /
+     positions are returned unchanged and the slot and rollback rows are all
+     -1; accepted length and bonus are still reported.
 """
 
 import numpy as np
@@ -41,6 +44,8 @@ import numpy as np
 REQ_OK = 0
 REQ_CAPACITY = 1
 REQ_BAD_PAGE = 2
+REQ_BAD_INPUT = 3
+INT32_MAX = 2 ** 31 - 1
 
 
 def accept_length(d_row, g_row):
@@ -94,9 +99,13 @@ def rebuild_metadata(accepted, K, seq_lens, positions, page_table, num_pages, pa
 
     for b in range(B):
         a = int(accepted[b])
+        S, Q = int(seq_lens[b]), int(positions[b])
+        if not (0 <= S <= INT32_MAX - 2 * K and 0 <= Q <= INT32_MAX - 2 * K):
+            status[b] = REQ_BAD_INPUT
+            continue
         kept = min(a, K - 1) + 1
-        S_next = int(seq_lens[b]) + kept
-        Q_next = int(positions[b]) + a + 1
+        S_next = S + kept
+        Q_next = Q + a + 1
         if S_next + K > max_pages * page_size:
             status[b] = REQ_CAPACITY
             continue

@@ -16,13 +16,14 @@ from . import build as _build
 PE_OK = 0
 PE_REQ_OK, PE_REQ_CAPACITY, PE_REQ_BAD_PAGE, PE_REQ_BAD_INPUT = 0, 1, 2, 3
 PE_DTYPE_BF16, PE_DTYPE_FP32 = 0, 1
+PE_DEVERR_GEMM_TIMEOUT, PE_DEVERR_ATTN_TIMEOUT, PE_DEVERR_CHAIN_TIMEOUT = 1, 2, 4
 
 EXPORTS = (
     "pe_init_drafter", "pe_draft", "pe_verify_rebuild", "pe_device_errors",
     "pe_last_launch_count", "pe_destroy", "pe_last_error", "pe_abi_version", "pe_linear_scratch", "pe_linear",
     "pe_profile_start", "pe_profile_stop", "pe_kernel_name",
     "pe_step_graph_create", "pe_step_graph_launch", "pe_step_graph_launch_count", "pe_step_graph_destroy",
-    "pe_linear_noalloc",
+    "pe_linear_noalloc", "pe_test_stall_chain",
 )
 KERNEL_KINDS = ("fc", "row_build", "rmsnorm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "argmax",
                 "layer_chain")
@@ -95,6 +96,8 @@ def load():
     lib.pe_linear.restype = ctypes.c_int
     lib.pe_linear_noalloc.argtypes = [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp]
     lib.pe_linear_noalloc.restype = ctypes.c_int
+    lib.pe_test_stall_chain.argtypes = [_vp, _vp]
+    lib.pe_test_stall_chain.restype = ctypes.c_int
     lib.pe_profile_start.argtypes = [_vp, _i32, _i32]
     lib.pe_profile_start.restype = ctypes.c_int
     lib.pe_profile_stop.argtypes = [_vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_i32)]
@@ -209,6 +212,11 @@ class Drafter:
 
     def launch_count(self):
         return load().pe_last_launch_count(self._h)
+
+    def test_stall_chain(self, stream=None):
+        """Host-side fault injection (tests only): the next draft pass's
+        layer-chain waits cannot complete and must give up."""
+        _check(load().pe_test_stall_chain(self._h, _stream_ptr(stream)))
 
     def step_graph(self, last_token, target_hidden, positions, seq_lens, page_table, num_pages, k_cache, v_cache,
                    K, target_tokens, positions_out=None, seq_lens_out=None):

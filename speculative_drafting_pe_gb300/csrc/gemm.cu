@@ -533,6 +533,13 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     return g;
 }
 
+int gemm_store_kernels_load() {
+    cudaFuncAttributes fa;
+    PE_CUDA_TRY(cudaFuncGetAttributes(&fa, k_gemm<__nv_bfloat16, EPI_STORE>));
+    PE_CUDA_TRY(cudaFuncGetAttributes(&fa, k_gemm<float, EPI_STORE>));
+    return PE_OK;
+}
+
 int launch_gemm(int dtype, int epi, const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B,
                 const GemmPlan& plan, GemmParams p, cudaStream_t stream, bool pdl) {
     p.m_tiles = plan.m_tiles;

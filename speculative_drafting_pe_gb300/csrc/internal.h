@@ -97,6 +97,9 @@ struct GemmPlan {
 GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster);
 int launch_gemm(int dtype, int epi, const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B,
                 const GemmPlan& plan, GemmParams p, cudaStream_t stream, bool pdl);
+// Loads the plain-store GEMM kernels of both dtypes on the current device
+// (module loading is lazy; this makes the first launch of either load nothing)
+int gemm_store_kernels_load();
 
 // ---------------------------------------------------------------- persistent layer chain
 

@@ -33,6 +33,9 @@ DeviceScratch g_scratch[64];
 // Device addresses of the arrays on the current device. In host code the
 // array names are host-side stand-ins, so the addresses come from
 // cudaGetSymbolAddress, looked up once per device with that device current.
+// The cached addresses stay valid for the life of the device's primary
+// context: after cudaDeviceReset the library must not be called on that
+// device again in this process.
 int scratch_for_current_device(DeviceScratch* out) {
     int dev = 0;
     PE_CUDA_TRY(cudaGetDevice(&dev));
@@ -55,6 +58,10 @@ int scratch_for_current_device(DeviceScratch* out) {
             pe::set_error(std::string("pe_linear_noalloc: cudaGetSymbolAddress(tickets): ") + cudaGetErrorString(e));
             return PE_ERR_CUDA;
         }
+        // both dtype instances of the kernel, so that a first call in the
+        // other dtype later loads no module
+        const int rc = pe::gemm_store_kernels_load();
+        if (rc != PE_OK) return rc;
         s.ws = static_cast<float*>(ws);
         s.tickets = static_cast<int*>(tk);
     }
@@ -79,7 +86,8 @@ extern "C" int pe_linear_noalloc(int32_t dtype, int32_t M, int32_t N, int32_t Kd
     PE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     const int eb = dtype == PE_DTYPE_BF16 ? 2 : 4;
     const GemmPlan g = plan_gemm(M, N, Kd, EPI_STORE, eb, sms, false);
-    if (g.ws_floats > kWsFloats || g.tiles > kTickets) {
+    // the tickets are used only by split-K plans (one per tile)
+    if (g.ws_floats > kWsFloats || (g.splits > 1 && g.tiles > kTickets)) {
         set_error("pe_linear_noalloc: this shape needs " + std::to_string(g.ws_floats) + " floats of split-K scratch and " +
                   std::to_string(g.tiles) + " tickets; the built-in maximum is " + std::to_string(kWsFloats) +
                   " floats and " + std::to_string(kTickets) + " tickets (use pe_linear)");

@@ -423,6 +423,20 @@ void pe_destroy(pe_handle* h) {
 
 int pe_last_launch_count(const pe_handle* h) { return h ? h->last_launches : 0; }
 
+int pe_test_stall_chain(pe_handle* h, void* stream) {
+    if (h == nullptr) { set_error("null handle"); return PE_ERR_ARG; }
+    if (!h->chain) {
+        set_error("the handle runs no layer chain (create it with PE_LAYER_CHAIN=1, bf16)");
+        return PE_ERR_UNSUPPORTED;
+    }
+    // Phase 0 (the O projection) owns the first ceil(H/128) tickets. Bytes of
+    // 0x01 make each ticket 0x01010101: no segment of a shared tile then sees
+    // the arrival count that makes it the last, so phase 0 never completes.
+    const size_t n = static_cast<size_t>((h->cfg.hidden + 127) / 128);
+    PE_CUDA_TRY(cudaMemsetAsync(h->chain_tickets, 0x01, n * sizeof(int), static_cast<cudaStream_t>(stream)));
+    return PE_OK;
+}
+
 int pe_device_errors(pe_handle* h, void* stream, uint32_t* out_bits) {
     if (h == nullptr || out_bits == nullptr) { set_error("null argument"); return PE_ERR_ARG; }
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -10,8 +10,9 @@
 //   S'    = S + kept,  Q' = Q + a + 1
 //   slot_mapping[j] = page_table[(S'+j)/16]*16 + (S'+j)%16,  j < K
 //   rollback: slots of entries S' .. S+K-1, then -1
-// A request whose next K entries exceed its page table, or whose page index
-// is out of range, gets a per-request status and pass-through metadata.
+// A request whose length or position is negative or too close to 2^31 - 1,
+// whose next K entries exceed its page table, or whose page index is out of
+// range gets a per-request status and pass-through metadata.
 #include "common.cuh"
 #include "internal.h"
 
@@ -43,12 +44,17 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int S = seq_lens[b];
     const int Q = positions[b];
     __syncwarp();
+    // Lengths and positions must leave room for the next step's K entries and
+    // positions in a signed 32-bit integer; with S, Q <= 2^31 - 1 - 2K the
+    // sums below cannot overflow.
+    const int lim = 0x7FFFFFFF - 2 * K;
+    const bool in_range = S >= 0 && Q >= 0 && S <= lim && Q <= lim;
     const int kept = min(a, K - 1) + 1;
-    const int S2 = S + kept;
-    const int Q2 = Q + a + 1;
+    const int S2 = in_range ? S + kept : 0;
+    const int Q2 = in_range ? Q + a + 1 : 0;
 
     int st = PE_REQ_OK;
-    if (S < 0 || Q < 0) st = PE_REQ_BAD_INPUT;
+    if (!in_range) st = PE_REQ_BAD_INPUT;
     else if (static_cast<long long>(S2) + K > static_cast<long long>(max_pages) * page_size) st = PE_REQ_CAPACITY;
     int slot = -1;
     int bad = 0;

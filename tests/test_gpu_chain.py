@@ -131,3 +131,44 @@ def test_chain_repeatable_and_counters_reset(monkeypatch):
     for d, lg in outs:
         assert (d == a[0]).all()
         assert np.array_equal(lg, a[2])
+
+
+def test_chain_wait_gives_up_and_the_handle_recovers(monkeypatch):
+    # Host-side injection: the first phase's tickets are primed so that its
+    # shared tiles never complete. The next phase's waits must give up after
+    # their time limit, report PE_DEVERR_CHAIN_TIMEOUT and return; the next
+    # draft pass on the same handle must then be oracle-correct.
+    import time
+
+    shape, B, K = MINI_HD64, 2, 5
+    W, inp = _setup(shape, B, K, seed=61)
+    ref = oracle_batch(shape, synth.weights_to_numpy(W), inp, K)
+    monkeypatch.setenv("PE_LAYER_CHAIN", "1")
+    dev = torch.device("cuda")
+    dr = binding.Drafter(shape, W, max_batch=B, k_max=K)
+    kc, vc = inp.k_cache.clone(), inp.v_cache.clone()
+    dr.test_stall_chain()
+    t0 = time.time()
+    dr.draft(inp.last_token, inp.target_hidden, inp.positions, inp.seq_lens, inp.page_table, inp.num_pages,
+             kc, vc, K)
+    torch.cuda.synchronize()
+    waited = time.time() - t0
+    bits = dr.device_errors()
+    assert bits & binding.PE_DEVERR_CHAIN_TIMEOUT, bits
+    assert waited < 30.0, waited
+    assert dr.launch_count() < 27          # the chain ran (it replaces 13 per-GEMM launches)
+
+    kc, vc = inp.k_cache.clone(), inp.v_cache.clone()
+    lg = torch.empty(B, K, shape.vocab, device=dev)
+    d, st = dr.draft(inp.last_token, inp.target_hidden, inp.positions, inp.seq_lens, inp.page_table,
+                     inp.num_pages, kc, vc, K, logits=lg)
+    torch.cuda.synchronize()
+    assert dr.device_errors() == 0
+    assert (st.cpu().numpy() == binding.PE_REQ_OK).all()
+    assert_logits_close(lg.cpu().numpy(), ref["logits"])
+    assert_drafts_match(d.cpu().numpy(), ref)
+    for b in range(B):
+        k_got, v_got = read_new_kv(inp, kc, vc, b, K)
+        assert_kv_close(k_got, ref["k_new"][:, b], "k rows")
+        assert_kv_close(v_got, ref["v_new"][:, b], "v rows")
+    dr.close()

@@ -163,15 +163,37 @@ def test_qwen_b1_full_size(K):
     assert_kv_close(v_got, ref["v_new"][:, 0], "v rows")
 
 
-@pytest.mark.parametrize("name,samples", [("qwen-b128-k11", (0, 77, 127)), ("qwen-b8-k7", (3,)),
-                                          ("qwen-b32-k11", (0, 17, 31)),   # one wave of (request, kv head) attention CTAs
-                                          ("gptoss-b64-k10", (0, 63))])
-def test_batched_full_size_sampled(name, samples):
+_FULL = {}
+
+
+def _full_size_setup(wl):
+    """Device weights and their host copy for a workload's drafter, shared by
+    the full-size tests of the same shape and seed."""
+    key = (wl.shape.name, wl.seed)
+    if key not in _FULL:
+        _FULL.clear()
+        dev = torch.device("cuda")
+        W = synth.make_weights(wl.shape, wl.seed, device=dev)
+        _FULL[key] = (W, synth.weights_to_numpy(W))
+    return _FULL[key]
+
+
+def _sample_requests(seq_lens):
+    """The longest-prefix request (the one cut into the most attention
+    pieces when pieces are used), the shortest, and the median one."""
+    order = np.argsort(seq_lens, kind="stable")
+    return sorted({int(order[-1]), int(order[0]), int(order[len(order) // 2])})
+
+
+C3_PAIRS = [f"qwen-b{B}-k{K}" for B in (4, 8, 32, 128) for K in (3, 7, 11)]
+
+
+@pytest.mark.parametrize("name", C3_PAIRS + ["gptoss-b64-k10"])
+def test_batched_full_size_sampled(name):
     wl = synth.WORKLOADS[name]
     dev = torch.device("cuda")
-    W = synth.make_weights(wl.shape, wl.seed, device=dev)
+    W, Wn = _full_size_setup(wl)
     inp = synth.make_step_inputs(wl, device=dev)
-    Wn = synth.weights_to_numpy(W)
     dr = binding.Drafter(wl.shape, W, max_batch=wl.B, k_max=wl.K)
     kc, vc = inp.k_cache.clone(), inp.v_cache.clone()
     lg = torch.empty(wl.B, wl.K, wl.shape.vocab, device=dev)
@@ -182,10 +204,44 @@ def test_batched_full_size_sampled(name, samples):
     assert (st.cpu().numpy() == 0).all()
     dn = d.cpu().numpy()
     assert ((dn >= 0) & (dn < wl.shape.vocab)).all()
-    for b in samples:
+    for b in _sample_requests(inp.seq_lens.cpu().numpy()):
         ref = oracle_request(wl.shape, Wn, inp, b, wl.K)
         assert_logits_close(lg[b:b + 1].cpu().numpy(), ref["logits"])
         assert_drafts_match(dn[b:b + 1], ref)
         k_got, v_got = read_new_kv(inp, kc, vc, b, wl.K)
         assert_kv_close(k_got, ref["k_new"][:, 0], "k rows")
         assert_kv_close(v_got, ref["v_new"][:, 0], "v rows")
+    dr.close()
+
+
+@pytest.mark.parametrize("name", ["qwen-b1-k7", "qwen-b128-k11"])
+def test_step_graph_without_logits_matches_oracle(name):
+    # The exact call the benchmark times: draft (no logits output) + verify
+    # replayed from the step graph. Drafts under the gap rule, the verify
+    # outputs bit-exact against the oracle's verify of those drafts.
+    wl = synth.WORKLOADS[name]
+    dev = torch.device("cuda")
+    W, Wn = _full_size_setup(wl)
+    inp = synth.make_step_inputs(wl, device=dev)
+    dr = binding.Drafter(wl.shape, W, max_batch=wl.B, k_max=wl.K)
+    g = torch.as_tensor(synth.plant_targets(np.zeros((wl.B, wl.K), np.int64), inp.alpha, wl.shape.vocab, wl.seed),
+                        device=dev)
+    sg = dr.step_graph(inp.last_token, inp.target_hidden, inp.positions, inp.seq_lens, inp.page_table,
+                       inp.num_pages, inp.k_cache, inp.v_cache, wl.K, g)
+    sg.launch()
+    torch.cuda.synchronize()
+    assert dr.device_errors() == 0
+    dn = sg.out["drafts"].cpu().numpy()
+    assert (sg.out["draft_status"].cpu().numpy() == 0).all()
+    for b in _sample_requests(inp.seq_lens.cpu().numpy()):
+        ref = oracle_request(wl.shape, Wn, inp, b, wl.K)
+        assert_drafts_match(dn[b:b + 1], ref)
+    a, bonus = oracle.verify(dn, g.cpu().numpy())
+    meta = oracle.rebuild_metadata(a, wl.K, inp.seq_lens.cpu().numpy(), inp.positions.cpu().numpy(),
+                                   inp.page_table.cpu().numpy(), inp.num_pages)
+    np.testing.assert_array_equal(sg.out["accepted"].cpu().numpy(), a)
+    np.testing.assert_array_equal(sg.out["bonus"].cpu().numpy(), bonus)
+    for k in ("slot_mapping", "rollback_slots", "status", "positions", "seq_lens"):
+        np.testing.assert_array_equal(sg.out[k].cpu().numpy(), meta[k], err_msg=k)
+    sg.close()
+    dr.close()

@@ -86,3 +86,17 @@ def test_verify_in_place_metadata(lib):
     np.testing.assert_array_equal(pos.cpu().numpy(), exp["positions"])
     np.testing.assert_array_equal(sl.cpu().numpy(), exp["seq_lens"])
     np.testing.assert_array_equal(out["slot_mapping"].cpu().numpy(), exp["slot_mapping"])
+
+
+def test_verify_bad_input_lengths(lib):
+    # negative lengths / positions and values too close to 2^31 - 1
+    K = 3
+    lim = 2 ** 31 - 1 - 2 * K
+    v = dict(drafts=np.array([[1, 2, 3]] * 6), targets=np.array([[1, 2, 9, 9]] * 6),
+             page_table=np.array([[0, 1], [2, 3], [4, 5], [6, 7], [8, 9], [10, 11]]), num_pages=12,
+             seq_lens=np.array([-1, 5, lim + 1, 5, 5, lim]), positions=np.array([7, -3, 7, lim + 1, 9, 4]))
+    got = _run(lib, v, K, torch.device("cuda"))
+    exp = _expect(v, K)
+    _assert_equal(got, exp)
+    assert list(got["status"][:4]) == [oracle.REQ_BAD_INPUT] * 4
+    assert got["status"][4] == oracle.REQ_OK and got["status"][5] == oracle.REQ_CAPACITY

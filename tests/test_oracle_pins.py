@@ -144,16 +144,19 @@ def test_build_rows_row0_real_rest_placeholders():
 
 # --------------------------------------------------------------- whole draft pass
 
-def _torch_reference_pass(W, inp, K):
+def _torch_reference_pass(W, inp, K, full=False):
     """Independent float64 restatement with torch library routines
     (F.linear, F.rms_norm, F.silu, SDPA, complex-number RoPE) and an explicit
-    per-entry walk of the page table."""
+    per-entry walk of the page table. With full=True also returns, per layer,
+    the layer's input rows x [L, B, K, in], the rotated new k rows and the
+    raw new v rows [L, B, K, nkv, hd] that the pass writes to the cache."""
     cfg = TINY
     d = torch.float64
     t = lambda a: a.to(d)
     B = inp.last_token.shape[0]
     H, nq, nkv, hd = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     eps = cfg.rms_eps
+    nl = len(W["layers"])
 
     def norm(x, g):
         return F.rms_norm(x, (x.shape[-1],), weight=t(g), eps=eps)
@@ -169,6 +172,9 @@ def _torch_reference_pass(W, inp, K):
     emb = torch.stack([t(W["embed"][int(tok)]) for tok in inp.last_token])
     L0 = W["layers"][0]
     logits = torch.empty(B, K, cfg.vocab, dtype=d)
+    xs = [[None] * B for _ in range(nl)]
+    k_rows = torch.empty(nl, B, K, nkv, hd, dtype=d)
+    v_rows = torch.empty(nl, B, K, nkv, hd, dtype=d)
     for b in range(B):
         rows_e = [emb[b]] + [t(W["emb_mask"])] * (K - 1)
         rows_h = [h[b]] + [t(W["h_shared"])] * (K - 1)
@@ -179,10 +185,12 @@ def _torch_reference_pass(W, inp, K):
         for li, Lw in enumerate(W["layers"]):
             if li > 0:
                 x = norm(r, Lw["attn_norm"])
+            xs[li][b] = x
             qkv = F.linear(x, t(Lw["w_qkv"]))
             q = rope(qkv[:, : nq * hd].reshape(K, nq, hd), pos[:, None])
             k = rope(qkv[:, nq * hd:(nq + nkv) * hd].reshape(K, nkv, hd), pos[:, None])
             v = qkv[:, (nq + nkv) * hd:].reshape(K, nkv, hd)
+            k_rows[li, b], v_rows[li, b] = k, v
             ks, vs = [], []
             for e in range(S):
                 page = int(inp.page_table[b, e // cfg.page_size])
@@ -200,7 +208,10 @@ def _torch_reference_pass(W, inp, K):
             x = norm(r, Lw["mlp_norm"])
             r = r + F.linear(F.silu(F.linear(x, t(Lw["w_gate"]))) * F.linear(x, t(Lw["w_up"])), t(Lw["w_down"]))
         logits[b] = F.linear(norm(r, W["final_norm"]), t(W["lm_head"]))
-    return logits.numpy()
+    if not full:
+        return logits.numpy()
+    return dict(logits=logits.numpy(), x=[torch.stack(xs[li]) for li in range(nl)], k_new=k_rows.numpy(),
+                v_new=v_rows.numpy())
 
 
 @pytest.mark.parametrize("K", [1, 4])
@@ -252,15 +263,75 @@ def test_draft_argmax_exhaustive_on_tiny_vocab():
         assert out["drafts"][b, j] == best
 
 
+def test_new_kv_rows_match_independent_torch_restatement():
+    # The rows the pass writes to the cache (k after RoPE, v as projected)
+    # equal the torch restatement's own k and v rows, layer by layer.
+    W, inp = _tiny_case(K=4)
+    out = _run_oracle(W, inp, 4)
+    ref = _torch_reference_pass(W, inp, 4, full=True)
+    assert out["k_new"].shape == (4, 2, 4, TINY.n_kv_heads, TINY.head_dim)
+    np.testing.assert_allclose(out["k_new"], ref["k_new"], rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(out["v_new"], ref["v_new"], rtol=1e-10, atol=1e-10)
+
+
+def _unrotate(k, pos):
+    """Inverse rotate-half RoPE by complex division: k [..., hd], pos [...]."""
+    hd = k.shape[-1]
+    half = hd // 2
+    inv = TINY.rope_theta ** (-(np.arange(half) * 2.0) / hd)
+    z = (k[..., :half] + 1j * k[..., half:]) * np.exp(-1j * np.asarray(pos, dtype=np.float64)[..., None] * inv)
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def _kv_rows_violations(k_new, v_new, x, W, positions, K):
+    """Checks k_new / v_new [L, B, K, nkv, hd] against the layer inputs x
+    (list of [B, K, in] float64 tensors): un-rotating row j of request b by
+    the angle of position Q_b + j must give W_k x exactly, v must be W_v x
+    unrotated. Returns the list of failed checks (empty when all hold)."""
+    nq, nkv, hd = TINY.n_q_heads, TINY.n_kv_heads, TINY.head_dim
+    bad = []
+    B = k_new.shape[1]
+    pos = np.asarray(positions, dtype=np.int64)[:, None] + np.arange(K)[None, :]      # [B, K]
+    for li, Lw in enumerate(W["layers"]):
+        wq = torch.as_tensor(Lw["w_qkv"]).double()
+        k_raw = F.linear(x[li], wq[nq * hd:(nq + nkv) * hd]).numpy().reshape(B, K, nkv, hd)
+        v_raw = F.linear(x[li], wq[(nq + nkv) * hd:]).numpy().reshape(B, K, nkv, hd)
+        un = _unrotate(k_new[li], pos[:, :, None])
+        if not np.allclose(un, k_raw, rtol=1e-9, atol=1e-10):
+            bad.append(f"layer {li}: k does not un-rotate to W_k x at positions Q+j")
+        if not np.allclose(v_new[li], v_raw, rtol=1e-9, atol=1e-10):
+            bad.append(f"layer {li}: v is not W_v x")
+    return bad
+
+
 def test_new_kv_rows_are_rotated_with_row_positions():
-    # The k row written for row j equals RoPE(W_k x_j) at position Q_b + j:
-    # un-rotating by the same angle restores an unrotated projection whose
-    # norm equals the rotated one per pair.
+    # k of row j un-rotates (angle of position Q_b + j) to an independent
+    # F.linear of that layer's input; v is that layer's raw projection.
     W, inp = _tiny_case(K=3)
     out = _run_oracle(W, inp, 3)
-    kn = out["k_new"]
-    assert kn.shape == (4, 2, 3, TINY.n_kv_heads, TINY.head_dim)
-    assert np.isfinite(kn).all() and np.isfinite(out["v_new"]).all()
+    ref = _torch_reference_pass(W, inp, 3, full=True)
+    assert _kv_rows_violations(out["k_new"], out["v_new"], ref["x"], W, inp.positions.numpy(), 3) == []
+    # rotating by Q_b + j + 1 instead is caught
+    pos1 = inp.positions.numpy() + 1
+    assert _kv_rows_violations(out["k_new"], out["v_new"], ref["x"], W, pos1, 3) != []
+
+
+@pytest.mark.parametrize("mistake", ["unrotated_k", "position_off_by_one", "k_v_swapped"])
+def test_kv_row_check_fails_on_planted_oracle_mistakes(mistake):
+    # Each plausible mistake in how the oracle forms its new cache rows leaves
+    # the logits unchanged; the row check above must still reject it.
+    W, inp = _tiny_case(K=3)
+    out = _run_oracle(W, inp, 3)
+    ref = _torch_reference_pass(W, inp, 3, full=True)
+    k, v = out["k_new"].copy(), out["v_new"].copy()
+    pos = inp.positions.numpy()[:, None] + np.arange(3)[None, :]
+    if mistake == "unrotated_k":
+        k = _unrotate(k, pos[None, :, :, None])
+    elif mistake == "position_off_by_one":
+        k = oracle.rope_neox(_unrotate(k, pos[None, :, :, None]), (pos + 1)[None, :, :, None], TINY.rope_theta)
+    else:
+        k, v = v, k
+    assert _kv_rows_violations(k, v, ref["x"], W, inp.positions.numpy(), 3) != []
 
 
 # --------------------------------------------------------------- verify / rebuild
@@ -337,6 +408,22 @@ def test_rebuild_capacity_and_bad_page_status():
     out2 = oracle.rebuild_metadata(np.array([0, 0, 0]), K, np.array([27, 0, 0]), Q, pt, 5, P)
     assert out2["status"][0] == oracle.REQ_OK            # 28 + 4 = 32 fits exactly
     np.testing.assert_array_equal(out2["slot_mapping"][0], [1 * P + 12, 1 * P + 13, 1 * P + 14, 1 * P + 15])
+
+
+def test_rebuild_bad_input_status_on_out_of_range_lengths():
+    # Negative lengths or positions, or values too close to 2^31 - 1 for the
+    # next step's K entries, are rejected before any slot arithmetic.
+    P, K = 16, 3
+    lim = 2 ** 31 - 1 - 2 * K
+    pt = np.array([[0, 1], [2, 3], [4, 5], [6, 7], [8, 9]])
+    S = np.array([-1, 5, lim + 1, 5, 5])
+    Q = np.array([7, -3, 7, lim + 1, 9])
+    out = oracle.rebuild_metadata(np.array([1, 1, 1, 1, 1]), K, S, Q, pt, num_pages=10, page_size=P)
+    np.testing.assert_array_equal(out["status"], [oracle.REQ_BAD_INPUT] * 4 + [oracle.REQ_OK])
+    np.testing.assert_array_equal(out["seq_lens"][:4], S[:4])
+    np.testing.assert_array_equal(out["positions"][:4], Q[:4])
+    assert (out["slot_mapping"][:4] == -1).all() and (out["rollback_slots"][:4] == -1).all()
+    assert out["seq_lens"][4] == 7 and out["positions"][4] == 11
 
 
 # --------------------------------------------------------------- acceptance statistics
