@@ -16,7 +16,10 @@ from .drafter import (  # noqa: F401
     gather_prefix_kv,
     causal_paged_attention,
     build_rows,
+    run_layers,
+    lm_head_logits,
     draft_pass,
+    draft_sequential,
     argmax_lowest,
     top2_gap,
 )

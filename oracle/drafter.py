@@ -163,36 +163,22 @@ def top2_gap(logits):
     return part[..., -1] - part[..., -2]
 
 
-def draft_pass(cfg, W, last_token, target_hidden, positions, seq_lens,
-               page_table, k_cache, v_cache, K, perturb_rows=None):
-    """One parallel draft pass for a batch of B requests.
+def run_layers(cfg, W, u, resid, positions, seq_lens, page_table, k_cache, v_cache, perturb_rows=None):
+    """The drafter's 4 layers over the new rows of every request (R2..R6).
 
-    cfg: object with hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn,
-         vocab, rms_eps, rope_theta, page_size.
-    W:   dict of arrays: fc [H,3H], embed [V,H], emb_mask [H], h_shared [H],
-         final_norm [H], lm_head [V,H], layers: list of dicts with norm_e,
-         norm_h (layer 0), attn_norm (layers 1..), w_qkv, w_o, mlp_norm,
-         w_gate, w_up, w_down (all [out, in]).
-    last_token [B]; target_hidden [B, 3H]; positions Q [B]; seq_lens S [B];
-    page_table [B, max_pages]; k_cache/v_cache [L, pages, nkv, P, hd] (read).
-    perturb_rows: optional test hook applied to the [B, K, 2H] layer-0 input.
-
-    Returns a dict: logits [B,K,V], drafts [B,K], gap [B,K] (top-2 logit gap),
-    k_new / v_new [L, B, K, nkv, hd] (the rows the pass writes to the cache at
-    entries S_b + j), h [B, H] (FC output).
+    u [B, K, 2H] layer-0 input rows, resid [B, K, H] the residual stream they
+    start from; row j of request b is at RoPE position positions[b] + j and
+    cache entry seq_lens[b] + j, and attends to entries 0 .. seq_lens[b] + j
+    (the committed ones read from the cache, then the new rows themselves).
+    Returns (resid [B, K, H] after the last layer, k_new, v_new
+    [L, B, K, nkv, hd]: the rows the pass writes to the cache).
     """
-    B = len(last_token)
+    B, K = u.shape[:2]
     nq, nkv, hd = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     eps = cfg.rms_eps
     P = cfg.page_size
     positions = np.asarray(positions, dtype=np.int64)
     seq_lens = np.asarray(seq_lens, dtype=np.int64)
-
-    # Step 1 input: the 3d concat of target hidden states, fused to H (R1).
-    h = linear(target_hidden, W["fc"])
-
-    # Step 2: K rows per request (R2).
-    u, resid = build_rows(cfg, W, last_token, h, K)
     if perturb_rows is not None:
         u = perturb_rows(u)
 
@@ -224,8 +210,102 @@ def draft_pass(cfg, W, last_token, target_hidden, positions, seq_lens,
         gate = linear(x, Lw["w_gate"])
         up = linear(x, Lw["w_up"])
         resid = resid + linear(silu(gate) * up, Lw["w_down"])
+    return resid, k_new, v_new
 
-    logits = linear(rms_norm(resid, W["final_norm"], eps), W["lm_head"])
+
+def lm_head_logits(cfg, W, resid):
+    """Final RMSNorm and LM head: fp64 logits of every row (pages' Step 2)."""
+    return linear(rms_norm(resid, W["final_norm"], cfg.rms_eps), W["lm_head"])
+
+
+def draft_pass(cfg, W, last_token, target_hidden, positions, seq_lens,
+               page_table, k_cache, v_cache, K, perturb_rows=None):
+    """One parallel draft pass for a batch of B requests.
+
+    cfg: object with hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn,
+         vocab, rms_eps, rope_theta, page_size.
+    W:   dict of arrays: fc [H,3H], embed [V,H], emb_mask [H], h_shared [H],
+         final_norm [H], lm_head [V,H], layers: list of dicts with norm_e,
+         norm_h (layer 0), attn_norm (layers 1..), w_qkv, w_o, mlp_norm,
+         w_gate, w_up, w_down (all [out, in]).
+    last_token [B]; target_hidden [B, 3H]; positions Q [B]; seq_lens S [B];
+    page_table [B, max_pages]; k_cache/v_cache [L, pages, nkv, P, hd] (read).
+    perturb_rows: optional test hook applied to the [B, K, 2H] layer-0 input.
+
+    Returns a dict: logits [B,K,V], drafts [B,K], gap [B,K] (top-2 logit gap),
+    k_new / v_new [L, B, K, nkv, hd] (the rows the pass writes to the cache at
+    entries S_b + j), h [B, H] (FC output).
+    """
+    # Step 1 input: the 3d concat of target hidden states, fused to H (R1).
+    h = linear(target_hidden, W["fc"])
+
+    # Step 2: K rows per request (R2), all through the layers in one pass.
+    u, resid = build_rows(cfg, W, last_token, h, K)
+    resid, k_new, v_new = run_layers(cfg, W, u, resid, positions, seq_lens, page_table, k_cache, v_cache,
+                                     perturb_rows=perturb_rows)
+    logits = lm_head_logits(cfg, W, resid)
+    return {
+        "logits": logits,
+        "drafts": argmax_lowest(logits),
+        "gap": top2_gap(logits),
+        "k_new": k_new,
+        "v_new": v_new,
+        "h": h,
+    }
+
+
+def draft_sequential(cfg, W, last_token, target_hidden, positions, seq_lens,
+                     page_table, k_cache, v_cache, K, tokens=None):
+    """Sequential (EAGLE-style) drafting: K passes of one row per request.
+
+    The chain P-EAGLE breaks ([zh] "P-EAGLE 如何打破这个链"): every draft
+    needs the embedding of the token drafted just before it and the hidden
+    state that produced it. Readings (also in the design notes):
+     S1  Pass 0 is the parallel pass's row 0: embedding of the last accepted
+         token and the FC-fused target hidden state. Pass j > 0 takes the
+         embedding of draft j-1 and, as its hidden half and residual start,
+         the drafter's own final residual stream of pass j-1 (the hidden
+         state before the final RMSNorm, H-wide, where the parallel pass uses
+         h_shared).
+     S2  Pass j sits at RoPE position Q_b + j and cache entry S_b + j; its
+         k/v rows are written there before pass j+1 attends over entries
+         0 .. S_b + j + 1, so the cache holds real rows for every pass.
+    tokens: optional [B, K] int array; when given, pass j > 0 takes
+    tokens[:, j-1] as its input token instead of its own draft j-1 (to
+    compare against another implementation whose drafts differ at a near
+    tie). Returns the same dict as draft_pass (h is the FC output).
+    """
+    B = len(last_token)
+    H = cfg.hidden
+    eps = cfg.rms_eps
+    P = cfg.page_size
+    positions = np.asarray(positions, dtype=np.int64)
+    seq_lens = np.asarray(seq_lens, dtype=np.int64)
+    kc = np.array(k_cache, dtype=np.float64, copy=True)
+    vc = np.array(v_cache, dtype=np.float64, copy=True)
+    L0 = W["layers"][0]
+    embed = np.asarray(W["embed"], dtype=np.float64)
+
+    h = linear(target_hidden, W["fc"])
+    tok = np.asarray(last_token, dtype=np.int64)
+    hid = h
+    logits = np.empty((B, K, cfg.vocab), dtype=np.float64)
+    k_new = np.empty((cfg.n_layers, B, K, cfg.n_kv_heads, cfg.head_dim), dtype=np.float64)
+    v_new = np.empty_like(k_new)
+    for j in range(K):
+        u = np.concatenate([rms_norm(embed[tok], L0["norm_e"], eps), rms_norm(hid, L0["norm_h"], eps)], axis=-1)
+        resid, kj, vj = run_layers(cfg, W, u[:, None, :], hid[:, None, :].copy(), positions + j, seq_lens + j,
+                                   page_table, kc, vc)
+        logits[:, j] = lm_head_logits(cfg, W, resid)[:, 0]
+        k_new[:, :, j], v_new[:, :, j] = kj[:, :, 0], vj[:, :, 0]
+        for b in range(B):                                       # S2: the pass's rows join the cache
+            e = int(seq_lens[b]) + j
+            page = int(page_table[b][e // P])
+            kc[:, page, :, e % P, :] = kj[:, b, 0]
+            vc[:, page, :, e % P, :] = vj[:, b, 0]
+        d = argmax_lowest(logits[:, j])
+        tok = d if tokens is None or j + 1 >= K else np.asarray(tokens, dtype=np.int64)[:, j]
+        hid = resid[:, 0]
     return {
         "logits": logits,
         "drafts": argmax_lowest(logits),

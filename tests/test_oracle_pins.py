@@ -334,6 +334,131 @@ def test_kv_row_check_fails_on_planted_oracle_mistakes(mistake):
     assert _kv_rows_violations(k, v, ref["x"], W, inp.positions.numpy(), 3) != []
 
 
+# --------------------------------------------------------------- sequential drafting
+
+def _torch_sequential(W, inp, K):
+    """Independent float64 restatement of sequential EAGLE drafting: per
+    request, K one-row passes; each layer's cache is a Python list of the
+    committed rows (walked through the page table) to which every pass
+    appends its own k/v row; the single query attends to the whole list."""
+    cfg = TINY
+    d = torch.float64
+    t = lambda a: a.to(d)
+    H, nq, nkv, hd = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    eps = cfg.rms_eps
+    G = nq // nkv
+
+    def norm(x, g):
+        return F.rms_norm(x, (x.shape[-1],), weight=t(g), eps=eps)
+
+    def rope(x, pos):
+        half = hd // 2
+        inv = cfg.rope_theta ** (-(torch.arange(half, dtype=d) * 2.0) / hd)
+        ang = torch.tensor(float(pos), dtype=d) * inv
+        z = torch.complex(x[..., :half], x[..., half:]) * torch.polar(torch.ones_like(ang), ang)
+        return torch.cat([z.real, z.imag], dim=-1)
+
+    B = inp.last_token.shape[0]
+    h = F.linear(t(inp.target_hidden), t(W["fc"]))
+    logits = torch.empty(B, K, cfg.vocab, dtype=d)
+    k_rows = torch.empty(4, B, K, nkv, hd, dtype=d)
+    v_rows = torch.empty(4, B, K, nkv, hd, dtype=d)
+    L0 = W["layers"][0]
+    for b in range(B):
+        S, Q = int(inp.seq_lens[b]), int(inp.positions[b])
+        ks = [[t(inp.k_cache[li, int(inp.page_table[b, e // 16]), :, e % 16, :]) for e in range(S)]
+              for li in range(4)]
+        vs = [[t(inp.v_cache[li, int(inp.page_table[b, e // 16]), :, e % 16, :]) for e in range(S)]
+              for li in range(4)]
+        tok, hid = int(inp.last_token[b]), h[b]
+        for j in range(K):
+            x = torch.cat([norm(t(W["embed"][tok])[None], L0["norm_e"]), norm(hid[None], L0["norm_h"])], -1)
+            r = hid[None].clone()
+            for li, Lw in enumerate(W["layers"]):
+                if li > 0:
+                    x = norm(r, Lw["attn_norm"])
+                qkv = F.linear(x, t(Lw["w_qkv"]))[0]
+                q = rope(qkv[: nq * hd].reshape(nq, hd), Q + j)
+                ks[li].append(rope(qkv[nq * hd:(nq + nkv) * hd].reshape(nkv, hd), Q + j))
+                vs[li].append(qkv[(nq + nkv) * hd:].reshape(nkv, hd))
+                k_rows[li, b, j], v_rows[li, b, j] = ks[li][-1], vs[li][-1]
+                k_all = torch.stack(ks[li]).permute(1, 0, 2).repeat_interleave(G, 0)
+                v_all = torch.stack(vs[li]).permute(1, 0, 2).repeat_interleave(G, 0)
+                a = F.scaled_dot_product_attention(q[:, None, :], k_all, v_all)[:, 0, :]
+                r = r + F.linear(a.reshape(1, nq * hd), t(Lw["w_o"]))
+                x = norm(r, Lw["mlp_norm"])
+                r = r + F.linear(F.silu(F.linear(x, t(Lw["w_gate"]))) * F.linear(x, t(Lw["w_up"])),
+                                 t(Lw["w_down"]))
+            logits[b, j] = F.linear(norm(r, W["final_norm"]), t(W["lm_head"]))[0]
+            tok, hid = int(torch.argmax(logits[b, j])), r[0]
+    return dict(logits=logits.numpy(), k_new=k_rows.numpy(), v_new=v_rows.numpy())
+
+
+def _run_sequential(W, inp, K, **kw):
+    Wn = synth.weights_to_numpy(W)
+    return oracle.draft_sequential(
+        TINY, Wn, inp.last_token.numpy(), inp.target_hidden.double().numpy(),
+        inp.positions.numpy(), inp.seq_lens.numpy(), inp.page_table.numpy(),
+        inp.k_cache.double().numpy(), inp.v_cache.double().numpy(), K, **kw)
+
+
+def test_sequential_matches_independent_torch_restatement():
+    W, inp = _tiny_case(K=4)
+    out = _run_sequential(W, inp, 4)
+    ref = _torch_sequential(W, inp, 4)
+    np.testing.assert_allclose(out["logits"], ref["logits"], rtol=1e-10, atol=1e-10)
+    ok = out["gap"] > 1e-9
+    np.testing.assert_array_equal(out["drafts"][ok], ref["logits"].argmax(-1)[ok])
+    # every pass's cache rows, the last pass's included
+    np.testing.assert_allclose(out["k_new"], ref["k_new"], rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(out["v_new"], ref["v_new"], rtol=1e-10, atol=1e-10)
+
+
+def test_sequential_k1_is_the_parallel_pass_k1():
+    # one sequential step and a one-row parallel pass are the same computation
+    W, inp = _tiny_case(K=1)
+    seq = _run_sequential(W, inp, 1)
+    par = _run_oracle(W, inp, 1)
+    for k in ("logits", "k_new", "v_new"):
+        np.testing.assert_allclose(seq[k], par[k], rtol=1e-12, atol=1e-12)
+
+
+def test_sequential_row0_equals_parallel_row0_and_later_rows_differ():
+    W, inp = _tiny_case(K=4)
+    seq = _run_sequential(W, inp, 4)
+    par = _run_oracle(W, inp, 4)
+    np.testing.assert_allclose(seq["logits"][:, 0], par["logits"][:, 0], rtol=1e-12, atol=1e-12)
+    assert np.abs(seq["logits"][:, 1:] - par["logits"][:, 1:]).max() > 1e-3
+
+
+def test_sequential_prefix_consistency_and_forced_tokens():
+    W, inp = _tiny_case(K=5)
+    full = _run_sequential(W, inp, 5)
+    part = _run_sequential(W, inp, 2)
+    np.testing.assert_allclose(part["logits"], full["logits"][:, :2], rtol=1e-12, atol=1e-12)
+    # forcing the oracle's own drafts changes nothing
+    same = _run_sequential(W, inp, 5, tokens=full["drafts"])
+    np.testing.assert_array_equal(same["logits"], full["logits"])
+    # forcing another token at pass 1 leaves passes 0 and 1 unchanged and moves pass 2
+    forced = full["drafts"].copy()
+    forced[:, 1] = (forced[:, 1] + 1) % TINY.vocab
+    other = _run_sequential(W, inp, 5, tokens=forced)
+    np.testing.assert_array_equal(other["logits"][:, :2], full["logits"][:, :2])
+    assert np.abs(other["logits"][:, 2] - full["logits"][:, 2]).max() > 1e-6
+
+
+def test_sequential_cache_rows_are_the_passes_own_rows():
+    # the k/v rows pass j writes are those the torch restatement appends: check
+    # through the next pass, which must see them (perturbing one changes it)
+    W, inp = _tiny_case(K=3)
+    out = _run_sequential(W, inp, 3)
+    assert out["k_new"].shape == (4, 2, 3, TINY.n_kv_heads, TINY.head_dim)
+    # pass 0's rows equal the parallel pass's row 0
+    par = _run_oracle(W, inp, 3)
+    np.testing.assert_allclose(out["k_new"][:, :, 0], par["k_new"][:, :, 0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out["v_new"][:, :, 0], par["v_new"][:, :, 0], rtol=1e-12, atol=1e-12)
+
+
 # --------------------------------------------------------------- verify / rebuild
 
 def _brute_accept(d, g):
