@@ -496,25 +496,28 @@ def bench_ours(args):
     # ---------------- flatness in K at B=1 (step graphs of the draft pass
     # followed by the verify/rebuild, ~3 us of the step)
     k_sweep = None
+    k_sweep_seq = None
     if not args.no_sweep and wl.B == 1 and wl.shape.name.startswith("qwen"):
-        k_sweep = {}
+        k_sweep, k_sweep_seq = {}, {}
         for Ks in (3, 7, 11):
             inp_k = synth.make_step_inputs(wl, device=dev, K=Ks)
             g_k = torch.zeros(1, Ks + 1, dtype=torch.int32, device=dev)
-            sg_k = drafter.step_graph(inp_k.last_token, inp_k.target_hidden, inp_k.positions, inp_k.seq_lens,
-                                      inp_k.page_table, inp_k.num_pages, inp_k.k_cache, inp_k.v_cache, Ks, g_k)
-            for _ in range(10):
-                sg_k.launch()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            n = 300
-            e0.record(stream)
-            for _ in range(n):
-                sg_k.launch()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            k_sweep[str(Ks)] = e0.elapsed_time(e1) / n
-            sg_k.close()
+            for sequential, out in ((False, k_sweep), (True, k_sweep_seq)):
+                sg_k = drafter.step_graph(inp_k.last_token, inp_k.target_hidden, inp_k.positions, inp_k.seq_lens,
+                                          inp_k.page_table, inp_k.num_pages, inp_k.k_cache, inp_k.v_cache, Ks, g_k,
+                                          sequential=sequential)
+                for _ in range(10):
+                    sg_k.launch()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                n = 100 if sequential else 300
+                e0.record(stream)
+                for _ in range(n):
+                    sg_k.launch()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                out[str(Ks)] = e0.elapsed_time(e1) / n
+                sg_k.close()
             del inp_k
 
     # ---------------- end to end through the public API with pinned host buffers:
@@ -626,6 +629,12 @@ def bench_ours(args):
         line["k_sweep_step_ms"] = k_sweep
         line["k_sweep_note"] = "ms per step-graph replay (draft pass + verify/rebuild) at B=1, K = 3 / 7 / 11"
         line["k11_over_k3"] = k_sweep["11"] / k_sweep["3"]
+    if k_sweep_seq:
+        line["k_sweep_sequential_step_ms"] = k_sweep_seq
+        line["k_sweep_sequential_note"] = ("the same steps with sequential EAGLE-style drafting (K one-row passes "
+                                           "on the same kernels, pe_draft_sequential) in place of the parallel pass")
+        line["sequential_k11_over_k3"] = k_sweep_seq["11"] / k_sweep_seq["3"]
+        line["parallel_speedup_over_sequential"] = {k: k_sweep_seq[k] / k_sweep[k] for k in k_sweep}
     if cold:
         line["cold_l2"] = cold
     if sweep:

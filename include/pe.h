@@ -133,6 +133,29 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K,
              void* k_cache, void* v_cache,
              int32_t* drafts, float* logits_dbg, int32_t* status, void* stream);
 
+/* Sequential (EAGLE-style) drafting on the same kernels: the chain that
+ * P-EAGLE breaks ("在 Amazon SageMaker AI 上使用 P-EAGLE 并行化推测解码",
+ * "P-EAGLE 如何打破这个链": each draft needs the embedding of the token drafted
+ * just before it and the hidden state that produced it). K passes of one row
+ * per request, each a full drafter forward:
+ *  - pass 0 is the parallel pass's row 0 (embedding of last_token, FC-fused
+ *    target hidden state);
+ *  - pass j > 0 takes the embedding of draft j-1 and, as its hidden input and
+ *    residual start, the drafter's own final residual stream of pass j-1
+ *    (the hidden state before the final RMSNorm);
+ *  - pass j sits at RoPE position Q_b + j and cache entry S_b + j and writes
+ *    its k/v rows there before pass j+1 attends over them.
+ * Same arguments, layouts, outputs and errors as pe_draft (drafts[b, j] is
+ * pass j's argmax; logits_dbg row (b, j) its logits); every entry
+ * S_b .. S_b+K-1 the step writes is validated by pass 0. The launch count
+ * grows linearly in K (K forward passes), where pe_draft's does not. */
+int pe_draft_sequential(pe_handle* h, int32_t B, int32_t K,
+                        const int32_t* last_token, const void* target_hidden,
+                        const int32_t* positions, const int32_t* seq_lens,
+                        const int32_t* page_table, int32_t max_pages, int32_t num_pages,
+                        void* k_cache, void* v_cache,
+                        int32_t* drafts, float* logits_dbg, int32_t* status, void* stream);
+
 /* Greedy verification + batch-metadata rebuild + KV rollback (one kernel).
  * h may be NULL (the kernel needs no drafter state).
  *
@@ -214,6 +237,18 @@ int pe_step_graph_create(pe_handle* h, int32_t B, int32_t K, const int32_t* last
                          int32_t* seq_lens_out, int32_t* accepted, int32_t* bonus, int32_t* emitted,
                          int32_t* slot_mapping, int32_t* rollback_slots, int32_t* verify_status,
                          pe_step_graph** out);
+/* The same with the draft half chosen by draft_mode: PE_DRAFT_PARALLEL
+ * (pe_draft, what pe_step_graph_create captures) or PE_DRAFT_SEQUENTIAL
+ * (pe_draft_sequential). */
+#define PE_DRAFT_PARALLEL   0
+#define PE_DRAFT_SEQUENTIAL 1
+int pe_step_graph_create_ex(pe_handle* h, int32_t draft_mode, int32_t B, int32_t K, const int32_t* last_token,
+                            const void* target_hidden, const int32_t* positions, const int32_t* seq_lens,
+                            const int32_t* page_table, int32_t max_pages, int32_t num_pages, void* k_cache,
+                            void* v_cache, int32_t* drafts, int32_t* draft_status, const int32_t* target_tokens,
+                            int32_t* positions_out, int32_t* seq_lens_out, int32_t* accepted, int32_t* bonus,
+                            int32_t* emitted, int32_t* slot_mapping, int32_t* rollback_slots,
+                            int32_t* verify_status, pe_step_graph** out);
 int pe_step_graph_launch(pe_step_graph* g, void* stream);
 /* kernels one replay launches */
 int pe_step_graph_launch_count(const pe_step_graph* g);

@@ -17,13 +17,14 @@ PE_OK = 0
 PE_REQ_OK, PE_REQ_CAPACITY, PE_REQ_BAD_PAGE, PE_REQ_BAD_INPUT = 0, 1, 2, 3
 PE_DTYPE_BF16, PE_DTYPE_FP32 = 0, 1
 PE_DEVERR_GEMM_TIMEOUT, PE_DEVERR_ATTN_TIMEOUT, PE_DEVERR_CHAIN_TIMEOUT = 1, 2, 4
+PE_DRAFT_PARALLEL, PE_DRAFT_SEQUENTIAL = 0, 1
 
 EXPORTS = (
     "pe_init_drafter", "pe_draft", "pe_verify_rebuild", "pe_device_errors",
     "pe_last_launch_count", "pe_destroy", "pe_last_error", "pe_abi_version", "pe_linear_scratch", "pe_linear",
     "pe_profile_start", "pe_profile_stop", "pe_kernel_name",
     "pe_step_graph_create", "pe_step_graph_launch", "pe_step_graph_launch_count", "pe_step_graph_destroy",
-    "pe_linear_noalloc", "pe_test_stall_chain",
+    "pe_linear_noalloc", "pe_test_stall_chain", "pe_draft_sequential", "pe_step_graph_create_ex",
 )
 KERNEL_KINDS = ("fc", "row_build", "rmsnorm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "argmax",
                 "layer_chain")
@@ -81,6 +82,8 @@ def load():
     lib.pe_init_drafter.restype = ctypes.c_int
     lib.pe_draft.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.pe_draft.restype = ctypes.c_int
+    lib.pe_draft_sequential.argtypes = lib.pe_draft.argtypes
+    lib.pe_draft_sequential.restype = ctypes.c_int
     lib.pe_verify_rebuild.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                       _vp, _vp, _vp, _vp, _vp]
     lib.pe_verify_rebuild.restype = ctypes.c_int
@@ -107,6 +110,8 @@ def load():
     lib.pe_step_graph_create.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp,
                                          _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(_vp)]
     lib.pe_step_graph_create.restype = ctypes.c_int
+    lib.pe_step_graph_create_ex.argtypes = [_vp, _i32] + lib.pe_step_graph_create.argtypes[1:]
+    lib.pe_step_graph_create_ex.restype = ctypes.c_int
     lib.pe_step_graph_launch.argtypes = [_vp, _vp]
     lib.pe_step_graph_launch.restype = ctypes.c_int
     lib.pe_step_graph_launch_count.argtypes = [_vp]
@@ -178,8 +183,9 @@ class Drafter:
         self._h = h
 
     def draft(self, last_token, target_hidden, positions, seq_lens, page_table, num_pages, k_cache, v_cache,
-              K, drafts=None, status=None, logits=None, stream=None):
-        """Enqueue one draft pass; returns (drafts [B, K] int32, status [B] int32)."""
+              K, drafts=None, status=None, logits=None, stream=None, sequential=False):
+        """Enqueue one draft pass (K sequential one-row passes with
+        sequential=True); returns (drafts [B, K] int32, status [B] int32)."""
         B = last_token.shape[0]
         dev = self.device
         for name, t in (("last_token", last_token), ("positions", positions), ("seq_lens", seq_lens),
@@ -194,9 +200,10 @@ class Drafter:
             status = torch.empty(B, dtype=torch.int32, device=dev)
         if logits is not None:
             _need(logits, torch.float32, dev, "logits")
-        _check(load().pe_draft(self._h, B, K, _p(last_token), _p(target_hidden), _p(positions), _p(seq_lens),
-                               _p(page_table), page_table.shape[1], num_pages, _p(k_cache), _p(v_cache),
-                               _p(drafts), _p(logits), _p(status), _stream_ptr(stream)))
+        fn = load().pe_draft_sequential if sequential else load().pe_draft
+        _check(fn(self._h, B, K, _p(last_token), _p(target_hidden), _p(positions), _p(seq_lens),
+                  _p(page_table), page_table.shape[1], num_pages, _p(k_cache), _p(v_cache),
+                  _p(drafts), _p(logits), _p(status), _stream_ptr(stream)))
         return drafts, status
 
     def profile_start(self, kind, max_launches):
@@ -219,11 +226,11 @@ class Drafter:
         _check(load().pe_test_stall_chain(self._h, _stream_ptr(stream)))
 
     def step_graph(self, last_token, target_hidden, positions, seq_lens, page_table, num_pages, k_cache, v_cache,
-                   K, target_tokens, positions_out=None, seq_lens_out=None):
+                   K, target_tokens, positions_out=None, seq_lens_out=None, sequential=False):
         """Capture draft + verify/rebuild into a replayable StepGraph over
         fixed buffers (outputs allocated here unless given)."""
         return StepGraph(self, last_token, target_hidden, positions, seq_lens, page_table, num_pages, k_cache,
-                         v_cache, K, target_tokens, positions_out, seq_lens_out)
+                         v_cache, K, target_tokens, positions_out, seq_lens_out, sequential=sequential)
 
     def device_errors(self, stream=None):
         bits = ctypes.c_uint32(0)
@@ -247,7 +254,7 @@ class StepGraph:
     library; ``launch()`` replays it. Buffers are fixed at capture."""
 
     def __init__(self, drafter, last_token, target_hidden, positions, seq_lens, page_table, num_pages, k_cache,
-                 v_cache, K, target_tokens, positions_out=None, seq_lens_out=None):
+                 v_cache, K, target_tokens, positions_out=None, seq_lens_out=None, sequential=False):
         lib = load()
         dev = drafter.device
         B = last_token.shape[0]
@@ -265,8 +272,8 @@ class StepGraph:
                         seq_lens=seq_lens_out if seq_lens_out is not None else z(B))
         o = self.out
         g = _vp()
-        _check(lib.pe_step_graph_create(
-            drafter._h, B, K, _p(last_token), _p(target_hidden), _p(positions), _p(seq_lens), _p(page_table),
+        _check(lib.pe_step_graph_create_ex(
+            drafter._h, PE_DRAFT_SEQUENTIAL if sequential else PE_DRAFT_PARALLEL, B, K, _p(last_token), _p(target_hidden), _p(positions), _p(seq_lens), _p(page_table),
             page_table.shape[1], num_pages, _p(k_cache), _p(v_cache), _p(o["drafts"]), _p(o["draft_status"]),
             _p(target_tokens), _p(o["positions"]), _p(o["seq_lens"]), _p(o["accepted"]), _p(o["bonus"]),
             _p(o["emitted"]), _p(o["slot_mapping"]), _p(o["rollback_slots"]), _p(o["status"]), ctypes.byref(g)))

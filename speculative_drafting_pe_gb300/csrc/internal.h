@@ -153,11 +153,20 @@ bool chain_supported(int device);
 
 struct RowBuildParams {
     int B, K, H, V, hd, max_pages, num_pages, page_size;
-    const int32_t* last_token;
+    const int32_t* last_token; // row-0 token of request b: last_token[b * tok_stride]
+    int tok_stride;
     const int32_t* positions;
     const int32_t* seq_lens;
     const int32_t* page_table;
-    const float* h;            // [B, H] FC output
+    const float* h;            // row-0 hidden of request b: h[b * hid_stride .. + H) (FC output, or a residual row)
+    int hid_stride;
+    // This pass's rows sit j0 entries (and positions) past S_b / Q_b: row j
+    // at entry S_b + j0 + j, RoPE position Q_b + j0 + j (0 for the parallel
+    // pass; the pass index for sequential drafting). k_check: entries past
+    // S_b that the whole step writes, validated against the page table.
+    int j0, k_check;
+    int status_in;             // 1: status[b] was set by an earlier pass; read it, write nothing
+    int32_t* seq_eff;          // OUT [B] or null: S_b + j0 (the attention's committed-entry count)
     const void* embed;         // [V, H]
     const void* emb_mask;      // [H]
     const void* h_shared;      // [H]
@@ -189,8 +198,10 @@ int launch_row_build(int dtype, const RowBuildParams& p, cudaStream_t s, bool pd
 int launch_logits_rms_scale(float* logits, int rows, int V, int ld, const float* ss, int ss_ld, float scale,
                             float eps, cudaStream_t s, bool pdl);
 
+// drafts[b * out_stride + j] = decoded record of row b * K + j (-1 when the
+// request is not OK)
 int launch_argmax_finalize(const unsigned long long* amax, const int32_t* status, int B, int K, int32_t* drafts,
-                           cudaStream_t s, bool pdl);
+                           int out_stride, cudaStream_t s, bool pdl);
 
 // ---------------------------------------------------------------- attention
 

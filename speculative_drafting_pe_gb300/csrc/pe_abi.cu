@@ -43,6 +43,7 @@ struct pe_handle {
     unsigned long long* amax = nullptr;
     int* row_slot = nullptr;
     int32_t* attn_order = nullptr;   // [max_batch] requests by decreasing seq_len
+    int32_t* seq_eff = nullptr;      // [max_batch] S_b + j0 of the current sequential pass
     float2* rope_cs = nullptr;
     double* inv_freq = nullptr;
     float* gemm_ws = nullptr;
@@ -202,7 +203,7 @@ void free_handle(pe_handle* h) {
     void* ptrs[] = {h->h,    h->resid,    h->u,        h->xn,         h->ss,      h->q,            h->attn,      h->act,
                     h->amax, h->row_slot, h->attn_order, h->rope_cs, h->inv_freq, h->gemm_ws, h->gemm_tickets, h->attn_ws,
                     h->attn_tickets, h->err, h->chain_ctr, h->chain_ws, h->chain_tickets, h->attn_items,
-                    h->attn_plan};
+                    h->attn_plan, h->seq_eff};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     delete h;
@@ -357,6 +358,7 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
     if (a == PE_OK) a = dev_alloc(&h->amax, R * 8);
     if (a == PE_OK) a = dev_alloc(&h->row_slot, R * 4);
     if (a == PE_OK) a = dev_alloc(&h->attn_order, static_cast<size_t>(max_batch) * 4);
+    if (a == PE_OK) a = dev_alloc(&h->seq_eff, static_cast<size_t>(max_batch) * 4);
     if (a == PE_OK) a = dev_alloc(&h->rope_cs, R * (hd / 2) * sizeof(float2));
     if (a == PE_OK) a = dev_alloc(&h->inv_freq, (hd / 2) * sizeof(double));
     if (a == PE_OK) a = dev_alloc(&h->gemm_ws, h->gemm_ws_floats * 4);
@@ -449,28 +451,40 @@ int pe_device_errors(pe_handle* h, void* stream, uint32_t* out_bits) {
     return PE_OK;
 }
 
-int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, const void* target_hidden,
-             const int32_t* positions, const int32_t* seq_lens, const int32_t* page_table, int32_t max_pages,
-             int32_t num_pages, void* k_cache, void* v_cache, int32_t* drafts, float* logits_dbg, int32_t* status,
-             void* stream) {
-    if (h == nullptr) { set_error("null handle"); return PE_ERR_ARG; }
-    if (B < 1 || B > h->max_batch) { set_error("B out of range 1..max_batch"); return PE_ERR_ARG; }
-    if (K < 1 || K > h->cfg.k_max) { set_error("K out of range 1..k_max"); return PE_ERR_ARG; }
-    if (!last_token || !target_hidden || !positions || !seq_lens || !page_table || !k_cache || !v_cache || !drafts ||
-        !status) {
-        set_error("null tensor argument");
-        return PE_ERR_ARG;
-    }
-    if (max_pages < 1 || num_pages < 1) { set_error("max_pages and num_pages must be >= 1"); return PE_ERR_ARG; }
+}  // extern "C"
+
+namespace {
+
+// One draft pass over B requests of ps.Kp rows each (all K rows of the
+// parallel pass, or one row of a sequential pass).
+struct PassSpec {
+    int B = 0, Kp = 0;
+    int j0 = 0;                    // entry / position offset of the pass's rows
+    int k_check = 0;               // entries past S_b the step writes (validated by the first pass)
+    bool run_fc = true;            // compute h = W_fc [h_lo; h_mid; h_hi] first
+    const int32_t* tok = nullptr;  // row-0 token of request b: tok[b * tok_stride]
+    int tok_stride = 1;
+    const float* hid = nullptr;    // row-0 hidden of request b (null: the FC output)
+    int hid_stride = 0;
+    bool status_in = false;        // status was written by an earlier pass of the step
+    bool seq_eff_out = false;      // the attention reads S_b + j0 from the workspace
+    int32_t* drafts = nullptr;     // drafts[b * drafts_stride + j]
+    int drafts_stride = 0;
+    float* logits = nullptr;       // optional: pass row n (= b * Kp + j) at logits + n * logits_ld
+    int logits_ld = 0;
+};
+
+int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, const int32_t* positions,
+                 const int32_t* seq_lens, const int32_t* page_table, int32_t max_pages, int32_t num_pages,
+                 void* k_cache, void* v_cache, int32_t* status, cudaStream_t s, int& launches) {
     const pe_config& c = h->cfg;
     const int H = c.hidden, F = c.ffn, V = c.vocab, hd = c.head_dim, nq = c.n_q_heads, nkv = c.n_kv_heads;
     const int qd = nq * hd, qkv_rows = (nq + 2 * nkv) * hd;
+    const int B = ps.B, K = ps.Kp;
     const int R = B * K;
     const int eb = static_cast<int>(h->elem);
     const int dt = c.dtype;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool pdl = h->pdl;
-    int launches = 0;
     int rc;
 
     // GEMM plans (bn depends only on the row count)
@@ -495,7 +509,7 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     // the map (QKV, O and down may take narrower tiles than gate/up and the LM head)
     CUtensorMap tm_th, tm_u, tm_xq, tm_xn, tm_attn, tm_act;
     if (p_qkv0.bn != p_qkv.bn || p_lm.bn != p_gu.bn) { set_error("GEMM token tiles disagree"); return PE_ERR_UNSUPPORTED; }
-    if ((rc = act_map(h, &tm_th, target_hidden, B, 3 * H, p_fc.bn)) != PE_OK) return rc;
+    if (ps.run_fc && (rc = act_map(h, &tm_th, target_hidden, B, 3 * H, p_fc.bn)) != PE_OK) return rc;
     if ((rc = act_map(h, &tm_u, h->u, R, 2 * H, p_qkv.bn)) != PE_OK) return rc;      // layer 0's QKV
     if ((rc = act_map(h, &tm_xq, h->xn, R, H, p_qkv.bn)) != PE_OK) return rc;       // QKV of layers 1-3
     if ((rc = act_map(h, &tm_xn, h->xn, R, H, p_gu.bn)) != PE_OK) return rc;        // gate/up, LM head
@@ -542,8 +556,8 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         return r;
     };
 
-    // a1: h = W_fc [h_lo; h_mid; h_hi]
-    {
+    // a1: h = W_fc [h_lo; h_mid; h_hi] (the first pass of a step)
+    if (ps.run_fc) {
         GemmParams p = base;
         p.M = H; p.N = B; p.Kd = 3 * H;
         p.out_f32 = h->h; p.ld_out = H;
@@ -555,8 +569,12 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         RowBuildParams rp{};
         rp.B = B; rp.K = K; rp.H = H; rp.V = V; rp.hd = hd;
         rp.max_pages = max_pages; rp.num_pages = num_pages; rp.page_size = c.page_size;
-        rp.last_token = last_token; rp.positions = positions; rp.seq_lens = seq_lens; rp.page_table = page_table;
-        rp.h = h->h; rp.embed = h->w.embed; rp.emb_mask = h->w.emb_mask; rp.h_shared = h->w.h_shared;
+        rp.last_token = ps.tok; rp.tok_stride = ps.tok_stride;
+        rp.positions = positions; rp.seq_lens = seq_lens; rp.page_table = page_table;
+        rp.h = ps.hid != nullptr ? ps.hid : h->h; rp.hid_stride = ps.hid != nullptr ? ps.hid_stride : H;
+        rp.j0 = ps.j0; rp.k_check = ps.k_check; rp.status_in = ps.status_in ? 1 : 0;
+        rp.seq_eff = ps.j0 > 0 || ps.seq_eff_out ? h->seq_eff : nullptr;
+        rp.embed = h->w.embed; rp.emb_mask = h->w.emb_mask; rp.h_shared = h->w.h_shared;
         rp.norm_e = h->w.layer[0].norm_e; rp.norm_h = h->w.layer[0].norm_h; rp.eps = c.rms_eps;
         rp.u = h->u; rp.resid = h->resid; rp.row_slot = h->row_slot; rp.rope_cs = h->rope_cs;
         rp.inv_freq = h->inv_freq; rp.amax = h->amax; rp.status = status;
@@ -568,6 +586,7 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
         rp.piece_min_tiles = p_at.piece_min_tiles;
         if ((rc = run(PE_KERNEL_ROW_BUILD, [&] { return launch_row_build(dt, rp, s, pdl); })) != PE_OK) return rc;
     }
+    const int32_t* rp_seq = ps.j0 > 0 || ps.seq_eff_out ? h->seq_eff : seq_lens;
     const size_t layer_elems = static_cast<size_t>(num_pages) * nkv * c.page_size * hd;
     auto kcache = [&](int l) { return static_cast<char*>(k_cache) + l * layer_elems * h->elem; };
     auto vcache = [&](int l) { return static_cast<char*>(v_cache) + l * layer_elems * h->elem; };
@@ -601,7 +620,7 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
     };
     auto gp_lm = [&]() {          // a7: LM head + fused argmax on W_lm (g * r): 1/rms(r) > 0 does not move it
         GemmParams p = base;
-        p.M = V; p.Kd = H; p.amax = h->amax; p.logits = logits_dbg; p.ld_logits = V;
+        p.M = V; p.Kd = H; p.amax = h->amax; p.logits = ps.logits; p.ld_logits = ps.logits_ld;
         // the LM head's first ~40 MB of weights stay in L2 between steps
         // (measured: 40 MB faster, 80 and 100 MB slower than none at B=1, B=4)
         p.keep_tiles = static_cast<int>((40LL << 20) / (128LL * H * static_cast<long long>(h->elem)));
@@ -669,7 +688,8 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
             ap.B = B; ap.K = K; ap.nq = nq; ap.nkv = nkv; ap.hd = hd;
             ap.max_pages = max_pages; ap.num_pages = num_pages; ap.page_size = c.page_size;
             ap.chunk = p_at.chunk; ap.max_splits = p_at.max_splits;
-            ap.q = h->q; ap.k_cache = kc; ap.v_cache = vc; ap.page_table = page_table; ap.seq_lens = seq_lens;
+            ap.q = h->q; ap.k_cache = kc; ap.v_cache = vc; ap.page_table = page_table;
+            ap.seq_lens = rp_seq;   // S_b + j0: the entries committed before this pass's rows
             ap.status = status; ap.out = h->attn;
             ap.order = attn_umma && B <= 1024 ? h->attn_order : nullptr; ap.ws = h->attn_ws; ap.tickets = h->attn_tickets; ap.err = h->err;
             ap.layer_page0 = l * num_pages;
@@ -716,15 +736,87 @@ int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, cons
                  [&] { return launch_gemm(dt, EPI_ARGMAX, h->tm_lm, h->tm_lm, tm_xn, p_lm, p, s, pdl); });
         if (rc != PE_OK) return rc;
     }
-    if (logits_dbg != nullptr) {
+    if (ps.logits != nullptr) {
         rc = run(PE_KERNEL_LM_HEAD, [&] {
-            return launch_logits_rms_scale(logits_dbg, R, V, V, h->ss, h->ss_ld, 1.0f / static_cast<float>(H),
-                                           c.rms_eps, s, pdl);
+            return launch_logits_rms_scale(ps.logits, R, V, ps.logits_ld, h->ss, h->ss_ld,
+                                           1.0f / static_cast<float>(H), c.rms_eps, s, pdl);
         });
         if (rc != PE_OK) return rc;
     }
-    rc = run(PE_KERNEL_ARGMAX, [&] { return launch_argmax_finalize(h->amax, status, B, K, drafts, s, pdl); });
+    rc = run(PE_KERNEL_ARGMAX,
+             [&] { return launch_argmax_finalize(h->amax, status, B, K, ps.drafts, ps.drafts_stride, s, pdl); });
     if (rc != PE_OK) return rc;
+    return PE_OK;
+}
+
+
+int check_draft_args(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, const void* target_hidden,
+                     const int32_t* positions, const int32_t* seq_lens, const int32_t* page_table, int32_t max_pages,
+                     int32_t num_pages, void* k_cache, void* v_cache, int32_t* drafts, int32_t* status) {
+    if (h == nullptr) { set_error("null handle"); return PE_ERR_ARG; }
+    if (B < 1 || B > h->max_batch) { set_error("B out of range 1..max_batch"); return PE_ERR_ARG; }
+    if (K < 1 || K > h->cfg.k_max) { set_error("K out of range 1..k_max"); return PE_ERR_ARG; }
+    if (!last_token || !target_hidden || !positions || !seq_lens || !page_table || !k_cache || !v_cache || !drafts ||
+        !status) {
+        set_error("null tensor argument");
+        return PE_ERR_ARG;
+    }
+    if (max_pages < 1 || num_pages < 1) { set_error("max_pages and num_pages must be >= 1"); return PE_ERR_ARG; }
+    return PE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pe_draft(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, const void* target_hidden,
+             const int32_t* positions, const int32_t* seq_lens, const int32_t* page_table, int32_t max_pages,
+             int32_t num_pages, void* k_cache, void* v_cache, int32_t* drafts, float* logits_dbg, int32_t* status,
+             void* stream) {
+    int rc = check_draft_args(h, B, K, last_token, target_hidden, positions, seq_lens, page_table, max_pages,
+                              num_pages, k_cache, v_cache, drafts, status);
+    if (rc != PE_OK) return rc;
+    PassSpec ps;
+    ps.B = B; ps.Kp = K; ps.j0 = 0; ps.k_check = K; ps.run_fc = true;
+    ps.tok = last_token; ps.tok_stride = 1;
+    ps.drafts = drafts; ps.drafts_stride = K;
+    ps.logits = logits_dbg; ps.logits_ld = h->cfg.vocab;
+    int launches = 0;
+    rc = enqueue_pass(h, ps, target_hidden, positions, seq_lens, page_table, max_pages, num_pages, k_cache, v_cache,
+                      status, static_cast<cudaStream_t>(stream), launches);
+    if (rc != PE_OK) return rc;
+    h->last_launches = launches;
+    return PE_OK;
+}
+
+int pe_draft_sequential(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, const void* target_hidden,
+                        const int32_t* positions, const int32_t* seq_lens, const int32_t* page_table,
+                        int32_t max_pages, int32_t num_pages, void* k_cache, void* v_cache, int32_t* drafts,
+                        float* logits_dbg, int32_t* status, void* stream) {
+    int rc = check_draft_args(h, B, K, last_token, target_hidden, positions, seq_lens, page_table, max_pages,
+                              num_pages, k_cache, v_cache, drafts, status);
+    if (rc != PE_OK) return rc;
+    const int H = h->cfg.hidden, V = h->cfg.vocab;
+    int launches = 0;
+    for (int j = 0; j < K; ++j) {
+        PassSpec ps;
+        ps.B = B; ps.Kp = 1; ps.j0 = j; ps.k_check = K;
+        ps.run_fc = j == 0;
+        // pass 0: the last accepted token and the fused target hidden state;
+        // pass j: draft j-1 and the drafter's own final residual of pass j-1
+        ps.tok = j == 0 ? last_token : drafts + (j - 1);
+        ps.tok_stride = j == 0 ? 1 : K;
+        ps.hid = j == 0 ? nullptr : h->resid;
+        ps.hid_stride = H;
+        ps.status_in = j > 0;
+        ps.seq_eff_out = true;
+        ps.drafts = drafts + j; ps.drafts_stride = K;
+        ps.logits = logits_dbg != nullptr ? logits_dbg + static_cast<size_t>(j) * V : nullptr;
+        ps.logits_ld = K * V;
+        rc = enqueue_pass(h, ps, target_hidden, positions, seq_lens, page_table, max_pages, num_pages, k_cache,
+                          v_cache, status, static_cast<cudaStream_t>(stream), launches);
+        if (rc != PE_OK) return rc;
+    }
     h->last_launches = launches;
     return PE_OK;
 }
@@ -828,14 +920,18 @@ struct pe_step_graph {
     int launches = 0;
 };
 
-int pe_step_graph_create(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, const void* target_hidden,
-                         const int32_t* positions, const int32_t* seq_lens, const int32_t* page_table,
-                         int32_t max_pages, int32_t num_pages, void* k_cache, void* v_cache, int32_t* drafts,
-                         int32_t* draft_status, const int32_t* target_tokens, int32_t* positions_out,
-                         int32_t* seq_lens_out, int32_t* accepted, int32_t* bonus, int32_t* emitted,
-                         int32_t* slot_mapping, int32_t* rollback_slots, int32_t* verify_status,
-                         pe_step_graph** out) {
+int pe_step_graph_create_ex(pe_handle* h, int32_t draft_mode, int32_t B, int32_t K, const int32_t* last_token,
+                            const void* target_hidden, const int32_t* positions, const int32_t* seq_lens,
+                            const int32_t* page_table, int32_t max_pages, int32_t num_pages, void* k_cache,
+                            void* v_cache, int32_t* drafts, int32_t* draft_status, const int32_t* target_tokens,
+                            int32_t* positions_out, int32_t* seq_lens_out, int32_t* accepted, int32_t* bonus,
+                            int32_t* emitted, int32_t* slot_mapping, int32_t* rollback_slots,
+                            int32_t* verify_status, pe_step_graph** out) {
     if (h == nullptr || out == nullptr) { set_error("null argument"); return PE_ERR_ARG; }
+    if (draft_mode != PE_DRAFT_PARALLEL && draft_mode != PE_DRAFT_SEQUENTIAL) {
+        set_error("unknown draft mode");
+        return PE_ERR_ARG;
+    }
     *out = nullptr;
     PE_CUDA_TRY(cudaSetDevice(h->device));
     cudaStream_t cs = nullptr;
@@ -844,9 +940,11 @@ int pe_step_graph_create(pe_handle* h, int32_t B, int32_t K, const int32_t* last
     h->prof_kind = -1;   // no profiling events inside a graph
     cudaError_t ce = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
     int rc = ce == cudaSuccess ? PE_OK : PE_ERR_CUDA;
-    if (rc == PE_OK)
-        rc = pe_draft(h, B, K, last_token, target_hidden, positions, seq_lens, page_table, max_pages, num_pages,
-                      k_cache, v_cache, drafts, nullptr, draft_status, cs);
+    if (rc == PE_OK) {
+        auto draft = draft_mode == PE_DRAFT_PARALLEL ? pe_draft : pe_draft_sequential;
+        rc = draft(h, B, K, last_token, target_hidden, positions, seq_lens, page_table, max_pages, num_pages,
+                   k_cache, v_cache, drafts, nullptr, draft_status, cs);
+    }
     const int n_draft = h->last_launches;
     if (rc == PE_OK)
         rc = pe_verify_rebuild(h, B, K, drafts, target_tokens, page_table, max_pages, num_pages, positions, seq_lens,
@@ -874,6 +972,19 @@ int pe_step_graph_create(pe_handle* h, int32_t B, int32_t K, const int32_t* last
     g->launches = n_draft + 1;
     *out = g;
     return PE_OK;
+}
+
+int pe_step_graph_create(pe_handle* h, int32_t B, int32_t K, const int32_t* last_token, const void* target_hidden,
+                         const int32_t* positions, const int32_t* seq_lens, const int32_t* page_table,
+                         int32_t max_pages, int32_t num_pages, void* k_cache, void* v_cache, int32_t* drafts,
+                         int32_t* draft_status, const int32_t* target_tokens, int32_t* positions_out,
+                         int32_t* seq_lens_out, int32_t* accepted, int32_t* bonus, int32_t* emitted,
+                         int32_t* slot_mapping, int32_t* rollback_slots, int32_t* verify_status,
+                         pe_step_graph** out) {
+    return pe_step_graph_create_ex(h, PE_DRAFT_PARALLEL, B, K, last_token, target_hidden, positions, seq_lens,
+                                   page_table, max_pages, num_pages, k_cache, v_cache, drafts, draft_status,
+                                   target_tokens, positions_out, seq_lens_out, accepted, bonus, emitted, slot_mapping,
+                                   rollback_slots, verify_status, out);
 }
 
 int pe_step_graph_launch(pe_step_graph* g, void* stream) {

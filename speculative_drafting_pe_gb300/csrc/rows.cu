@@ -56,14 +56,16 @@ __device__ __forceinline__ float4 scale4(float4 a, float s, float4 g) {
 
 constexpr int kMaxG = 8;   // 4-element groups per thread: H <= 4 * 8 * 256
 
-// Status of request b: inputs, capacity, page indices of entries 0..S+K-1.
+// Status of request b: inputs, capacity, page indices of entries
+// 0..S+k_check-1 (every entry the step writes).
 __device__ int request_status(const RowBuildParams& p, int b) {
     const int S = p.seq_lens[b];
-    const int tok = p.last_token[b];
+    const int tok = p.last_token[static_cast<size_t>(b) * p.tok_stride];
     const int Q = p.positions[b];
     if (S < 0 || Q < 0 || tok < 0 || tok >= p.V) return PE_REQ_BAD_INPUT;
-    if (static_cast<long long>(S) + p.K > static_cast<long long>(p.max_pages) * p.page_size) return PE_REQ_CAPACITY;
-    const int n_pages = (S + p.K + p.page_size - 1) / p.page_size;
+    if (static_cast<long long>(S) + p.k_check > static_cast<long long>(p.max_pages) * p.page_size)
+        return PE_REQ_CAPACITY;
+    const int n_pages = (S + p.k_check + p.page_size - 1) / p.page_size;
     int bad = 0;
     for (int i = threadIdx.x; i < n_pages; i += blockDim.x) {
         const int pg = p.page_table[static_cast<size_t>(b) * p.max_pages + i];
@@ -98,13 +100,15 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
     }
     pdl_launch_dependents();
     pdl_wait();
-    const int st = request_status(p, b);
+    const int st = p.status_in ? p.status[b] : request_status(p, b);
     const bool ok = st == PE_REQ_OK;
-    if (j == 0 && tid == 0) p.status[b] = st;
+    if (j == 0 && tid == 0 && !p.status_in) p.status[b] = st;
+    if (j == 0 && tid == 0 && p.seq_eff != nullptr) p.seq_eff[b] = p.seq_lens[b] + p.j0;
     if (tid == 0) p.amax[r] = 0ull;
     if (r == 0 && p.order != nullptr) {
         // requests by decreasing length (ties by index, so a permutation):
         // the attention issues its longest (request, kv head) CTAs first
+        // (every pass of a step adds the same j0, so S_b orders them)
         for (int q = tid; q < p.B; q += blockDim.x) {
             const int sq = p.seq_lens[q];
             int rank = 0;
@@ -127,8 +131,8 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
         __syncthreads();
         const long long cap = static_cast<long long>(p.max_pages) * p.page_size;
         for (int q = tid; q < p.B; q += blockDim.x) {
-            const int sq = p.seq_lens[q];
-            const bool fits = sq >= 0 && static_cast<long long>(sq) + p.K <= cap;
+            const int sq = p.seq_lens[q] + p.j0;
+            const bool fits = sq >= p.j0 && static_cast<long long>(sq) + p.K <= cap;
             const int tiles = fits ? (sq + p.K + kPieceTile - 1) / kPieceTile : 0;
             s_t[q] = tiles;
             atomicAdd(&s_total, tiles);
@@ -181,7 +185,7 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
             const int t = s_t[q];
             const int n = pieces_of(t);
             const int per_piece = s_sz[q];
-            const int len = t > 0 ? p.seq_lens[q] + p.K : 0;
+            const int len = t > 0 ? p.seq_lens[q] + p.j0 + p.K : 0;
             p.attn_plan[1 + q] = n;
             p.attn_plan[1 + p.B + q] = s_off[k];
             for (int i = 0; i < n; ++i) {
@@ -195,8 +199,9 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
         }
     }
     if (j == 0) {
-        const T* emb = static_cast<const T*>(p.embed) + static_cast<size_t>(ok ? p.last_token[b] : 0) * H;
-        const float* h0 = p.h + static_cast<size_t>(b) * H;
+        const T* emb = static_cast<const T*>(p.embed) +
+                       static_cast<size_t>(ok ? p.last_token[static_cast<size_t>(b) * p.tok_stride] : 0) * H;
+        const float* h0 = p.h + static_cast<size_t>(b) * p.hid_stride;
 #pragma unroll
         for (int i = 0; i < kMaxG; ++i) {
             const int g = tid + i * kRowThreads;
@@ -232,7 +237,7 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
     if (tid == 0) {
         int slot = -1;
         if (ok) {
-            const int e = p.seq_lens[b] + j;
+            const int e = p.seq_lens[b] + p.j0 + j;
             const int pg = p.page_table[static_cast<size_t>(b) * p.max_pages + e / p.page_size];
             slot = pg * p.page_size + e % p.page_size;
         }
@@ -241,7 +246,7 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
     // RoPE table for this row: angle = (Q_b + j) * inv_freq_i in double,
     // reduced to [-pi, pi] in double, then sin/cos in float.
     const int half = p.hd / 2;
-    const double pos = static_cast<double>(ok ? p.positions[b] + j : 0);
+    const double pos = static_cast<double>(ok ? p.positions[b] + p.j0 + j : 0);
     for (int i = tid; i < half; i += blockDim.x) {
         const double a = pos * p.inv_freq[i];
         const double two_pi = 6.283185307179586476925286766559;
@@ -268,14 +273,15 @@ __global__ void k_logits_rms_scale(float* __restrict__ logits, int V, int ld, co
 }
 
 __global__ void k_argmax_finalize(const unsigned long long* __restrict__ amax, const int32_t* __restrict__ status,
-                                  int B, int K, int32_t* __restrict__ drafts) {
+                                  int B, int K, int32_t* __restrict__ drafts, int out_stride) {
     pdl_launch_dependents();
     pdl_wait();
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= B * K) return;
     const int b = r / K;
     const unsigned long long key = amax[r];
-    drafts[r] = (status[b] == PE_REQ_OK && key != 0ull) ? static_cast<int32_t>(argmax_key_index(key)) : -1;
+    drafts[static_cast<size_t>(b) * out_stride + (r - b * K)] =
+        (status[b] == PE_REQ_OK && key != 0ull) ? static_cast<int32_t>(argmax_key_index(key)) : -1;
 }
 
 }  // namespace
@@ -295,9 +301,10 @@ int launch_logits_rms_scale(float* logits, int rows, int V, int ld, const float*
 }
 
 int launch_argmax_finalize(const unsigned long long* amax, const int32_t* status, int B, int K, int32_t* drafts,
-                           cudaStream_t s, bool pdl) {
+                           int out_stride, cudaStream_t s, bool pdl) {
     const int R = B * K;
-    PE_CUDA_TRY(launch_ex(k_argmax_finalize, dim3((R + 127) / 128), dim3(128), 0, s, pdl, amax, status, B, K, drafts));
+    PE_CUDA_TRY(launch_ex(k_argmax_finalize, dim3((R + 127) / 128), dim3(128), 0, s, pdl, amax, status, B, K, drafts,
+                          out_stride));
     return PE_OK;
 }
 
