@@ -235,6 +235,50 @@ def make_verify_inputs(B, K, vocab, seq_range, alpha, seed, page_size=16):
                 page_table=page_table, num_pages=num_pages)
 
 
+FP8_LAYER_MATRICES = ("w_qkv", "w_o", "w_gate", "w_up", "w_down")
+
+
+def quantize_weights_fp8(W):
+    """FP8 drafter weights from a random-init weight dict: every GEMM matrix
+    (FC, QKV, O, gate, up, down, LM head) becomes E4M3 codes (uint8, same
+    [out, in] layout, torch's round-to-nearest-even float8_e4m3fn conversion)
+    with one float32 scale per output row, max|row| / 448; the other entries
+    are kept. Returns (Wq, scales) with the same nesting as W."""
+    def q(t):
+        t32 = t.to(torch.float32)
+        s = t32.abs().amax(dim=1).clamp_min(1e-30) / 448.0
+        codes = (t32 / s[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+        return codes.contiguous(), s.contiguous()
+
+    Wq = {k: v for k, v in W.items() if k != "layers"}
+    scales = {"layers": []}
+    for k in ("fc", "lm_head"):
+        Wq[k], scales[k] = q(W[k])
+    Wq["layers"] = []
+    for L in W["layers"]:
+        Lq, Ls = dict(L), {}
+        for k in FP8_LAYER_MATRICES:
+            Lq[k], Ls[k] = q(L[k])
+        Wq["layers"].append(Lq)
+        scales["layers"].append(Ls)
+    return Wq, scales
+
+
+def fp8_to_numpy(Wq, scales):
+    """Host copies for the oracle: uint8 codes and float32 scales as numpy,
+    other tensors as float32 (exact for bf16)."""
+    def cv(t):
+        if t is None:
+            return None
+        t = t.detach().to("cpu")
+        return t.numpy() if t.dtype == torch.uint8 else t.to(torch.float32).numpy()
+    Wn = {k: cv(v) for k, v in Wq.items() if k != "layers"}
+    Wn["layers"] = [{k: cv(v) for k, v in L.items()} for L in Wq["layers"]]
+    Sn = {k: cv(v) for k, v in scales.items() if k != "layers"}
+    Sn["layers"] = [{k: cv(v) for k, v in L.items()} for L in scales["layers"]]
+    return Wn, Sn
+
+
 def weights_to_numpy(W):
     """Host float32 copies of a weight dict for the oracle (exact for bf16 and
     fp32 values; the oracle widens to float64 as it computes)."""

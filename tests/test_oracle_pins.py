@@ -459,6 +459,71 @@ def test_sequential_cache_rows_are_the_passes_own_rows():
     np.testing.assert_allclose(out["v_new"][:, :, 0], par["v_new"][:, :, 0], rtol=1e-12, atol=1e-12)
 
 
+# --------------------------------------------------------------- FP8 weights
+
+def test_e4m3_decode_matches_torch_float8_on_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_decode(codes)
+    nan = np.isnan(ref)
+    np.testing.assert_array_equal(np.isnan(got), nan)
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+    assert nan.sum() == 2                                    # 0x7F and 0xFF
+
+
+def test_e4m3_decode_special_values():
+    d = oracle.e4m3_decode(np.array([0x00, 0x80, 0x01, 0x07, 0x08, 0x38, 0x7E, 0xFE, 0x7F], dtype=np.uint8))
+    np.testing.assert_array_equal(d[:8], [0.0, -0.0, 2.0 ** -9, 7 * 2.0 ** -9, 2.0 ** -6, 1.0, 448.0, -448.0])
+    assert np.signbit(d[1]) and np.isnan(d[8])
+    assert oracle.E4M3_MAX == 448.0
+
+
+def test_dequant_rows_scales_each_output_row():
+    rng = np.random.default_rng(12)
+    q = rng.integers(0, 256, size=(5, 9), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x3C                             # no NaN codes
+    sc = rng.uniform(0.001, 2.0, size=5)
+    ref = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy() * sc[:, None]
+    np.testing.assert_array_equal(oracle.dequant_rows(q, sc), ref)
+
+
+def test_fp8_weight_recipe_round_trips_within_e4m3_precision():
+    # the synthetic FP8 weights decode to within half an E4M3 step of the
+    # bf16 weights they were made from, and each row's largest magnitude maps
+    # to 448 exactly
+    W = synth.make_weights(TINY, 3)
+    Wq, sc = synth.quantize_weights_fp8(W)
+    Wn, Sn = synth.fp8_to_numpy(Wq, sc)
+    Wd = oracle.dequant_weights(Wn, Sn)
+    for name, w0, wd, s in [("fc", W["fc"], Wd["fc"], Sn["fc"]),
+                            ("w_down", W["layers"][2]["w_down"], Wd["layers"][2]["w_down"],
+                             Sn["layers"][2]["w_down"])]:
+        w0 = w0.double().numpy()
+        rel = np.abs(wd - w0) / np.maximum(np.abs(w0), 2.0 ** -6 * s[:, None])
+        assert rel.max() <= 2.0 ** -4 + 1e-12, name
+        np.testing.assert_allclose(np.abs(wd).max(axis=1), np.abs(w0).max(axis=1), rtol=1e-6)
+    assert Wq["embed"] is W["embed"] and Wq["layers"][0]["norm_e"] is W["layers"][0]["norm_e"]
+
+
+def test_fp8_draft_pass_is_the_draft_pass_on_dequantised_weights():
+    # the oracle's FP8 drafter is its ordinary drafter on W = decode(q) * s;
+    # the K=1 torch restatement confirms it on those weights
+    W, inp = _tiny_case(K=3)
+    Wq, sc = synth.quantize_weights_fp8(W)
+    Wn, Sn = synth.fp8_to_numpy(Wq, sc)
+    Wd = oracle.dequant_weights(Wn, Sn)
+    out = oracle.draft_pass(TINY, Wd, inp.last_token.numpy(), inp.target_hidden.double().numpy(),
+                            inp.positions.numpy(), inp.seq_lens.numpy(), inp.page_table.numpy(),
+                            inp.k_cache.double().numpy(), inp.v_cache.double().numpy(), 3)
+    Wt = {k: (torch.from_numpy(np.asarray(v)) if v is not None and k != "layers" else v) for k, v in Wd.items()}
+    Wt["layers"] = [{k: (torch.from_numpy(np.asarray(v)) if v is not None else None) for k, v in L.items()}
+                    for L in Wd["layers"]]
+    ref = _torch_reference_pass(Wt, inp, 3)
+    np.testing.assert_allclose(out["logits"], ref, rtol=1e-10, atol=1e-10)
+    base = _run_oracle(W, inp, 3)
+    assert np.abs(out["logits"] - base["logits"]).max() > 1e-6    # quantisation moved the logits
+
+
 # --------------------------------------------------------------- verify / rebuild
 
 def _brute_accept(d, g):
