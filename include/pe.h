@@ -58,6 +58,9 @@ extern "C" {
 
 #define PE_DTYPE_BF16 0         /* bf16 weights/activations/KV, fp32 accumulate */
 #define PE_DTYPE_FP32 1         /* fp32 everything; GEMMs run as tf32 */
+#define PE_DTYPE_FP8W 2         /* FP8 (E4M3) GEMM weights with one fp32 scale per output row;
+                                   bf16 activations, embeddings, norm gains and KV cache
+                                   (pe_init_drafter_fp8) */
 
 /* Drafter shape. n_layers must be 4, page_size 16, head_dim 64 or 128,
  * n_kv_heads must divide n_q_heads, n_q_heads*head_dim and
@@ -101,6 +104,28 @@ typedef struct pe_weights {
     pe_layer_weights layer[4];
 } pe_weights;
 
+/* FP8 drafter weights. The pages run their benchmarks in FP8 ("在 Amazon
+ * SageMaker AI 上使用 P-EAGLE 并行化推测解码", section "基准测试"); here every
+ * GEMM weight matrix (FC, QKV, O, gate, up, down, LM head) may be given as
+ * E4M3 codes q[m, k] (uint8, the same [out, in] layout, rows a multiple of 16
+ * bytes) standing for W[m, k] = q[m, k] * scale[m]. The codes are widened to
+ * bf16 in shared memory (exactly: every E4M3 value is a bf16 value), the
+ * tensor cores multiply bf16 by bf16 with fp32 accumulation, and the epilogue
+ * applies scale[m]. Each array below is fp32 [rows of that matrix]. */
+typedef struct pe_layer_scales {
+    const float* w_qkv;     /* [(nq+2nkv)*hd] */
+    const float* w_o;       /* [H] */
+    const float* w_gate;    /* [F] */
+    const float* w_up;      /* [F] */
+    const float* w_down;    /* [H] */
+} pe_layer_scales;
+
+typedef struct pe_weight_scales {
+    const float* fc;        /* [H] */
+    const float* lm_head;   /* [V] */
+    pe_layer_scales layer[4];
+} pe_weight_scales;
+
 typedef struct pe_handle pe_handle;
 
 /* Create a drafter on `device` (the device must be current or will be made
@@ -109,6 +134,15 @@ typedef struct pe_handle pe_handle;
  * cfg->k_max rows and builds TMA descriptors for the weights. Synchronous. */
 int pe_init_drafter(const pe_config* cfg, const pe_weights* weights,
                     int32_t max_batch, int32_t device, pe_handle** out);
+
+/* The same for FP8 weights: cfg->dtype must be PE_DTYPE_FP8W; the GEMM
+ * matrices of `weights` point at E4M3 codes, the other entries (embed,
+ * emb_mask, h_shared, norm gains) at bf16; `scales` gives the per-row scales
+ * (device fp32, caller-owned like the weights). Every other entry point works
+ * unchanged on the handle, with bf16 target hidden states and KV cache. The
+ * persistent layer chain (PE_LAYER_CHAIN) is not used with FP8 weights. */
+int pe_init_drafter_fp8(const pe_config* cfg, const pe_weights* weights, const pe_weight_scales* scales,
+                        int32_t max_batch, int32_t device, pe_handle** out);
 
 /* One parallel draft pass (pages' Step 2) for B requests, K drafts each.
  *
@@ -195,6 +229,12 @@ int pe_verify_rebuild(pe_handle* h, int32_t B, int32_t K,
 int pe_linear_scratch(int32_t dtype, int32_t M, int32_t N, int32_t Kd, int64_t* ws_floats, int32_t* n_tickets);
 int pe_linear(int32_t dtype, int32_t M, int32_t N, int32_t Kd, const void* w, const void* x, float* y,
               float* ws, int32_t* tickets, void* stream);
+/* The FP8-weight GEMM engine on its own: y[n, m] = scale[m] * sum_k q[m, k] * x[n, k]
+ *  w  [M, Kd] E4M3 codes (uint8), w_scale [M] fp32, x [N, Kd] bf16, y [N, M]
+ *  fp32 OUT; Kd a multiple of 16, w and x 16-byte aligned. ws / tickets as
+ *  for pe_linear, sized by pe_linear_scratch(PE_DTYPE_FP8W, ...). */
+int pe_linear_fp8(int32_t M, int32_t N, int32_t Kd, const void* w, const float* w_scale, const void* x, float* y,
+                  float* ws, int32_t* tickets, void* stream);
 
 /* pe_linear for callers that cannot allocate device memory (this entry point
  * has no counterpart in the paper). Some callers may not call cudaMalloc

@@ -15,7 +15,7 @@ from . import build as _build
 
 PE_OK = 0
 PE_REQ_OK, PE_REQ_CAPACITY, PE_REQ_BAD_PAGE, PE_REQ_BAD_INPUT = 0, 1, 2, 3
-PE_DTYPE_BF16, PE_DTYPE_FP32 = 0, 1
+PE_DTYPE_BF16, PE_DTYPE_FP32, PE_DTYPE_FP8W = 0, 1, 2
 PE_DEVERR_GEMM_TIMEOUT, PE_DEVERR_ATTN_TIMEOUT, PE_DEVERR_CHAIN_TIMEOUT = 1, 2, 4
 PE_DRAFT_PARALLEL, PE_DRAFT_SEQUENTIAL = 0, 1
 
@@ -25,6 +25,7 @@ EXPORTS = (
     "pe_profile_start", "pe_profile_stop", "pe_kernel_name",
     "pe_step_graph_create", "pe_step_graph_launch", "pe_step_graph_launch_count", "pe_step_graph_destroy",
     "pe_linear_noalloc", "pe_test_stall_chain", "pe_draft_sequential", "pe_step_graph_create_ex",
+    "pe_init_drafter_fp8", "pe_linear_fp8",
 )
 KERNEL_KINDS = ("fc", "row_build", "rmsnorm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "argmax",
                 "layer_chain")
@@ -51,6 +52,17 @@ _TOP_FIELDS = ("fc", "embed", "emb_mask", "h_shared", "final_norm", "lm_head")
 
 class PeWeights(ctypes.Structure):
     _fields_ = [(n, _vp) for n in _TOP_FIELDS] + [("layer", PeLayerWeights * 4)]
+
+
+_LAYER_SCALE_FIELDS = ("w_qkv", "w_o", "w_gate", "w_up", "w_down")
+
+
+class PeLayerScales(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in _LAYER_SCALE_FIELDS]
+
+
+class PeWeightScales(ctypes.Structure):
+    _fields_ = [("fc", _vp), ("lm_head", _vp), ("layer", PeLayerScales * 4)]
 
 
 class PeError(RuntimeError):
@@ -80,6 +92,11 @@ def load():
     lib.pe_init_drafter.argtypes = [ctypes.POINTER(PeConfig), ctypes.POINTER(PeWeights), _i32, _i32,
                                     ctypes.POINTER(_vp)]
     lib.pe_init_drafter.restype = ctypes.c_int
+    lib.pe_init_drafter_fp8.argtypes = [ctypes.POINTER(PeConfig), ctypes.POINTER(PeWeights),
+                                        ctypes.POINTER(PeWeightScales), _i32, _i32, ctypes.POINTER(_vp)]
+    lib.pe_init_drafter_fp8.restype = ctypes.c_int
+    lib.pe_linear_fp8.argtypes = [_i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.pe_linear_fp8.restype = ctypes.c_int
     lib.pe_draft.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.pe_draft.restype = ctypes.c_int
     lib.pe_draft_sequential.argtypes = lib.pe_draft.argtypes
@@ -154,7 +171,10 @@ class Drafter:
     device; the Drafter keeps references so they outlive the handle.
     """
 
-    def __init__(self, shape, weights, max_batch, k_max, device=None):
+    def __init__(self, shape, weights, max_batch, k_max, device=None, fp8_scales=None):
+        """fp8_scales: per-row fp32 scales ({"fc", "lm_head", "layers": [...]})
+        when the GEMM matrices of `weights` are E4M3 codes (uint8, as made by
+        ``synth.quantize_weights_fp8``); the drafter then runs bf16 otherwise."""
         lib = load()
         self.shape = shape
         self.dtype = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
@@ -162,24 +182,42 @@ class Drafter:
         self.k_max = k_max
         self.max_batch = max_batch
         self._weights = weights
+        self._scales = fp8_scales
+        fp8 = fp8_scales is not None
+        if fp8 and self.dtype != torch.bfloat16:
+            raise ValueError("FP8 weights go with a bf16 drafter shape")
         cfg = PeConfig(shape.hidden, 4, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn,
                        shape.vocab, shape.rms_eps, shape.rope_theta, shape.page_size, k_max,
-                       PE_DTYPE_BF16 if shape.dtype == "bf16" else PE_DTYPE_FP32)
+                       PE_DTYPE_FP8W if fp8 else (PE_DTYPE_BF16 if shape.dtype == "bf16" else PE_DTYPE_FP32))
+        gemm = {"fc", "lm_head", "w_qkv", "w_o", "w_gate", "w_up", "w_down"}
         w = PeWeights()
         for n in _TOP_FIELDS:
             t = weights[n]
-            _need(t, self.dtype, self.device, n)
+            _need(t, torch.uint8 if fp8 and n in gemm else self.dtype, self.device, n)
             setattr(w, n, t.data_ptr())
         for li, L in enumerate(weights["layers"]):
             for n in _LAYER_FIELDS:
                 t = L.get(n)
                 if t is not None:
-                    _need(t, self.dtype, self.device, f"layers[{li}].{n}")
+                    _need(t, torch.uint8 if fp8 and n in gemm else self.dtype, self.device, f"layers[{li}].{n}")
                     setattr(w.layer[li], n, t.data_ptr())
         self._cfg, self._w = cfg, w
         h = _vp()
-        _check(lib.pe_init_drafter(ctypes.byref(cfg), ctypes.byref(w), max_batch, self.device.index or 0,
-                                   ctypes.byref(h)))
+        if fp8:
+            sc = PeWeightScales()
+            for n in ("fc", "lm_head"):
+                _need(fp8_scales[n], torch.float32, self.device, f"scales.{n}")
+                setattr(sc, n, fp8_scales[n].data_ptr())
+            for li, L in enumerate(fp8_scales["layers"]):
+                for n in _LAYER_SCALE_FIELDS:
+                    _need(L[n], torch.float32, self.device, f"scales.layers[{li}].{n}")
+                    setattr(sc.layer[li], n, L[n].data_ptr())
+            self._sc = sc
+            _check(lib.pe_init_drafter_fp8(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(sc), max_batch,
+                                           self.device.index or 0, ctypes.byref(h)))
+        else:
+            _check(lib.pe_init_drafter(ctypes.byref(cfg), ctypes.byref(w), max_batch, self.device.index or 0,
+                                       ctypes.byref(h)))
         self._h = h
 
     def draft(self, last_token, target_hidden, positions, seq_lens, page_table, num_pages, k_cache, v_cache,
@@ -312,6 +350,25 @@ def linear(w, x, stream=None):
     tickets = torch.zeros(max(nt.value, 1), dtype=torch.int32, device=w.device)
     y = torch.empty(N, M, dtype=torch.float32, device=w.device)
     _check(lib.pe_linear(dtype, M, N, Kd, _p(w), _p(x), _p(y), _p(ws), _p(tickets), _stream_ptr(stream)))
+    return y
+
+
+def linear_fp8(w_codes, w_scale, x, stream=None):
+    """y = x @ (decode(w_codes) * w_scale[:, None]).T in fp32: E4M3 weight
+    codes (uint8 [M, Kd]), fp32 row scales [M], bf16 x [N, Kd]."""
+    lib = load()
+    M, Kd = w_codes.shape
+    N = x.shape[0]
+    _need(w_codes, torch.uint8, x.device, "w_codes")
+    _need(w_scale, torch.float32, x.device, "w_scale")
+    _need(x, torch.bfloat16, x.device, "x")
+    wsf, nt = ctypes.c_int64(0), _i32(0)
+    _check(lib.pe_linear_scratch(PE_DTYPE_FP8W, M, N, Kd, ctypes.byref(wsf), ctypes.byref(nt)))
+    ws = torch.empty(max(wsf.value, 1), dtype=torch.float32, device=x.device)
+    tickets = torch.zeros(max(nt.value, 1), dtype=torch.int32, device=x.device)
+    y = torch.empty(N, M, dtype=torch.float32, device=x.device)
+    _check(lib.pe_linear_fp8(M, N, Kd, _p(w_codes), _p(w_scale), _p(x), _p(y), _p(ws), _p(tickets),
+                             _stream_ptr(stream)))
     return y
 
 

@@ -16,17 +16,25 @@
 // split to arrive at the tile's ticket sums the partials in split order
 // (0, 1, ..., S-1), so the result does not depend on arrival order, then
 // applies the epilogue and resets the ticket for the next launch.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "gemm_epi.cuh"
 
 namespace pe {
 namespace {
 
 constexpr int kThreads = 192;
+constexpr int kThreadsW8 = 320;              // + warps 6..9: FP8 -> bf16 weight converters
 constexpr int kMaxClusterSplits = 8;         // cluster split-K: at most 8 CTAs per tile
+constexpr int kConvStages = 2;               // bf16 copies of FP8 weight stages (W8)
+constexpr uint32_t kConvBytes = 2 * kABytes; // 128 rows x 128 k as two 64-k SW128 tiles
 
-__host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn, int inv_floats) {
-    size_t off = static_cast<size_t>(stages) * (kABytes + static_cast<size_t>(bn) * kRowBytes);
-    off += static_cast<size_t>(2 * stages + 4) * 8;   // mbarriers
+__host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn, int inv_floats, bool w8) {
+    const size_t b_stage = static_cast<size_t>(bn) * kRowBytes * (w8 ? 2 : 1);
+    size_t off = static_cast<size_t>(stages) * (kABytes + b_stage);
+    if (w8) off += static_cast<size_t>(kConvStages) * kConvBytes;
+    off += static_cast<size_t>(2 * stages + 4 + 2 * kConvStages) * 8;   // mbarriers
     off += 16;                                        // TMEM base + flags
     off = (off + 15) & ~static_cast<size_t>(15);
     off += static_cast<size_t>(kChunk) * kPitch * 4;  // epilogue staging tile
@@ -34,10 +42,63 @@ __host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn, int inv_fl
     return off + 1024;                                // base alignment slack
 }
 
-template <typename T, int EPI>
+// FP8 weights: the scale of this thread's accumulator row (TMEM lane ml of
+// weight tile m_tile).
+template <int EPI>
+__device__ __forceinline__ float w8_row_scale(const GemmParams& p, int m_tile, int ml) {
+    if constexpr (EPI == EPI_SWIGLU) {
+        const int f = m_tile * 64 + (ml & 63);
+        if (f >= p.M) return 0.f;
+        return ml < 64 ? p.w_scale[f] : p.w_scale2[f];
+    } else {
+        const int m = m_tile * kBM + ml;
+        return m < p.M ? p.w_scale[m] : 0.f;
+    }
+}
+
+template <bool W8>
+__device__ __forceinline__ void scale_row(float (&v)[kChunk], float s) {
+    if constexpr (W8) {
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) v[i] *= s;
+    }
+}
+
+// One FP8 weight stage (128 rows x 128 E4M3 codes, 128-byte swizzle) widened
+// to bf16 as two 64-k tiles in the same swizzle: the 16-byte chunk c of row r
+// sits at r*128 + ((c ^ (r & 7)) << 4) in every tile. Thread t (0..127) owns
+// row t. E4M3 -> bf16 is exact (every E4M3 value is a bf16 value).
+__device__ __forceinline__ void widen_fp8_stage(const uint8_t* raw, uint8_t* conv, int t) {
+    const int r = t;
+    const int sw = r & 7;
+    const uint8_t* src = raw + r * kRowBytes;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xFFFFu);
+                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+                const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+                o[2 * i + h] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+        }
+        uint8_t* dst = conv + (c >> 2) * kABytes + r * kRowBytes;
+        const int j0 = 2 * (c & 3);
+        *reinterpret_cast<uint4*>(dst + ((j0 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(dst + (((j0 + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+template <typename T, int EPI, bool W8>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_acc, float* stile, int* sflag,
-                                              float* part, const float* inv, float xg_g, int m_tile, int n_tile,
-                                              int split, int warp, int lane) {
+                                              float* part, const float* inv, float xg_g, float wsc, int m_tile,
+                                              int n_tile, int split, int warp, int lane) {
     const int quad = warp & 3;               // TMEM lane quadrant this warp may read
     const int ml = quad * 32 + lane;         // tile row = TMEM lane
     const uint32_t t_row = t_acc + (static_cast<uint32_t>(quad * 32) << 16);
@@ -98,6 +159,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_ac
                     }
                 }
             }
+            scale_row<W8>(v, wsc);
             scale_cols(v, inv, c0, 1, kChunk);
             apply_chunk<T, EPI>(p, v, ml, m_tile, ColMap{n_base + c0, 1, kChunk, c0}, stile, xg_g);
         }
@@ -106,6 +168,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_ac
         for (int c0 = 0; c0 < bn; c0 += kChunk) {
             float v[kChunk];
             tmem_ld16(t_row + c0, v);
+            scale_row<W8>(v, wsc);
             scale_cols(v, inv, c0, 1, kChunk);
             apply_chunk<T, EPI>(p, v, ml, m_tile, ColMap{n_base + c0, 1, kChunk, c0}, stile, xg_g);
         }
@@ -117,10 +180,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_ac
 // columns c = rank + j * splits over all peers' partial tiles (read through
 // distributed shared memory, in split order) and applies the epilogue to
 // them, 16 of its own columns per chunk.
-template <typename T, int EPI>
+template <typename T, int EPI, bool W8>
 __device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile, const float* part,
-                                               const float* inv, float xg_g, int m_tile, int n_tile, int warp,
-                                               int lane) {
+                                               const float* inv, float xg_g, float wsc, int m_tile, int n_tile,
+                                               int warp, int lane) {
     const int ml = (warp & 3) * 32 + lane;
     const int bn = p.bn;
     const int C = p.splits;
@@ -155,6 +218,7 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile
                 }
             }
         }
+        scale_row<W8>(v, wsc);
         scale_cols(v, inv, c0, C, cnt);
         apply_chunk<T, EPI>(p, v, ml, m_tile, ColMap{n_tile * bn + c0, C, cnt, j0}, stile, xg_g);
     }
@@ -162,23 +226,33 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile
 }
 
 // ------------------------------------------------------------ kernel
+//
+// W8 (FP8 weights, bf16 activations): a stage holds 128 k of E4M3 weight
+// codes (one 16 KB TMA box) and the matching two 64-k bf16 token tiles; the
+// converter warps 6..9 widen the codes into one of two bf16 weight copies,
+// which the MMA reads as two K-major SW128 tiles (the tensor cores see a
+// bf16 x bf16 product: A and B of one kind::f16 MMA share a type).
 
-template <typename T, int EPI>
-__global__ void __launch_bounds__(kThreads, 2)
+template <typename T, int EPI, bool W8>
+__global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, W8 ? 1 : 2)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
            const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stages = p.stages;
     const int bn = p.bn;
-    const uint32_t b_bytes = static_cast<uint32_t>(bn) * kRowBytes;
+    const uint32_t b_box = static_cast<uint32_t>(bn) * kRowBytes;     // one 128-byte-wide token tile
+    const uint32_t b_bytes = W8 ? 2 * b_box : b_box;                  // token bytes per stage
     uint8_t* sA = smem;
     uint8_t* sB = smem + static_cast<size_t>(stages) * kABytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + static_cast<size_t>(stages) * b_bytes);
+    uint8_t* sC = sB + static_cast<size_t>(stages) * b_bytes;         // W8: bf16 weight copies
+    uint64_t* full = reinterpret_cast<uint64_t*>(sC + (W8 ? static_cast<size_t>(kConvStages) * kConvBytes : 0));
     uint64_t* empty = full + stages;
     uint64_t* tfull = empty + stages;      // [2] accumulator ready
     uint64_t* tempty = tfull + 2;          // [2] accumulator drained by the epilogue
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint64_t* cfull = tempty + 2;          // [kConvStages] W8: bf16 copy written
+    uint64_t* cempty = cfull + kConvStages;   // [kConvStages] W8: bf16 copy consumed by the MMA
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cempty + kConvStages);
     int* sflag = reinterpret_cast<int*>(tmem_slot + 1);
     float* stile = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(sflag + 3) + 15) & ~uintptr_t(15));
     float* s_inv = stile + kChunk * kPitch;   // [inv_slots(N)] in the QKV and gate/up GEMMs
@@ -200,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int nacc = p.persistent ? 2 : 1;           // double-buffered accumulator when persistent
     const bool inv_all = norm_scaled<EPI>(p) && p.N <= kMaxInvAll;
     float xg_g = 0.f;                                // folded RMSNorm gain of this epilogue thread's row
+    float wsc = 1.f;                                 // W8: scale of this epilogue thread's row
     const uint32_t acc_cols = tmem_cols_for(bn);
     const uint32_t tmem_cols = acc_cols * static_cast<uint32_t>(nacc);
 
@@ -215,6 +290,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], 128);
         }
+        if constexpr (W8) {
+            for (int c = 0; c < kConvStages; ++c) {
+                mbar_init(&cfull[c], 128);
+                mbar_init(&cempty[c], 1);
+            }
+        }
         sflag[0] = 0;
         sflag[1] = 0;
         fence_mbar_init();
@@ -229,16 +310,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t tmem_base = *tmem_slot;
 
     pdl_launch_dependents();
-    // Everything but the producer waits here for the previous kernel in the
-    // stream (a no-op without programmatic dependent launch).
-    if (warp != 0) pdl_wait();
+    // Everything but the producer and the converters waits here for the
+    // previous kernel in the stream (a no-op without programmatic dependent
+    // launch); the converters only touch weights.
+    if (warp != 0 && warp < 6) pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_keep = l2_policy_evict_last();   // weight tiles kept in L2 across steps
             const uint64_t pol_x = l2_policy_evict_last();
-            constexpr int kBK = kRowBytes / static_cast<int>(sizeof(T));
+            // k elements per stage: one 128-byte swizzle row of weights
+            constexpr int kBK = W8 ? kRowBytes : kRowBytes / static_cast<int>(sizeof(T));
             int s = 0;
             uint32_t ph = 0;
             bool first = true, ok = true;
@@ -256,8 +339,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 };
                 auto load_b = [&](int st, int kb) {
-                    tma_load_2d(sB + static_cast<size_t>(st) * b_bytes, &tmB, &full[st], kb * kBK, n_tile * bn,
-                                pol_x);
+                    uint8_t* b_dst = sB + static_cast<size_t>(st) * b_bytes;
+                    if constexpr (W8) {
+                        // the stage's 128 k as two 64-element bf16 token tiles
+                        tma_load_2d(b_dst, &tmB, &full[st], kb * kBK, n_tile * bn, pol_x);
+                        tma_load_2d(b_dst + b_box, &tmB, &full[st], kb * kBK + kBK / 2, n_tile * bn, pol_x);
+                    } else {
+                        tma_load_2d(b_dst, &tmB, &full[st], kb * kBK, n_tile * bn, pol_x);
+                    }
                 };
                 int kb = kb0;
                 if (first) {
@@ -298,6 +387,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint32_t idesc = umma_idesc(UmmaKind<T>::kFmt, kBM, bn);
             int s = 0;
             uint32_t ph = 0;
+            int c = 0;
+            uint32_t cph = 0;
             int it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
@@ -317,13 +408,38 @@ __global__ void __launch_bounds__(kThreads, 2)
                         ok = false;
                         break;
                     }
+                    if constexpr (W8) {
+                        if (!mbar_wait(&cfull[c], cph, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                     tc_fence_after_sync();
-                    const uint32_t a_addr = smem_u32(sA + static_cast<size_t>(s) * kABytes);
                     const uint32_t b_addr = smem_u32(sB + static_cast<size_t>(s) * b_bytes);
+                    if constexpr (W8) {
+                        const uint32_t a_addr = smem_u32(sC + static_cast<size_t>(c) * kConvBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kRowBytes / 32; ++kk) {
-                        UmmaKind<T>::mma(d_tmem, umma_desc_sw128(a_addr + kk * 32), umma_desc_sw128(b_addr + kk * 32),
-                                         idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                            for (int kk = 0; kk < kRowBytes / 32; ++kk) {
+                                UmmaKind<T>::mma(d_tmem, umma_desc_sw128(a_addr + half * kABytes + kk * 32),
+                                                 umma_desc_sw128(b_addr + half * b_box + kk * 32), idesc,
+                                                 (kb > kb0 || half > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        }
+                        umma_commit(&cempty[c]);
+                        if (++c == kConvStages) {
+                            c = 0;
+                            cph ^= 1u;
+                        }
+                    } else {
+                        const uint32_t a_addr = smem_u32(sA + static_cast<size_t>(s) * kABytes);
+#pragma unroll
+                        for (int kk = 0; kk < kRowBytes / 32; ++kk) {
+                            UmmaKind<T>::mma(d_tmem, umma_desc_sw128(a_addr + kk * 32),
+                                             umma_desc_sw128(b_addr + kk * 32), idesc,
+                                             (kb > kb0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     umma_commit(&empty[s]);
                     if (++s == stages) {
@@ -335,6 +451,41 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
         __syncwarp();
+    } else if (W8 && warp >= 6) {
+        // converters: widen each weight stage into the next bf16 copy, in the
+        // MMA's order; the MMA releases the raw stage, so the codes stay put
+        // until the copy is complete
+        if constexpr (W8) {
+            const int t = static_cast<int>(threadIdx.x) - 192;
+            int s = 0;
+            uint32_t ph = 0;
+            int c = 0;
+            uint32_t cph = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                int m_tile, n_tile, split, kb0, kb1;
+                decode(u, m_tile, n_tile, split, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&full[s], ph, p.err, PE_DEVERR_GEMM_TIMEOUT) ||
+                        !mbar_wait(&cempty[c], cph ^ 1u, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    widen_fp8_stage(sA + static_cast<size_t>(s) * kABytes, sC + static_cast<size_t>(c) * kConvBytes,
+                                    t);
+                    fence_proxy_async_smem();   // the MMA (async proxy) reads what these threads wrote
+                    mbar_arrive(&cfull[c]);
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    if (++c == kConvStages) {
+                        c = 0;
+                        cph ^= 1u;
+                    }
+                }
+            }
+        }
     } else {
         // Folded RMSNorm: the scales of every token row, computed once while
         // the first mainloop runs (published by the barrier after the first
@@ -364,13 +515,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int m = m_tile * kBM + (warp & 3) * 32 + lane;
                 xg_g = (p.xg != nullptr && m < p.M) ? Elem<T>::to_f(static_cast<const T*>(p.xg_gain)[m]) : 0.f;
             }
+            if constexpr (W8) wsc = w8_row_scale<EPI>(p, m_tile, (warp & 3) * 32 + lane);
             const bool ok = mbar_wait(&tfull[acc], static_cast<uint32_t>(use & 1), p.err, PE_DEVERR_GEMM_TIMEOUT);
             tc_fence_after_sync();
             if (!ok) sflag[0] = 1;
             named_bar_sync(1, 128);
             if (sflag[0]) break;
-            epilogue_tile<T, EPI>(p, tmem_base + static_cast<uint32_t>(acc) * acc_cols, stile, sflag,
-                                  reinterpret_cast<float*>(smem), inv, xg_g, m_tile, n_tile, split, warp, lane);
+            epilogue_tile<T, EPI, W8>(p, tmem_base + static_cast<uint32_t>(acc) * acc_cols, stile, sflag,
+                                      reinterpret_cast<float*>(smem), inv, xg_g, wsc, m_tile, n_tile, split, warp,
+                                      lane);
             tc_fence_before_sync();
             mbar_arrive(&tempty[acc]);
         }
@@ -381,10 +534,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         decode(blockIdx.x, m_tile, n_tile, split, kb0, kb1);
         __syncthreads();              // this CTA's partial is in shared memory
         cluster_sync_all();           // ... and so are the peers'
-        if (warp >= 2 && !sflag[0]) {
+        if (warp >= 2 && warp < 6 && !sflag[0]) {
             const float* inv = inv_all ? s_inv + n_tile * bn : (norm_scaled<EPI>(p) ? s_inv : nullptr);
-            cluster_reduce<T, EPI>(p, stile, reinterpret_cast<const float*>(smem), inv, xg_g, m_tile, n_tile, warp,
-                                   lane);
+            cluster_reduce<T, EPI, W8>(p, stile, reinterpret_cast<const float*>(smem), inv, xg_g, wsc, m_tile,
+                                       n_tile, warp, lane);
         }
         cluster_sync_all();           // peers are done reading this CTA's partial
     }
@@ -403,10 +556,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-template <typename T, int EPI>
+template <typename T, int EPI, bool W8>
 int launch_typed(const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B, const GemmPlan& plan,
                  const GemmParams& p, cudaStream_t stream, bool pdl) {
-    auto kern = k_gemm<T, EPI>;
+    auto kern = k_gemm<T, EPI, W8>;
     static size_t smem_set[64] = {};
     int dev = 0;
     PE_CUDA_TRY(cudaGetDevice(&dev));
@@ -418,7 +571,7 @@ int launch_typed(const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap&
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(W8 ? kThreadsW8 : kThreads);
     cfg.dynamicSmemBytes = plan.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -438,15 +591,15 @@ int launch_typed(const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap&
     return PE_OK;
 }
 
-template <typename T>
+template <typename T, bool W8>
 int launch_dispatch(int epi, const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B,
                     const GemmPlan& plan, const GemmParams& p, cudaStream_t stream, bool pdl) {
     switch (epi) {
-        case EPI_STORE: return launch_typed<T, EPI_STORE>(A, A2, B, plan, p, stream, pdl);
-        case EPI_QKV: return launch_typed<T, EPI_QKV>(A, A2, B, plan, p, stream, pdl);
-        case EPI_RESID: return launch_typed<T, EPI_RESID>(A, A2, B, plan, p, stream, pdl);
-        case EPI_SWIGLU: return launch_typed<T, EPI_SWIGLU>(A, A2, B, plan, p, stream, pdl);
-        case EPI_ARGMAX: return launch_typed<T, EPI_ARGMAX>(A, A2, B, plan, p, stream, pdl);
+        case EPI_STORE: return launch_typed<T, EPI_STORE, W8>(A, A2, B, plan, p, stream, pdl);
+        case EPI_QKV: return launch_typed<T, EPI_QKV, W8>(A, A2, B, plan, p, stream, pdl);
+        case EPI_RESID: return launch_typed<T, EPI_RESID, W8>(A, A2, B, plan, p, stream, pdl);
+        case EPI_SWIGLU: return launch_typed<T, EPI_SWIGLU, W8>(A, A2, B, plan, p, stream, pdl);
+        case EPI_ARGMAX: return launch_typed<T, EPI_ARGMAX, W8>(A, A2, B, plan, p, stream, pdl);
         default: set_error("unknown GEMM epilogue"); return PE_ERR_ARG;
     }
 }
@@ -456,20 +609,25 @@ inline int round_up(int a, int b) { return ceil_div(a, b) * b; }
 
 }  // namespace
 
-GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster) {
+GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster, bool w8) {
     GemmPlan g{};
-    const int bk = kRowBytes / elem_bytes;
+    g.w8 = w8;
+    // k elements per stage: one 128-byte swizzle row of weights (128 FP8 codes)
+    const int bk = w8 ? kRowBytes : kRowBytes / elem_bytes;
     g.kb_total = ceil_div(Kd, bk);
-    if (N <= 256) {
+    // token tile: up to 256 rows (128 with FP8 weights, whose stages carry
+    // two token tiles each next to the bf16 weight copies)
+    const int bn_max = w8 ? 128 : 256;
+    if (N <= bn_max) {
         g.n_tiles = 1;
         g.bn = round_up(N < 1 ? 1 : N, 16);
     } else {
-        g.n_tiles = ceil_div(N, 256);
+        g.n_tiles = ceil_div(N, bn_max);
         g.bn = round_up(ceil_div(N, g.n_tiles), 16);
     }
     const int rows_per_tile = epi == EPI_SWIGLU ? 64 : kBM;
     g.m_tiles = ceil_div(M, rows_per_tile);
-    if ((epi == EPI_RESID || epi == EPI_QKV) && cluster && N > 256) {
+    if ((epi == EPI_RESID || epi == EPI_QKV) && cluster && N > 256 && !w8) {
         // O, down and QKV have few weight tiles (16 and 40 at the Qwen
         // shape): narrower token tiles, down to 128 rows, when that lets the
         // tiles fill one wave of SMs
@@ -487,12 +645,17 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     // can start their weight loads beside this one) for token tiles up to
     // 128 rows; ~190 KB above that (at 96 rows the small ring measured 17%
     // faster per step, at 176 rows its two stages were much slower)
-    const size_t stage = kABytes + static_cast<size_t>(g.bn) * kRowBytes;
-    const size_t budget = g.bn <= 128 ? 100 * 1024 : 190 * 1024;
+    const size_t stage = kABytes + static_cast<size_t>(g.bn) * kRowBytes * (w8 ? 2 : 1);
+    const int inv_floats = (epi == EPI_QKV || epi == EPI_SWIGLU) ? inv_slots(N) : 0;
+    // FP8 weights: one CTA per SM, the ring in what the bf16 copies, the
+    // staging tile and the folded-norm scales leave of ~215 KB
+    const size_t budget = w8 ? 215 * 1024 - static_cast<size_t>(kConvStages) * kConvBytes -
+                                   static_cast<size_t>(kChunk) * kPitch * 4 - static_cast<size_t>(inv_floats) * 4 - 2048
+                             : (g.bn <= 128 ? 100 * 1024 : 190 * 1024);
     int st = static_cast<int>(budget / stage);
     g.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
-    g.smem_bytes = gemm_smem_bytes(g.stages, g.bn, (epi == EPI_QKV || epi == EPI_SWIGLU) ? inv_slots(N) : 0);
-    const int ctas_per_sm = g.smem_bytes <= 113 * 1024 ? 2 : 1;
+    g.smem_bytes = gemm_smem_bytes(g.stages, g.bn, inv_floats, w8);
+    const int ctas_per_sm = (!w8 && g.smem_bytes <= 113 * 1024) ? 2 : 1;
     int splits = 1;
     if (epi != EPI_ARGMAX) {
         if (cluster) {
@@ -535,8 +698,8 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
 
 int gemm_store_kernels_load() {
     cudaFuncAttributes fa;
-    PE_CUDA_TRY(cudaFuncGetAttributes(&fa, k_gemm<__nv_bfloat16, EPI_STORE>));
-    PE_CUDA_TRY(cudaFuncGetAttributes(&fa, k_gemm<float, EPI_STORE>));
+    PE_CUDA_TRY(cudaFuncGetAttributes(&fa, k_gemm<__nv_bfloat16, EPI_STORE, false>));
+    PE_CUDA_TRY(cudaFuncGetAttributes(&fa, k_gemm<float, EPI_STORE, false>));
     return PE_OK;
 }
 
@@ -551,8 +714,15 @@ int launch_gemm(int dtype, int epi, const CUtensorMap& A, const CUtensorMap& A2,
     p.stages = plan.stages;
     p.cluster = plan.cluster ? 1 : 0;
     p.persistent = plan.persistent ? 1 : 0;
-    if (dtype == PE_DTYPE_BF16) return launch_dispatch<__nv_bfloat16>(epi, A, A2, B, plan, p, stream, pdl);
-    return launch_dispatch<float>(epi, A, A2, B, plan, p, stream, pdl);
+    if (plan.w8) {
+        if (dtype != PE_DTYPE_BF16 || p.w_scale == nullptr || (epi == EPI_SWIGLU && p.w_scale2 == nullptr)) {
+            set_error("FP8 weights need bf16 activations and per-row weight scales");
+            return PE_ERR_ARG;
+        }
+        return launch_dispatch<__nv_bfloat16, true>(epi, A, A2, B, plan, p, stream, pdl);
+    }
+    if (dtype == PE_DTYPE_BF16) return launch_dispatch<__nv_bfloat16, false>(epi, A, A2, B, plan, p, stream, pdl);
+    return launch_dispatch<float, false>(epi, A, A2, B, plan, p, stream, pdl);
 }
 
 }  // namespace pe

@@ -27,6 +27,8 @@ void set_error(const std::string& msg);
 
 int encode_tmap_2d(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t rows,
                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
+// the same over one-byte elements (FP8 weight codes)
+int encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 
 // ---------------------------------------------------------------- GEMM
 
@@ -81,9 +83,15 @@ struct GemmParams {
     // weight tiles m_tile < keep_tiles are loaded evict-last (they stay in L2
     // across steps); the rest evict-first
     int keep_tiles;
+    // FP8 weights (the kernel's W8 instance): accumulator row m is multiplied
+    // by w_scale[m] before the epilogue (SWIGLU: gate row f by w_scale[f], up
+    // row f by w_scale2[f])
+    const float* w_scale;
+    const float* w_scale2;
 };
 
 struct GemmPlan {
+    bool w8;            // FP8 (E4M3) weights widened to bf16 in shared memory; 128 k per stage
     int bn, n_tiles, m_tiles, splits, kb_total, kb_per_split, stages;
     int units;
     size_t smem_bytes;
@@ -94,7 +102,7 @@ struct GemmPlan {
     int grid;           // CTAs launched
 };
 
-GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster);
+GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster, bool w8 = false);
 int launch_gemm(int dtype, int epi, const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B,
                 const GemmPlan& plan, GemmParams p, cudaStream_t stream, bool pdl);
 // Loads the plain-store GEMM kernels of both dtypes on the current device

@@ -22,8 +22,10 @@
 #include "internal.h"
 
 struct pe_handle {
-    pe_config cfg;
+    pe_config cfg;                // dtype is the activation dtype (bf16 for an FP8-weight drafter)
     pe_weights w;
+    bool w8 = false;              // GEMM weights are E4M3 codes with per-row scales
+    pe_weight_scales sc{};
     int device = 0;
     int max_batch = 0;
     int max_rows = 0;
@@ -123,6 +125,30 @@ int encode_tmap_2d(CUtensorMap* map, const void* base, int dtype, uint64_t inner
     return PE_OK;
 }
 
+int encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (fn == nullptr) {
+        set_error("cuTensorMapEncodeTiled entry point not available");
+        return PE_ERR_CUDA;
+    }
+    if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || (inner & 15u) != 0) {
+        set_error("FP8 weights must be 16-byte aligned with rows a multiple of 16 bytes");
+        return PE_ERR_ARG;
+    }
+    cuuint64_t dims[2] = {inner, rows < 1 ? 1 : rows};
+    cuuint64_t strides[1] = {inner};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled (u8) failed with code " + std::to_string(static_cast<int>(r)));
+        return PE_ERR_CUDA;
+    }
+    return PE_OK;
+}
+
 // bf16 paged KV cache [4][num_pages][nkv][16][hd] as a 4-D tensor
 // {hd, 16 slots, nkv, 4 * num_pages}; box = one page of one kv head, 64 dims
 // (128 bytes) wide, 128-byte swizzle.
@@ -185,8 +211,10 @@ constexpr int kBoxBytes = 128;   // inner TMA box = one 128-byte swizzle row
 
 int box_inner(const pe_handle* h) { return kBoxBytes / static_cast<int>(h->elem); }
 
-// weight [rows, cols] row-major; box rows 128 (64 for gate/up halves)
+// weight [rows, cols] row-major; box rows 128 (64 for gate/up halves); FP8
+// codes as one-byte elements, 128 per box row
 int weight_map(pe_handle* h, CUtensorMap* m, const void* w, int rows, int cols, int box_rows) {
+    if (h->w8) return encode_tmap_2d_u8(m, w, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows), box_rows);
     return encode_tmap_2d(m, w, h->cfg.dtype, cols, rows, static_cast<uint64_t>(cols) * h->elem, box_inner(h),
                           box_rows);
 }
@@ -231,7 +259,10 @@ int check_config(const pe_config& c) {
         set_error("k_max * (n_q_heads / n_kv_heads) must be <= 128");
         return PE_ERR_UNSUPPORTED;
     }
-    if (c.dtype != PE_DTYPE_BF16 && c.dtype != PE_DTYPE_FP32) { set_error("unknown dtype"); return PE_ERR_ARG; }
+    if (c.dtype != PE_DTYPE_BF16 && c.dtype != PE_DTYPE_FP32 && c.dtype != PE_DTYPE_FP8W) {
+        set_error("unknown dtype");
+        return PE_ERR_ARG;
+    }
     if (!(c.rms_eps > 0.f) || !(c.rope_theta > 0.f)) { set_error("rms_eps and rope_theta must be > 0"); return PE_ERR_ARG; }
     return PE_OK;
 }
@@ -254,12 +285,33 @@ int pe_abi_version(void) { return PE_ABI_VERSION; }
 
 const char* pe_last_error(void) { return g_last_error.c_str(); }
 
-int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max_batch, int32_t device,
-                    pe_handle** out) {
+}  // extern "C"
+
+namespace {
+
+int init_drafter(const pe_config* cfg, const pe_weights* weights, const pe_weight_scales* scales, int32_t max_batch,
+                 int32_t device, pe_handle** out) {
     if (cfg == nullptr || weights == nullptr || out == nullptr) { set_error("null argument"); return PE_ERR_ARG; }
     *out = nullptr;
     int rc = check_config(*cfg);
     if (rc != PE_OK) return rc;
+    const bool w8 = cfg->dtype == PE_DTYPE_FP8W;
+    if (w8 != (scales != nullptr)) {
+        set_error(w8 ? "FP8 weights need pe_init_drafter_fp8 and its scales"
+                     : "weight scales are only taken with dtype PE_DTYPE_FP8W");
+        return PE_ERR_ARG;
+    }
+    if (w8) {
+        const void* sp[] = {scales->fc, scales->lm_head};
+        for (const void* p : sp)
+            if (p == nullptr) { set_error("null weight scale pointer"); return PE_ERR_ARG; }
+        for (int l = 0; l < 4; ++l) {
+            const pe_layer_scales& L = scales->layer[l];
+            const void* lp[] = {L.w_qkv, L.w_o, L.w_gate, L.w_up, L.w_down};
+            for (const void* p : lp)
+                if (p == nullptr) { set_error("null layer weight scale pointer"); return PE_ERR_ARG; }
+        }
+    }
     if (max_batch < 1) { set_error("max_batch must be >= 1"); return PE_ERR_ARG; }
     const pe_weights& w = *weights;
     const void* req[] = {w.fc, w.embed, w.emb_mask, w.h_shared, w.final_norm, w.lm_head};
@@ -285,11 +337,16 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
 
     pe_handle* h = new pe_handle();
     h->cfg = *cfg;
+    h->w8 = w8;
+    if (w8) {
+        h->sc = *scales;
+        h->cfg.dtype = PE_DTYPE_BF16;   // activations, embeddings, norms and KV cache
+    }
     h->w = w;
     h->device = device;
     h->max_batch = max_batch;
     h->max_rows = max_batch * cfg->k_max;
-    h->elem = cfg->dtype == PE_DTYPE_BF16 ? 2 : 4;
+    h->elem = h->cfg.dtype == PE_DTYPE_BF16 ? 2 : 4;
     const char* pdl_env = std::getenv("PE_PDL");
     h->pdl = !(pdl_env != nullptr && pdl_env[0] == '0');
     if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
@@ -313,7 +370,7 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
                             {V, H, EPI_ARGMAX}};
     for (const Shape& s : shapes) {
         for (int n = 1; n <= h->max_rows; ++n) {
-            GemmPlan g = plan_gemm(s.M, n, s.Kd, s.epi, elem_bytes, h->num_sms, true);
+            GemmPlan g = plan_gemm(s.M, n, s.Kd, s.epi, elem_bytes, h->num_sms, true, h->w8);
             ws = ws > g.ws_floats ? ws : g.ws_floats;
             tiles = tiles > g.tiles ? tiles : g.tiles;
         }
@@ -330,7 +387,7 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
     // (O, gate/up, down, QKV and O, gate/up, down, LM head) at the widest
     // token tile it serves
     const char* chain_env = std::getenv("PE_LAYER_CHAIN");
-    h->chain = cfg->dtype == PE_DTYPE_BF16 && chain_env != nullptr && chain_env[0] == '1' &&
+    h->chain = cfg->dtype == PE_DTYPE_BF16 && !h->w8 && chain_env != nullptr && chain_env[0] == '1' &&
                chain_supported(device);
     if (h->chain) {
         const int n_top = h->max_rows < kMaxChainBn ? h->max_rows : kMaxChainBn;
@@ -416,6 +473,22 @@ int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max
     return PE_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int pe_init_drafter(const pe_config* cfg, const pe_weights* weights, int32_t max_batch, int32_t device,
+                    pe_handle** out) {
+    return init_drafter(cfg, weights, nullptr, max_batch, device, out);
+}
+
+int pe_init_drafter_fp8(const pe_config* cfg, const pe_weights* weights, const pe_weight_scales* scales,
+                        int32_t max_batch, int32_t device, pe_handle** out) {
+    if (scales == nullptr) { set_error("null weight scales"); return PE_ERR_ARG; }
+    if (cfg != nullptr && cfg->dtype != PE_DTYPE_FP8W) { set_error("pe_init_drafter_fp8 needs dtype PE_DTYPE_FP8W"); return PE_ERR_ARG; }
+    return init_drafter(cfg, weights, scales, max_batch, device, out);
+}
+
 void pe_destroy(pe_handle* h) {
     if (h == nullptr) return;
     cudaSetDevice(h->device);
@@ -488,13 +561,13 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
     int rc;
 
     // GEMM plans (bn depends only on the row count)
-    const GemmPlan p_fc = plan_gemm(H, B, 3 * H, EPI_STORE, eb, h->num_sms, true);
-    const GemmPlan p_qkv0 = plan_gemm(qkv_rows, R, 2 * H, EPI_QKV, eb, h->num_sms, true);
-    const GemmPlan p_qkv = plan_gemm(qkv_rows, R, H, EPI_QKV, eb, h->num_sms, true);
-    const GemmPlan p_o = plan_gemm(H, R, qd, EPI_RESID, eb, h->num_sms, true);
-    const GemmPlan p_gu = plan_gemm(F, R, H, EPI_SWIGLU, eb, h->num_sms, true);
-    const GemmPlan p_down = plan_gemm(H, R, F, EPI_RESID, eb, h->num_sms, true);
-    const GemmPlan p_lm = plan_gemm(V, R, H, EPI_ARGMAX, eb, h->num_sms, true);
+    const GemmPlan p_fc = plan_gemm(H, B, 3 * H, EPI_STORE, eb, h->num_sms, true, h->w8);
+    const GemmPlan p_qkv0 = plan_gemm(qkv_rows, R, 2 * H, EPI_QKV, eb, h->num_sms, true, h->w8);
+    const GemmPlan p_qkv = plan_gemm(qkv_rows, R, H, EPI_QKV, eb, h->num_sms, true, h->w8);
+    const GemmPlan p_o = plan_gemm(H, R, qd, EPI_RESID, eb, h->num_sms, true, h->w8);
+    const GemmPlan p_gu = plan_gemm(F, R, H, EPI_SWIGLU, eb, h->num_sms, true, h->w8);
+    const GemmPlan p_down = plan_gemm(H, R, F, EPI_RESID, eb, h->num_sms, true, h->w8);
+    const GemmPlan p_lm = plan_gemm(V, R, H, EPI_ARGMAX, eb, h->num_sms, true, h->w8);
     const bool attn_umma = dt == PE_DTYPE_BF16;
     const AttnPlan p_at = attn_umma ? plan_attention_umma(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms)
                                   : plan_attention(B, K, nq, nkv, hd, max_pages, c.page_size, h->num_sms);
@@ -561,6 +634,7 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
         GemmParams p = base;
         p.M = H; p.N = B; p.Kd = 3 * H;
         p.out_f32 = h->h; p.ld_out = H;
+        p.w_scale = h->sc.fc;
         rc = run(PE_KERNEL_FC, [&] { return launch_gemm(dt, EPI_STORE, h->tm_fc, h->tm_fc, tm_th, p_fc, p, s, pdl); });
         if (rc != PE_OK) return rc;
     }
@@ -597,24 +671,28 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
         p.out_act = h->q; p.ld_act = qd;
         p.k_cache = kcache(l); p.v_cache = vcache(l); p.nq_hd = qd; p.nkv = nkv; p.hd = hd;
         p.row_slot = h->row_slot; p.rope_cs = h->rope_cs;
+        p.w_scale = h->sc.layer[l].w_qkv;
         if (l > 0) fold_norm_in(p);   // attention RMSNorm of layer l
         return p;
     };
     auto gp_o = [&](int l) {      // a5: O projection + residual
         GemmParams p = base;
         p.M = H; p.Kd = qd; p.out_f32 = h->resid; p.ld_out = H;
+        p.w_scale = h->sc.layer[l].w_o;
         fold_norm_out(p, h->w.layer[l].mlp_norm);
         return p;
     };
-    auto gp_gu = [&](int) {       // a6: gate/up + SwiGLU
+    auto gp_gu = [&](int l) {     // a6: gate/up + SwiGLU
         GemmParams p = base;
         p.M = F; p.Kd = H; p.out_act = h->act; p.ld_act = F;
+        p.w_scale = h->sc.layer[l].w_gate; p.w_scale2 = h->sc.layer[l].w_up;
         fold_norm_in(p);   // MLP RMSNorm
         return p;
     };
     auto gp_down = [&](int l) {   // a6: down + residual
         GemmParams p = base;
         p.M = H; p.Kd = F; p.out_f32 = h->resid; p.ld_out = H;
+        p.w_scale = h->sc.layer[l].w_down;
         fold_norm_out(p, l < 3 ? h->w.layer[l + 1].attn_norm : h->w.final_norm);
         return p;
     };
@@ -623,7 +701,8 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
         p.M = V; p.Kd = H; p.amax = h->amax; p.logits = ps.logits; p.ld_logits = ps.logits_ld;
         // the LM head's first ~40 MB of weights stay in L2 between steps
         // (measured: 40 MB faster, 80 and 100 MB slower than none at B=1, B=4)
-        p.keep_tiles = static_cast<int>((40LL << 20) / (128LL * H * static_cast<long long>(h->elem)));
+        p.keep_tiles = static_cast<int>((40LL << 20) / (128LL * H * (h->w8 ? 1LL : static_cast<long long>(h->elem))));
+        p.w_scale = h->sc.lm_head;
         return p;
     };
     // O, gate/up, down of layer l and then the next layer's QKV (or the LM
@@ -883,12 +962,16 @@ int pe_verify_rebuild(pe_handle* h, int32_t B, int32_t K, const int32_t* drafts,
 
 int pe_linear_scratch(int32_t dtype, int32_t M, int32_t N, int32_t Kd, int64_t* ws_floats, int32_t* n_tickets) {
     if (ws_floats == nullptr || n_tickets == nullptr) { set_error("null argument"); return PE_ERR_ARG; }
-    if (dtype != PE_DTYPE_BF16 && dtype != PE_DTYPE_FP32) { set_error("unknown dtype"); return PE_ERR_ARG; }
+    if (dtype != PE_DTYPE_BF16 && dtype != PE_DTYPE_FP32 && dtype != PE_DTYPE_FP8W) {
+        set_error("unknown dtype");
+        return PE_ERR_ARG;
+    }
     if (M < 1 || N < 1 || Kd < 1) { set_error("M, N, Kd must be >= 1"); return PE_ERR_ARG; }
     int dev = 0, sms = 0;
     PE_CUDA_TRY(cudaGetDevice(&dev));
     PE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    const GemmPlan g = plan_gemm(M, N, Kd, EPI_STORE, dtype == PE_DTYPE_BF16 ? 2 : 4, sms, false);
+    const GemmPlan g = plan_gemm(M, N, Kd, EPI_STORE, dtype == PE_DTYPE_FP32 ? 4 : 2, sms, false,
+                                 dtype == PE_DTYPE_FP8W);
     *ws_floats = static_cast<int64_t>(g.ws_floats);
     *n_tickets = g.tiles;
     return PE_OK;
@@ -912,6 +995,28 @@ int pe_linear(int32_t dtype, int32_t M, int32_t N, int32_t Kd, const void* w, co
     GemmParams p{};
     p.M = M; p.N = N; p.Kd = Kd; p.out_f32 = y; p.ld_out = M; p.ws = ws; p.tickets = tickets; p.err = nullptr;
     return launch_gemm(dtype, EPI_STORE, ta, ta, tb, g, p, static_cast<cudaStream_t>(stream), false);
+}
+
+int pe_linear_fp8(int32_t M, int32_t N, int32_t Kd, const void* w, const float* w_scale, const void* x, float* y,
+                  float* ws, int32_t* tickets, void* stream) {
+    if (!w || !w_scale || !x || !y || !tickets) { set_error("null tensor argument"); return PE_ERR_ARG; }
+    if (M < 1 || N < 1 || Kd < 16 || Kd % 16 != 0) {
+        set_error("need M, N >= 1 and Kd a positive multiple of 16");
+        return PE_ERR_ARG;
+    }
+    int dev = 0, sms = 0;
+    PE_CUDA_TRY(cudaGetDevice(&dev));
+    PE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const GemmPlan g = plan_gemm(M, N, Kd, EPI_STORE, 2, sms, false, true);
+    if (g.ws_floats > 0 && ws == nullptr) { set_error("this shape needs split-K scratch"); return PE_ERR_ARG; }
+    CUtensorMap ta, tb;
+    int rc = encode_tmap_2d_u8(&ta, w, static_cast<uint64_t>(Kd), static_cast<uint64_t>(M), 128);
+    if (rc == PE_OK) rc = encode_tmap_2d(&tb, x, PE_DTYPE_BF16, Kd, N, static_cast<uint64_t>(Kd) * 2, 64, g.bn);
+    if (rc != PE_OK) return rc;
+    GemmParams p{};
+    p.M = M; p.N = N; p.Kd = Kd; p.out_f32 = y; p.ld_out = M; p.ws = ws; p.tickets = tickets; p.err = nullptr;
+    p.w_scale = w_scale;
+    return launch_gemm(PE_DTYPE_BF16, EPI_STORE, ta, ta, tb, g, p, static_cast<cudaStream_t>(stream), false);
 }
 
 struct pe_step_graph {
