@@ -71,11 +71,12 @@ def workload_desc(wl):
             f"V={s.vocab}, 4 layers, {s.dtype}), B={wl.B}, K={wl.K}, prefix {prefix} in 16-token pages")
 
 
-def algorithmic_work(kind, wl, seq_lens, chained=False):
+def algorithmic_work(kind, wl, seq_lens, chained=False, fp8=False):
     """Algorithmic HBM bytes and FLOPs of ONE launch of a kernel kind,
     averaged over that kind's launches in a step. `chained`: the step runs
     O, gate/up, down and the next QKV (or the LM head) as one persistent
-    layer-chain launch per layer."""
+    layer-chain launch per layer. `fp8`: the GEMM weights are E4M3 codes
+    (one byte each) with one fp32 scale per output row."""
     s = wl.shape
     e = 2 if s.dtype == "bf16" else 4
     H, F, V, hd, nq, nkv = s.hidden, s.ffn, s.vocab, s.head_dim, s.n_q_heads, s.n_kv_heads
@@ -83,26 +84,29 @@ def algorithmic_work(kind, wl, seq_lens, chained=False):
     R = B * K
     qd, qkv = nq * hd, s.qkv_rows
 
+    def wb(rows, cols):      # bytes of one weight matrix
+        return rows * cols + 4 * rows if fp8 else rows * cols * e
+
     def qkv_work(kin):       # + q out and the new K/V rows
-        return qkv * kin * e + R * kin * e + R * qd * e + R * 2 * nkv * hd * e, 2 * R * qkv * kin
+        return wb(qkv, kin) + R * kin * e + R * qd * e + R * 2 * nkv * hd * e, 2 * R * qkv * kin
 
     def o_work():            # + residual read/write and the folded RMSNorm's gain * r output
-        return H * qd * e + R * qd * e + 2 * R * H * 4 + R * H * e, 2 * R * H * qd
+        return wb(H, qd) + R * qd * e + 2 * R * H * 4 + R * H * e, 2 * R * H * qd
 
     def gu_work():
-        return 2 * F * H * e + R * H * e + R * F * e, 2 * R * 2 * F * H
+        return 2 * wb(F, H) + R * H * e + R * F * e, 2 * R * 2 * F * H
 
     def down_work():
-        return H * F * e + R * F * e + 2 * R * H * 4 + R * H * e, 2 * R * H * F
+        return wb(H, F) + R * F * e + 2 * R * H * 4 + R * H * e, 2 * R * H * F
 
     def lm_work():
-        return V * H * e + R * H * e + R * 8, 2 * R * V * H
+        return wb(V, H) + R * H * e + R * 8, 2 * R * V * H
 
     def add(*ws):
         return sum(w[0] for w in ws), sum(w[1] for w in ws)
 
     if kind == "fc":
-        return 3 * H * H * e + B * 3 * H * e + B * H * 4, 2 * B * 3 * H * H
+        return wb(H, 3 * H) + B * 3 * H * e + B * H * 4, 2 * B * 3 * H * H
     if kind == "qkv":
         if chained:          # only layer 0's QKV (2H inputs) runs on its own
             return qkv_work(2 * H)
@@ -130,15 +134,28 @@ def algorithmic_work(kind, wl, seq_lens, chained=False):
     return R * 12, R
 
 
-def step_bytes(wl, seq_lens):
+def gemm_weight_shapes(s):
+    """(rows, cols) of every GEMM weight matrix of the drafter."""
+    H, F, qd = s.hidden, s.ffn, s.n_q_heads * s.head_dim
+    mats = [(H, 3 * H), (s.vocab, H)]
+    for layer in range(s.n_layers):
+        mats += [(s.qkv_rows, 2 * H if layer == 0 else H), (H, qd), (F, H), (F, H), (H, F)]
+    return mats
+
+
+def step_bytes(wl, seq_lens, fp8=False):
     """Algorithmic HBM bytes of one whole step: every weight matrix once,
     except the token embedding, of which only the B gathered rows are read;
     plus the KV cache read (prefix and new entries) and the new entries
-    written."""
+    written. `fp8`: GEMM weights at one byte each plus a 4-byte scale per
+    row."""
     s = wl.shape
     e = 2 if s.dtype == "bf16" else 4
     R = wl.B * wl.K
     weights = (s.param_count() - s.vocab * s.hidden + wl.B * s.hidden) * e
+    if fp8:
+        gemm = gemm_weight_shapes(s)
+        weights += sum(r * c + 4 * r - r * c * e for r, c in gemm)
     kv_read = sum(int(S) + wl.K for S in seq_lens) * s.n_kv_heads * s.head_dim * 2 * e * s.n_layers
     kv_write = R * s.n_kv_heads * s.head_dim * 2 * e * s.n_layers
     return weights + kv_read + kv_write
@@ -271,16 +288,18 @@ def cpu_baseline_obj(res, wl):
 
 # ------------------------------------------------------------------ our arm
 
+FP8_WORKLOADS = ("qwen-b1-k3", "qwen-b1-k7", "qwen-b1-k11", "qwen-b8-k7", "qwen-b32-k11", "qwen-b128-k11",
+                 "gptoss-b64-k10")
 SWEEP_WORKLOADS = (["qwen-b1-k3", "qwen-b1-k7", "qwen-b1-k11"]
                    + [f"qwen-b{B}-k{K}" for B in (4, 8, 32, 128) for K in (3, 7, 11)]
                    + ["gptoss-b64-k10"])
 
 
-def roofline_of(kind, wl, seq_np, avg_launch_s, peaks, chained=False):
+def roofline_of(kind, wl, seq_np, avg_launch_s, peaks, chained=False, fp8=False):
     """Roofline of one kernel kind: its algorithmic bytes (or FLOPs) per
     launch over its measured average launch time, against the measured peak
     of whichever resource bounds it at these sizes."""
-    b, f = algorithmic_work(kind, wl, seq_np, chained=chained)
+    b, f = algorithmic_work(kind, wl, seq_np, chained=chained, fp8=fp8)
     t_hbm = b / (peaks["hbm_gbs"] * 1e9)
     t_tc = f / (peaks["bf16_tflops_sustained"] * 1e12)
     if t_hbm >= t_tc:
@@ -291,24 +310,27 @@ def roofline_of(kind, wl, seq_np, avg_launch_s, peaks, chained=False):
             "frac": a / peaks["bf16_tflops_sustained"]}
 
 
-def sweep_workload(name, dev, weights_cache, peaks, replays):
+def sweep_workload(name, dev, weights_cache, peaks, replays, fp8=False):
     """Steps/s, draft tok/s, step HBM fraction and the dominant kernel's
     roofline for one workload: per-kind CUDA events over three direct steps
-    (shares and per-launch times), then `replays` timed step-graph replays."""
+    (shares and per-launch times), then `replays` timed step-graph replays.
+    `fp8`: the drafter's GEMM weights as E4M3 codes with per-row scales."""
     import torch
 
     from speculative_drafting_pe_gb300 import binding, synth
 
     wl = synth.WORKLOADS[name]
-    key = (wl.shape.name, wl.seed)
+    key = (wl.shape.name, wl.seed, fp8)
     if key not in weights_cache:
         weights_cache.clear()
         torch.cuda.empty_cache()
-        weights_cache[key] = synth.make_weights(wl.shape, wl.seed, device=dev)
-    W = weights_cache[key]
+        W0 = synth.make_weights(wl.shape, wl.seed, device=dev)
+        weights_cache[key] = synth.quantize_weights_fp8(W0) if fp8 else (W0, None)
+        del W0
+    W, scales = weights_cache[key]
     inp = synth.make_step_inputs(wl, device=dev)
     seq_np = inp.seq_lens.cpu().numpy()
-    drafter = binding.Drafter(wl.shape, W, max_batch=wl.B, k_max=wl.K)
+    drafter = binding.Drafter(wl.shape, W, max_batch=wl.B, k_max=wl.K, fp8_scales=scales)
     B, K = wl.B, wl.K
     drafts = torch.empty(B, K, dtype=torch.int32, device=dev)
     status = torch.empty(B, dtype=torch.int32, device=dev)
@@ -348,9 +370,10 @@ def sweep_workload(name, dev, weights_cache, peaks, replays):
     torch.cuda.synchronize()
     assert drafter.device_errors() == 0
     ms_step = e0.elapsed_time(e1) / replays
-    roof = roofline_of(dominant, wl, seq_np, per_kind[dominant][1], peaks)
+    roof = roofline_of(dominant, wl, seq_np, per_kind[dominant][1], peaks, fp8=fp8)
     out = {"steps_s": 1e3 / ms_step, "ms_per_step": ms_step, "draft_tok_s": 1e3 / ms_step * B * K,
-           "step_hbm_frac": step_bytes(wl, seq_np) / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"],
+           "step_bytes": step_bytes(wl, seq_np, fp8=fp8),
+           "step_hbm_frac": step_bytes(wl, seq_np, fp8=fp8) / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"],
            "dominant": dominant, "dominant_us_per_launch": per_kind[dominant][1] * 1e6,
            "dominant_roofline": {k: roof[k] for k in ("bound", "achieved", "unit", "frac")},
            "kernel_ms_per_step": {k: round(v[0], 4) for k, v in sorted(per_kind.items(), key=lambda x: -x[1][0])}}
@@ -560,14 +583,18 @@ def bench_ours(args):
 
     # ---------------- every workload of the metric (C2, C3, C4): one line each
     sweep = None
+    fp8_lines = None
     if not args.no_sweep and world == 1 and args.max_prefix == 0:
         peaks0, _ = load_peaks()
         del sg, sg_e
         drafter.close()
-        cache = {(wl.shape.name, wl.seed): W}
+        cache = {(wl.shape.name, wl.seed, False): (W, None)}
         sweep = {}
         for name in SWEEP_WORKLOADS:
             sweep[name] = sweep_workload(name, dev, cache, peaks0, max(args.steps, 50))
+        fp8_lines = {}
+        for name in FP8_WORKLOADS:
+            fp8_lines[name] = sweep_workload(name, dev, cache, peaks0, max(args.steps, 50), fp8=True)
         cache.clear()
 
     if rank != 0:
@@ -639,6 +666,10 @@ def bench_ours(args):
         line["cold_l2"] = cold
     if sweep:
         line["sweep"] = sweep
+    if fp8_lines:
+        line["fp8_weights"] = fp8_lines
+        line["fp8_note"] = ("the same workloads with FP8 (E4M3) GEMM weights and per-row fp32 scales (bf16 "
+                            "activations and KV); step_bytes counts one byte per weight plus the scales")
     if world == 1 and not args.no_cpu_baseline:
         try:
             res = run_oracle_subprocess(args.workload, args.cpu_seconds, 1000)

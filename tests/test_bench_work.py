@@ -79,3 +79,21 @@ def test_max_prefix_option_caps_both_ends():
     wl = synth.WORKLOADS["qwen-b128-k11"]
     capped = dataclasses.replace(wl, prefix=(min(wl.prefix[0], 512), min(wl.prefix[1], 512)))
     assert capped.prefix == (512, 512) and capped.B == wl.B and capped.K == wl.K
+
+
+def test_fp8_step_bytes_count_one_byte_per_gemm_weight_plus_row_scales():
+    wl = synth.WORKLOADS["qwen-b1-k7"]
+    s = wl.shape
+    seq = [2048]
+    full = bench.step_bytes(wl, seq)
+    fp8 = bench.step_bytes(wl, seq, fp8=True)
+    mats = bench.gemm_weight_shapes(s)
+    assert len(mats) == 2 + 5 * 4
+    params = sum(r * c for r, c in mats)
+    rows = sum(r for r, _ in mats)
+    assert full - fp8 == params * 2 - (params + 4 * rows)
+    # the GEMM matrices are all weights but the embedding and the small vectors
+    assert params == pytest.approx(s.param_count() - s.vocab * s.hidden, rel=1e-3)
+    b, _ = bench.algorithmic_work("lm_head", wl, seq, fp8=True)
+    R = wl.B * wl.K
+    assert b == s.vocab * s.hidden + 4 * s.vocab + R * s.hidden * 2 + R * 8
