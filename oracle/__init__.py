@@ -20,6 +20,7 @@ from .drafter import (  # noqa: F401
     lm_head_logits,
     draft_pass,
     draft_sequential,
+    draft_pass_refeed,
     argmax_lowest,
     top2_gap,
 )
@@ -28,6 +29,7 @@ from .verify import (  # noqa: F401
     accept_length,
     verify,
     rebuild_metadata,
+    rebuild_metadata_refeed,
     emitted_tokens,
     expected_tokens_iid,
     tokens_per_pass_linear,

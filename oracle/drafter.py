@@ -314,3 +314,59 @@ def draft_sequential(cfg, W, last_token, target_hidden, positions, seq_lens,
         "v_new": v_new,
         "h": h,
     }
+
+
+def draft_pass_refeed(cfg, W, tokens, n_real, target_hidden, positions, seq_lens,
+                      page_table, k_cache, v_cache, K):
+    """Parallel draft pass with the accepted tokens re-fed as real rows.
+
+    Reading F2 (the alternative to R6 where the pages are silent on the
+    drafter's bookkeeping; also in the design notes): after a verify, the n_b
+    tokens it emitted (the accepted drafts and the bonus token) come back
+    with the target's hidden states at their positions as n_b REAL rows -
+    each row the embedding of its token and the FC-fused hidden state, the
+    pages' position-1 input - ahead of the K-1 placeholder rows (emb_mask,
+    h_shared). Real row i sits at position Q_b + i and cache entry S_b + i;
+    placeholder j (1..K-1) at position Q_b + n_b - 1 + j and entry
+    S_b + n_b - 1 + j. Draft 0 is the argmax of the last real row, draft j
+    that of placeholder j. Every row attends causally as in R6.
+
+    tokens [B, n_max] (entries past n_real[b] unused), n_real [B] in
+    1..n_max, target_hidden [B, n_max, 3H]. Each request runs as its own
+    batch of n_b + K - 1 rows. Returns logits / drafts / gap [B, K, ...] and
+    k_new / v_new [L, B, n_max + K - 1, nkv, hd] (rows past n_b + K - 1 of a
+    request are NaN).
+    """
+    B = len(n_real)
+    H = cfg.hidden
+    eps = cfg.rms_eps
+    n_max = int(np.max(n_real))
+    T_max = n_max + K - 1
+    L0 = W["layers"][0]
+    embed = np.asarray(W["embed"], dtype=np.float64)
+    logits = np.empty((B, K, cfg.vocab), dtype=np.float64)
+    k_new = np.full((cfg.n_layers, B, T_max, cfg.n_kv_heads, cfg.head_dim), np.nan)
+    v_new = np.full_like(k_new, np.nan)
+    for b in range(B):
+        n = int(n_real[b])
+        h = linear(np.asarray(target_hidden[b, :n], dtype=np.float64), W["fc"])      # R1, per real row
+        emb = embed[np.asarray(tokens[b, :n], dtype=np.int64)]
+        if K > 1:
+            emb = np.concatenate([emb, np.repeat(np.asarray(W["emb_mask"], np.float64)[None], K - 1, 0)])
+            hid = np.concatenate([h, np.repeat(np.asarray(W["h_shared"], np.float64)[None], K - 1, 0)])
+        else:
+            hid = h
+        u = np.concatenate([rms_norm(emb, L0["norm_e"], eps), rms_norm(hid, L0["norm_h"], eps)], axis=-1)
+        resid, kb, vb = run_layers(cfg, W, u[None], hid[None].copy(), np.asarray(positions)[b:b + 1],
+                                   np.asarray(seq_lens)[b:b + 1], np.asarray(page_table)[b:b + 1],
+                                   k_cache, v_cache)
+        logits[b] = lm_head_logits(cfg, W, resid[0, n - 1:])
+        k_new[:, b, :n + K - 1] = kb[:, 0]
+        v_new[:, b, :n + K - 1] = vb[:, 0]
+    return {
+        "logits": logits,
+        "drafts": argmax_lowest(logits),
+        "gap": top2_gap(logits),
+        "k_new": k_new,
+        "v_new": v_new,
+    }

@@ -156,3 +156,55 @@ def speedup_linear(alpha, K, overhead):
 def breakeven_alpha(overhead, K):
     """alpha at which speedup_linear equals 1: overhead / K."""
     return float(overhead) / K
+
+
+def rebuild_metadata_refeed(accepted, K, n_real, seq_lens, positions, page_table, num_pages, page_size=16):
+    """Batch metadata after a verify when the next pass re-feeds the emitted
+    tokens as real rows (reading F2 of the drafter).
+
+    The pass just verified wrote n_b real rows at entries S_b .. S_b+n_b-1
+    and K-1 placeholder rows after them. The real rows stay committed and the
+    placeholders are rolled back: S_b' = S_b + n_b, Q_b' = Q_b + n_b, and the
+    next pass has n_b' = a_b + 1 real rows (the accepted drafts and the bonus
+    token). Returns seq_lens, positions, n_real (next step), slot_mapping
+    [B, 2K] (slots of the next pass's entries S_b' .. S_b'+n_b'+K-2, then -1),
+    rollback_slots [B, K] (slots of entries S_b+n_b .. S_b+n_b+K-2, then -1)
+    and status, with the input checks of V5 (a request whose next pass does
+    not fit its page table, or whose page is out of range, keeps its
+    metadata, n_real' = n_real, and gets -1 rows).
+    """
+    accepted = np.asarray(accepted, dtype=np.int64)
+    seq_lens = np.asarray(seq_lens, dtype=np.int64)
+    positions = np.asarray(positions, dtype=np.int64)
+    n_real = np.asarray(n_real, dtype=np.int64)
+    page_table = np.asarray(page_table, dtype=np.int64)
+    B = len(accepted)
+    max_pages = page_table.shape[1]
+    new_S, new_Q, new_n = seq_lens.copy(), positions.copy(), n_real.copy()
+    slot_mapping = np.full((B, 2 * K), -1, dtype=np.int64)
+    rollback = np.full((B, K), -1, dtype=np.int64)
+    status = np.full(B, REQ_OK, dtype=np.int64)
+
+    def slot(b, e):
+        page = int(page_table[b, e // page_size])
+        return None if page < 0 or page >= num_pages else page * page_size + e % page_size
+
+    for b in range(B):
+        S, Q, n, a = int(seq_lens[b]), int(positions[b]), int(n_real[b]), int(accepted[b])
+        if not (0 <= S <= INT32_MAX - 4 * K and 0 <= Q <= INT32_MAX - 4 * K and 1 <= n <= K + 1):
+            status[b] = REQ_BAD_INPUT
+            continue
+        S2, Q2, n2 = S + n, Q + n, a + 1
+        if S2 + n2 + K - 1 > max_pages * page_size:
+            status[b] = REQ_CAPACITY
+            continue
+        nxt = [slot(b, S2 + j) for j in range(n2 + K - 1)]
+        rb = [slot(b, S + n + j) for j in range(K - 1)]
+        if any(x is None for x in nxt + rb):
+            status[b] = REQ_BAD_PAGE
+            continue
+        new_S[b], new_Q[b], new_n[b] = S2, Q2, n2
+        slot_mapping[b, :len(nxt)] = nxt
+        rollback[b, :len(rb)] = rb
+    return {"seq_lens": new_S, "positions": new_Q, "n_real": new_n, "slot_mapping": slot_mapping,
+            "rollback_slots": rollback, "status": status}

@@ -524,6 +524,168 @@ def test_fp8_draft_pass_is_the_draft_pass_on_dequantised_weights():
     assert np.abs(out["logits"] - base["logits"]).max() > 1e-6    # quantisation moved the logits
 
 
+# --------------------------------------------------------------- re-fed real rows
+
+def _torch_refeed(W, tokens, n_real, th, positions, seq_lens, page_table, kc, vc, K):
+    """Independent float64 restatement of the re-fed pass: per request a list
+    of n_b real rows (token embedding, FC of its target hidden state) and K-1
+    placeholder rows, causal SDPA over the page-table walk of the committed
+    entries followed by the rows, logits of the last real row and of every
+    placeholder."""
+    cfg = TINY
+    d = torch.float64
+    t = lambda a: torch.as_tensor(a).to(d)
+    H, nq, nkv, hd = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    G = nq // nkv
+
+    def norm(x, g):
+        return F.rms_norm(x, (x.shape[-1],), weight=t(g), eps=cfg.rms_eps)
+
+    def rope(x, pos):
+        half = hd // 2
+        inv = cfg.rope_theta ** (-(torch.arange(half, dtype=d) * 2.0) / hd)
+        ang = pos.to(d)[..., None] * inv
+        z = torch.complex(x[..., :half], x[..., half:]) * torch.polar(torch.ones_like(ang), ang)
+        return torch.cat([z.real, z.imag], dim=-1)
+
+    B = len(n_real)
+    L0 = W["layers"][0]
+    logits = torch.empty(B, K, cfg.vocab, dtype=d)
+    T_max = int(max(n_real)) + K - 1
+    k_rows = torch.full((4, B, T_max, nkv, hd), float("nan"), dtype=d)
+    v_rows = torch.full((4, B, T_max, nkv, hd), float("nan"), dtype=d)
+    for b in range(B):
+        n = int(n_real[b])
+        T = n + K - 1
+        rows_e = [t(W["embed"][int(tokens[b, i])]) for i in range(n)] + [t(W["emb_mask"])] * (K - 1)
+        rows_h = [F.linear(t(th[b, i]), t(W["fc"])) for i in range(n)] + [t(W["h_shared"])] * (K - 1)
+        x = torch.cat([norm(torch.stack(rows_e), L0["norm_e"]), norm(torch.stack(rows_h), L0["norm_h"])], -1)
+        r = torch.stack(rows_h).clone()
+        S = int(seq_lens[b])
+        pos = int(positions[b]) + torch.arange(T)
+        for li, Lw in enumerate(W["layers"]):
+            if li > 0:
+                x = norm(r, Lw["attn_norm"])
+            qkv = F.linear(x, t(Lw["w_qkv"]))
+            q = rope(qkv[:, : nq * hd].reshape(T, nq, hd), pos[:, None])
+            k = rope(qkv[:, nq * hd:(nq + nkv) * hd].reshape(T, nkv, hd), pos[:, None])
+            v = qkv[:, (nq + nkv) * hd:].reshape(T, nkv, hd)
+            k_rows[li, b, :T], v_rows[li, b, :T] = k, v
+            ks = [t(kc[li, int(page_table[b, e // 16]), :, e % 16, :]) for e in range(S)]
+            vs = [t(vc[li, int(page_table[b, e // 16]), :, e % 16, :]) for e in range(S)]
+            k_all = torch.cat([torch.stack(ks), k]) if S else k
+            v_all = torch.cat([torch.stack(vs), v]) if S else v
+            mask = torch.arange(S + T)[None, :] <= (S + torch.arange(T))[:, None]
+            a = F.scaled_dot_product_attention(
+                q.permute(1, 0, 2)[None], k_all.permute(1, 0, 2).repeat_interleave(G, 0)[None],
+                v_all.permute(1, 0, 2).repeat_interleave(G, 0)[None], attn_mask=mask)
+            r = r + F.linear(a[0].permute(1, 0, 2).reshape(T, nq * hd), t(Lw["w_o"]))
+            x = norm(r, Lw["mlp_norm"])
+            r = r + F.linear(F.silu(F.linear(x, t(Lw["w_gate"]))) * F.linear(x, t(Lw["w_up"])), t(Lw["w_down"]))
+        logits[b] = F.linear(norm(r[n - 1:], W["final_norm"]), t(W["lm_head"]))
+    return dict(logits=logits.numpy(), k_new=k_rows.numpy(), v_new=v_rows.numpy())
+
+
+def _refeed_case(K, n_real, seed=14):
+    B = len(n_real)
+    n_max = max(n_real)
+    wl = synth.Workload("pin-refeed", TINY, B, K, (10, 40), (0.7, 0.7), seed)
+    W = synth.make_weights(TINY, seed)
+    inp = synth.make_step_inputs(wl, K=n_max + K)      # pages for the real rows and the placeholders
+    rng = np.random.default_rng(seed)
+    tokens = rng.integers(0, TINY.vocab, size=(B, n_max))
+    th = torch.randn(B, n_max, 3 * TINY.hidden, generator=torch.Generator().manual_seed(seed), dtype=torch.float64)
+    return W, inp, tokens, np.asarray(n_real), th
+
+
+def _run_refeed(W, inp, tokens, n_real, th, K):
+    return oracle.draft_pass_refeed(TINY, synth.weights_to_numpy(W), tokens, n_real, th.numpy(),
+                                    inp.positions.numpy(), inp.seq_lens.numpy(), inp.page_table.numpy(),
+                                    inp.k_cache.double().numpy(), inp.v_cache.double().numpy(), K)
+
+
+def test_refeed_matches_independent_torch_restatement():
+    K = 3
+    W, inp, tokens, n_real, th = _refeed_case(K, [3, 1, 4])
+    out = _run_refeed(W, inp, tokens, n_real, th, K)
+    ref = _torch_refeed(W, tokens, n_real, th.numpy(), inp.positions.numpy(), inp.seq_lens.numpy(),
+                        inp.page_table.numpy(), inp.k_cache.double().numpy(), inp.v_cache.double().numpy(), K)
+    np.testing.assert_allclose(out["logits"], ref["logits"], rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(out["k_new"], ref["k_new"], rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(out["v_new"], ref["v_new"], rtol=1e-10, atol=1e-10)
+    assert np.isnan(out["k_new"][:, 1, 1 + K - 1:]).all() and not np.isnan(out["k_new"][:, 2]).any()
+
+
+def test_refeed_with_one_real_row_is_the_parallel_pass():
+    K = 4
+    W, inp, tokens, n_real, th = _refeed_case(K, [1, 1])
+    out = _run_refeed(W, inp, tokens, n_real, th, K)
+    par = oracle.draft_pass(TINY, synth.weights_to_numpy(W), tokens[:, 0], th[:, 0].numpy(), inp.positions.numpy(),
+                            inp.seq_lens.numpy(), inp.page_table.numpy(), inp.k_cache.double().numpy(),
+                            inp.v_cache.double().numpy(), K)
+    np.testing.assert_allclose(out["logits"], par["logits"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out["k_new"], par["k_new"], rtol=1e-12, atol=1e-12)
+
+
+def test_refeed_real_rows_are_causal_and_placeholders_see_them():
+    K = 3
+    W, inp, tokens, n_real, th = _refeed_case(K, [3, 2])
+    base = _run_refeed(W, inp, tokens, n_real, th, K)
+    # another first real token moves every draft; another last real token
+    # moves the drafts but not the first real row's cache rows
+    t2 = tokens.copy()
+    t2[:, 0] = (t2[:, 0] + 1) % TINY.vocab
+    moved = _run_refeed(W, inp, t2, n_real, th, K)
+    assert (np.abs(moved["logits"] - base["logits"]).max(axis=-1) > 1e-6).all()
+    t3 = tokens.copy()
+    t3[0, 2] = (t3[0, 2] + 1) % TINY.vocab
+    moved3 = _run_refeed(W, inp, t3, n_real, th, K)
+    np.testing.assert_array_equal(moved3["k_new"][:, 0, :2], base["k_new"][:, 0, :2])
+    np.testing.assert_array_equal(moved3["logits"][1], base["logits"][1])     # other request untouched
+
+
+def test_refeed_rebuild_against_explicit_slot_lists():
+    rng = np.random.default_rng(15)
+    P = 16
+    for trial in range(200):
+        B, K = 4, int(rng.integers(1, 12))
+        S = rng.integers(0, 100, size=B)
+        Q = S + rng.integers(0, 30, size=B)
+        n = rng.integers(1, K + 2, size=B)
+        max_pages = int(np.ceil((S.max() + 4 * K + 2) / P)) + int(rng.integers(0, 2))
+        num_pages = B * max_pages + 3
+        pt = rng.permutation(num_pages)[: B * max_pages].reshape(B, max_pages)
+        a = rng.integers(0, K + 1, size=B)
+        out = oracle.rebuild_metadata_refeed(a, K, n, S, Q, pt, num_pages, P)
+        for b in range(B):
+            slots = np.concatenate([p * P + np.arange(P) for p in pt[b]])
+            assert out["status"][b] == oracle.REQ_OK
+            assert out["seq_lens"][b] == S[b] + n[b] and out["positions"][b] == Q[b] + n[b]
+            assert out["n_real"][b] == a[b] + 1
+            m = a[b] + K
+            np.testing.assert_array_equal(out["slot_mapping"][b, :m], slots[S[b] + n[b]: S[b] + n[b] + m])
+            assert (out["slot_mapping"][b, m:] == -1).all()
+            np.testing.assert_array_equal(out["rollback_slots"][b, :K - 1], slots[S[b] + n[b]: S[b] + n[b] + K - 1])
+            assert (out["rollback_slots"][b, K - 1:] == -1).all()
+
+
+def test_refeed_rebuild_status_cases():
+    P, K = 16, 3
+    pt = np.array([[0, 1], [2, 3], [4, -1], [5, 6]])
+    S = np.array([20, 5, 10, -2])
+    Q = np.array([30, 30, 12, 4])
+    n = np.array([4, 1, 2, 1])
+    a = np.array([3, 0, 3, 0])
+    out = oracle.rebuild_metadata_refeed(a, K, n, S, Q, pt, num_pages=7, page_size=P)
+    # 0: S'=24, next rows 4 + 2 = 6 -> 30 <= 32 fits; 1: fits; 2: S'=12, 4 + 2 rows reach entry 17 -> page -1
+    np.testing.assert_array_equal(out["status"], [oracle.REQ_OK, oracle.REQ_OK, oracle.REQ_BAD_PAGE,
+                                                  oracle.REQ_BAD_INPUT])
+    out2 = oracle.rebuild_metadata_refeed(np.array([3]), K, np.array([4]), np.array([25]), np.array([30]),
+                                          pt[:1], 7, P)
+    assert out2["status"][0] == oracle.REQ_CAPACITY                   # 29 + 4 + 2 = 35 > 32
+    np.testing.assert_array_equal(out["n_real"][2:], n[2:])
+
+
 # --------------------------------------------------------------- verify / rebuild
 
 def _brute_accept(d, g):
