@@ -190,6 +190,31 @@ int pe_draft_sequential(pe_handle* h, int32_t B, int32_t K,
                         void* k_cache, void* v_cache,
                         int32_t* drafts, float* logits_dbg, int32_t* status, void* stream);
 
+/* The parallel draft pass with the tokens of the last verify re-fed as real
+ * rows (the alternative to the single-real-row bookkeeping; the pages leave
+ * the drafter's cache bookkeeping open). Request b brings n_b = n_real[b]
+ * real rows - tokens[b, i] with their target hidden states target_hidden[b, i]
+ * (each row: token embedding and FC-fused hidden state, the pages'
+ * position-1 input) - ahead of the K-1 placeholder rows. Real row i sits at
+ * position Q_b + i and entry S_b + i; placeholder j (1..K-1) at position
+ * Q_b + n_b - 1 + j and entry S_b + n_b - 1 + j; every row attends causally.
+ * drafts[b, 0] is the argmax of the last real row, drafts[b, j] that of
+ * placeholder j.
+ *  tokens        [B, n_max] int32 (entries past n_b unused), n_real [B] int32 in 1..n_max
+ *  target_hidden [B, n_max, 3H] bf16 (rows past n_b unused)
+ *  1 <= n_max <= k_max. Other arguments, outputs and errors as for pe_draft;
+ *  every entry S_b .. S_b+n_max+K-2 is validated (PE_REQ_BAD_INPUT also for
+ *  n_b out of range or a bad token).
+ * Runs as two passes: the layers over real rows 0..n_b-2 (which writes their
+ * cache rows; padded to n_max-1 rows, the padding writes nothing), then the
+ * parallel pass whose row 0 is the last real row. The result is that of one
+ * joint pass, because attention is the only place where rows meet. */
+int pe_draft_refeed(pe_handle* h, int32_t B, int32_t K, int32_t n_max, const int32_t* tokens,
+                    const int32_t* n_real, const void* target_hidden, const int32_t* positions,
+                    const int32_t* seq_lens, const int32_t* page_table, int32_t max_pages, int32_t num_pages,
+                    void* k_cache, void* v_cache, int32_t* drafts, float* logits_dbg, int32_t* status,
+                    void* stream);
+
 /* Greedy verification + batch-metadata rebuild + KV rollback (one kernel).
  * h may be NULL (the kernel needs no drafter state).
  *
@@ -217,6 +242,25 @@ int pe_verify_rebuild(pe_handle* h, int32_t B, int32_t K,
                       int32_t* accepted, int32_t* bonus, int32_t* emitted,
                       int32_t* slot_mapping, int32_t* rollback_slots,
                       int32_t* status, void* stream);
+
+/* Verify + rebuild after a pe_draft_refeed pass: the same greedy acceptance,
+ * bonus and emitted tokens; the n_b real rows stay committed and the K-1
+ * placeholder rows are rolled back:
+ *  n_real, positions, seq_lens [B] in; n_real_out = a_b + 1,
+ *  positions_out = Q_b + n_b, seq_lens_out = S_b + n_b (may alias the inputs)
+ *  slot_mapping  [B, 2K] OUT  slots of the next pass's entries
+ *                 S_b' .. S_b'+n_b'+K-2, then -1
+ *  rollback_slots [B, K] OUT  slots of entries S_b+n_b .. S_b+n_b+K-2, then -1
+ *  status: as pe_verify_rebuild (PE_REQ_BAD_INPUT also for n_b outside
+ *  1..K+1); a failed request keeps its metadata and n_real.
+ * The next step re-feeds emitted[b, 0..a_b] with their target hidden states.
+ * Requires 1 <= K <= 16. */
+int pe_verify_rebuild_refeed(pe_handle* h, int32_t B, int32_t K, const int32_t* drafts,
+                             const int32_t* target_tokens, const int32_t* page_table, int32_t max_pages,
+                             int32_t num_pages, const int32_t* n_real, const int32_t* positions,
+                             const int32_t* seq_lens, int32_t* n_real_out, int32_t* positions_out,
+                             int32_t* seq_lens_out, int32_t* accepted, int32_t* bonus, int32_t* emitted,
+                             int32_t* slot_mapping, int32_t* rollback_slots, int32_t* status, void* stream);
 
 /* The draft pass's tcgen05 GEMM engine on its own (plain store epilogue):
  *   y[n, m] = sum_k w[m, k] * x[n, k]

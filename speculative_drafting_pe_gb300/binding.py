@@ -25,7 +25,7 @@ EXPORTS = (
     "pe_profile_start", "pe_profile_stop", "pe_kernel_name",
     "pe_step_graph_create", "pe_step_graph_launch", "pe_step_graph_launch_count", "pe_step_graph_destroy",
     "pe_linear_noalloc", "pe_test_stall_chain", "pe_draft_sequential", "pe_step_graph_create_ex",
-    "pe_init_drafter_fp8", "pe_linear_fp8",
+    "pe_init_drafter_fp8", "pe_linear_fp8", "pe_draft_refeed", "pe_verify_rebuild_refeed",
 )
 KERNEL_KINDS = ("fc", "row_build", "rmsnorm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "argmax",
                 "layer_chain")
@@ -99,6 +99,12 @@ def load():
     lib.pe_linear_fp8.restype = ctypes.c_int
     lib.pe_draft.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.pe_draft.restype = ctypes.c_int
+    lib.pe_draft_refeed.argtypes = [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp,
+                                    _vp, _vp, _vp, _vp]
+    lib.pe_draft_refeed.restype = ctypes.c_int
+    lib.pe_verify_rebuild_refeed.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
+                                             _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.pe_verify_rebuild_refeed.restype = ctypes.c_int
     lib.pe_draft_sequential.argtypes = lib.pe_draft.argtypes
     lib.pe_draft_sequential.restype = ctypes.c_int
     lib.pe_verify_rebuild.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -242,6 +248,31 @@ class Drafter:
         _check(fn(self._h, B, K, _p(last_token), _p(target_hidden), _p(positions), _p(seq_lens),
                   _p(page_table), page_table.shape[1], num_pages, _p(k_cache), _p(v_cache),
                   _p(drafts), _p(logits), _p(status), _stream_ptr(stream)))
+        return drafts, status
+
+    def draft_refeed(self, tokens, n_real, target_hidden, positions, seq_lens, page_table, num_pages, k_cache,
+                     v_cache, K, drafts=None, status=None, logits=None, stream=None):
+        """Enqueue a draft pass with re-fed real rows: tokens [B, n_max]
+        int32, n_real [B] int32, target_hidden [B, n_max, 3H]. Returns
+        (drafts [B, K] int32, status [B] int32)."""
+        B, n_max = tokens.shape
+        dev = self.device
+        for name, t in (("tokens", tokens), ("n_real", n_real), ("positions", positions), ("seq_lens", seq_lens),
+                        ("page_table", page_table)):
+            _need(t, torch.int32, dev, name)
+        _need(target_hidden, self.dtype, dev, "target_hidden")
+        if tuple(target_hidden.shape[:2]) != (B, n_max):
+            raise ValueError("target_hidden must be [B, n_max, 3H]")
+        if drafts is None:
+            drafts = torch.empty(B, K, dtype=torch.int32, device=dev)
+        if status is None:
+            status = torch.empty(B, dtype=torch.int32, device=dev)
+        if logits is not None:
+            _need(logits, torch.float32, dev, "logits")
+        _check(load().pe_draft_refeed(self._h, B, K, n_max, _p(tokens), _p(n_real), _p(target_hidden),
+                                      _p(positions), _p(seq_lens), _p(page_table), page_table.shape[1], num_pages,
+                                      _p(k_cache), _p(v_cache), _p(drafts), _p(logits), _p(status),
+                                      _stream_ptr(stream)))
         return drafts, status
 
     def profile_start(self, kind, max_launches):
@@ -419,4 +450,25 @@ def verify_rebuild(drafts, target_tokens, page_table, num_pages, positions, seq_
                                  _p(buf("slot_mapping", B, K)), _p(buf("rollback_slots", B, K)),
                                  _p(buf("status", B)), _stream_ptr(stream)))
     o["emitted"] = em
+    return o
+
+
+def verify_rebuild_refeed(drafts, target_tokens, page_table, num_pages, n_real, positions, seq_lens, stream=None):
+    """Greedy verify + rebuild after a re-fed pass. Returns a dict of int32
+    device tensors: accepted, bonus, emitted, n_real, positions, seq_lens,
+    slot_mapping [B, 2K], rollback_slots [B, K], status."""
+    lib = load()
+    B, K = drafts.shape
+    dev = drafts.device
+    for name, t in (("drafts", drafts), ("target_tokens", target_tokens), ("page_table", page_table),
+                    ("n_real", n_real), ("positions", positions), ("seq_lens", seq_lens)):
+        _need(t, torch.int32, dev, name)
+    e = lambda *s: torch.empty(*s, dtype=torch.int32, device=dev)
+    o = dict(accepted=e(B), bonus=e(B), emitted=e(B, K + 1), n_real=e(B), positions=e(B), seq_lens=e(B),
+             slot_mapping=e(B, 2 * K), rollback_slots=e(B, K), status=e(B))
+    _check(lib.pe_verify_rebuild_refeed(None, B, K, _p(drafts), _p(target_tokens), _p(page_table),
+                                        page_table.shape[1], num_pages, _p(n_real), _p(positions), _p(seq_lens),
+                                        _p(o["n_real"]), _p(o["positions"]), _p(o["seq_lens"]), _p(o["accepted"]),
+                                        _p(o["bonus"]), _p(o["emitted"]), _p(o["slot_mapping"]),
+                                        _p(o["rollback_slots"]), _p(o["status"]), _stream_ptr(stream)))
     return o

@@ -174,7 +174,23 @@ struct RowBuildParams {
     // S_b that the whole step writes, validated against the page table.
     int j0, k_check;
     int status_in;             // 1: status[b] was set by an earlier pass; read it, write nothing
-    int32_t* seq_eff;          // OUT [B] or null: S_b + j0 (the attention's committed-entry count)
+    int32_t* seq_eff;          // OUT [B] or null: S_b + j0_b (the attention's committed-entry count)
+    // Rows with their own inputs and per-request offsets (re-fed real rows).
+    // Rows j < n_lead take token last_token[b * tok_stride + (o_b + j) * tok_jstride]
+    // and hidden h[b * hid_bstride + (o_b + j) * hid_stride], o_b = row_off[b] + off_add
+    // (0 without row_off); rows past them are placeholders. The pass's rows
+    // sit at entry S_b + j0 + o_b + j. Rows j >= row_lim[b] + lim_add (when
+    // row_lim is set) are padding: no cache write, outputs unused.
+    int n_lead;
+    int tok_jstride, hid_bstride;
+    const int32_t* row_off;
+    int off_add;
+    const int32_t* row_lim;
+    int lim_add;
+    // re-fed real rows: status also checks n_real[b] in [1, n_max] and the
+    // tokens last_token[b * tok_stride + i], i < n_real[b]
+    const int32_t* n_real;
+    int n_max;
     const void* embed;         // [V, H]
     const void* emb_mask;      // [H]
     const void* h_shared;      // [H]
@@ -270,6 +286,14 @@ int launch_verify_rebuild(int B, int K, const int32_t* drafts, const int32_t* ta
                           const int32_t* seq_lens, int32_t* positions_out, int32_t* seq_lens_out,
                           int32_t* accepted, int32_t* bonus, int32_t* emitted, int32_t* slot_mapping,
                           int32_t* rollback, int32_t* status, cudaStream_t s);
+
+// the same for re-fed real rows: n_real in/out, slot_mapping [B, 2K], rollback [B, K]
+int launch_verify_rebuild_refeed(int B, int K, const int32_t* drafts, const int32_t* target,
+                                 const int32_t* page_table, int max_pages, int num_pages, int page_size,
+                                 const int32_t* n_real, const int32_t* positions, const int32_t* seq_lens,
+                                 int32_t* n_real_out, int32_t* positions_out, int32_t* seq_lens_out,
+                                 int32_t* accepted, int32_t* bonus, int32_t* emitted, int32_t* slot_mapping,
+                                 int32_t* rollback, int32_t* status, cudaStream_t s);
 
 // Launch helper: every kernel goes through cudaLaunchKernelEx so that the
 // programmatic-dependent-launch attribute can be set uniformly.

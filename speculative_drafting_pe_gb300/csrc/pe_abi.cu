@@ -33,7 +33,7 @@ struct pe_handle {
     size_t elem = 2;
     bool pdl = false;
     // workspaces (device)
-    float* h = nullptr;           // [max_batch, H]
+    float* h = nullptr;           // [max_rows, H] FC outputs (one row per request, or per re-fed real row)
     float* resid = nullptr;       // [max_rows, H]
     void* u = nullptr;            // [max_rows, 2H]
     void* xn = nullptr;           // [max_rows, H] gain * residual (folded RMSNorm input)
@@ -403,7 +403,7 @@ int init_drafter(const pe_config* cfg, const pe_weights* weights, const pe_weigh
     }
 
     int a = PE_OK;
-    if (a == PE_OK) a = dev_alloc(&h->h, static_cast<size_t>(max_batch) * H * 4);
+    if (a == PE_OK) a = dev_alloc(&h->h, R * H * 4);
     if (a == PE_OK) a = dev_alloc(&h->resid, R * H * 4);
     if (a == PE_OK) a = dev_alloc(&h->u, R * 2 * H * E);
     if (a == PE_OK) a = dev_alloc(&h->xn, R * H * E);
@@ -545,6 +545,18 @@ struct PassSpec {
     int drafts_stride = 0;
     float* logits = nullptr;       // optional: pass row n (= b * Kp + j) at logits + n * logits_ld
     int logits_ld = 0;
+    // re-fed real rows (see RowBuildParams): rows j < n_lead take their own
+    // token and FC output, at a per-request row offset; padding rows
+    int n_lead = 1;
+    int tok_jstride = 0;
+    int fc_rows = 1;               // FC rows per request (hidden rows read at b * fc_rows + o_b + j)
+    const int32_t* row_off = nullptr;
+    int off_add = 0;
+    const int32_t* row_lim = nullptr;
+    int lim_add = 0;
+    const int32_t* n_real = nullptr;
+    int n_max = 0;
+    bool head = true;              // run the LM head and the argmax (off: the rows only feed the cache)
 };
 
 int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, const int32_t* positions,
@@ -561,7 +573,8 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
     int rc;
 
     // GEMM plans (bn depends only on the row count)
-    const GemmPlan p_fc = plan_gemm(H, B, 3 * H, EPI_STORE, eb, h->num_sms, true, h->w8);
+    const int fc_n = B * ps.fc_rows;
+    const GemmPlan p_fc = plan_gemm(H, fc_n, 3 * H, EPI_STORE, eb, h->num_sms, true, h->w8);
     const GemmPlan p_qkv0 = plan_gemm(qkv_rows, R, 2 * H, EPI_QKV, eb, h->num_sms, true, h->w8);
     const GemmPlan p_qkv = plan_gemm(qkv_rows, R, H, EPI_QKV, eb, h->num_sms, true, h->w8);
     const GemmPlan p_o = plan_gemm(H, R, qd, EPI_RESID, eb, h->num_sms, true, h->w8);
@@ -582,7 +595,7 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
     // the map (QKV, O and down may take narrower tiles than gate/up and the LM head)
     CUtensorMap tm_th, tm_u, tm_xq, tm_xn, tm_attn, tm_act;
     if (p_qkv0.bn != p_qkv.bn || p_lm.bn != p_gu.bn) { set_error("GEMM token tiles disagree"); return PE_ERR_UNSUPPORTED; }
-    if (ps.run_fc && (rc = act_map(h, &tm_th, target_hidden, B, 3 * H, p_fc.bn)) != PE_OK) return rc;
+    if (ps.run_fc && (rc = act_map(h, &tm_th, target_hidden, fc_n, 3 * H, p_fc.bn)) != PE_OK) return rc;
     if ((rc = act_map(h, &tm_u, h->u, R, 2 * H, p_qkv.bn)) != PE_OK) return rc;      // layer 0's QKV
     if ((rc = act_map(h, &tm_xq, h->xn, R, H, p_qkv.bn)) != PE_OK) return rc;       // QKV of layers 1-3
     if ((rc = act_map(h, &tm_xn, h->xn, R, H, p_gu.bn)) != PE_OK) return rc;        // gate/up, LM head
@@ -632,7 +645,7 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
     // a1: h = W_fc [h_lo; h_mid; h_hi] (the first pass of a step)
     if (ps.run_fc) {
         GemmParams p = base;
-        p.M = H; p.N = B; p.Kd = 3 * H;
+        p.M = H; p.N = fc_n; p.Kd = 3 * H;
         p.out_f32 = h->h; p.ld_out = H;
         p.w_scale = h->sc.fc;
         rc = run(PE_KERNEL_FC, [&] { return launch_gemm(dt, EPI_STORE, h->tm_fc, h->tm_fc, tm_th, p_fc, p, s, pdl); });
@@ -645,9 +658,14 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
         rp.max_pages = max_pages; rp.num_pages = num_pages; rp.page_size = c.page_size;
         rp.last_token = ps.tok; rp.tok_stride = ps.tok_stride;
         rp.positions = positions; rp.seq_lens = seq_lens; rp.page_table = page_table;
-        rp.h = ps.hid != nullptr ? ps.hid : h->h; rp.hid_stride = ps.hid != nullptr ? ps.hid_stride : H;
+        rp.h = ps.hid != nullptr ? ps.hid : h->h;
+        rp.hid_stride = H;
+        rp.hid_bstride = ps.hid != nullptr ? ps.hid_stride : ps.fc_rows * H;
+        rp.n_lead = ps.n_lead; rp.tok_jstride = ps.tok_jstride;
+        rp.row_off = ps.row_off; rp.off_add = ps.off_add; rp.row_lim = ps.row_lim; rp.lim_add = ps.lim_add;
+        rp.n_real = ps.n_real; rp.n_max = ps.n_max;
         rp.j0 = ps.j0; rp.k_check = ps.k_check; rp.status_in = ps.status_in ? 1 : 0;
-        rp.seq_eff = ps.j0 > 0 || ps.seq_eff_out ? h->seq_eff : nullptr;
+        rp.seq_eff = ps.j0 > 0 || ps.seq_eff_out || ps.row_off != nullptr ? h->seq_eff : nullptr;
         rp.embed = h->w.embed; rp.emb_mask = h->w.emb_mask; rp.h_shared = h->w.h_shared;
         rp.norm_e = h->w.layer[0].norm_e; rp.norm_h = h->w.layer[0].norm_h; rp.eps = c.rms_eps;
         rp.u = h->u; rp.resid = h->resid; rp.row_slot = h->row_slot; rp.rope_cs = h->rope_cs;
@@ -660,7 +678,7 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
         rp.piece_min_tiles = p_at.piece_min_tiles;
         if ((rc = run(PE_KERNEL_ROW_BUILD, [&] { return launch_row_build(dt, rp, s, pdl); })) != PE_OK) return rc;
     }
-    const int32_t* rp_seq = ps.j0 > 0 || ps.seq_eff_out ? h->seq_eff : seq_lens;
+    const int32_t* rp_seq = ps.j0 > 0 || ps.seq_eff_out || ps.row_off != nullptr ? h->seq_eff : seq_lens;
     const size_t layer_elems = static_cast<size_t>(num_pages) * nkv * c.page_size * hd;
     auto kcache = [&](int l) { return static_cast<char*>(k_cache) + l * layer_elems * h->elem; };
     auto vcache = [&](int l) { return static_cast<char*>(v_cache) + l * layer_elems * h->elem; };
@@ -707,7 +725,7 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
     };
     // O, gate/up, down of layer l and then the next layer's QKV (or the LM
     // head) as one persistent launch
-    const bool use_chain = h->chain && R <= kMaxChainBn;
+    const bool use_chain = h->chain && R <= kMaxChainBn && ps.head;
     auto launch_layer_chain = [&](int l) -> int {
         ChainParams cp{};
         cp.nphases = 4;
@@ -808,6 +826,7 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
             if (rc != PE_OK) return rc;
         }
     }
+    if (!ps.head) return PE_OK;
     // a7: final norm (folded), LM head + fused argmax (inside the last chain launch when chained)
     if (!use_chain) {
         GemmParams p = gp_lm();
@@ -900,6 +919,55 @@ int pe_draft_sequential(pe_handle* h, int32_t B, int32_t K, const int32_t* last_
     return PE_OK;
 }
 
+int pe_draft_refeed(pe_handle* h, int32_t B, int32_t K, int32_t n_max, const int32_t* tokens,
+                    const int32_t* n_real, const void* target_hidden, const int32_t* positions,
+                    const int32_t* seq_lens, const int32_t* page_table, int32_t max_pages, int32_t num_pages,
+                    void* k_cache, void* v_cache, int32_t* drafts, float* logits_dbg, int32_t* status,
+                    void* stream) {
+    int rc = check_draft_args(h, B, K, tokens, target_hidden, positions, seq_lens, page_table, max_pages, num_pages,
+                              k_cache, v_cache, drafts, status);
+    if (rc != PE_OK) return rc;
+    if (n_real == nullptr) { set_error("null n_real"); return PE_ERR_ARG; }
+    if (n_max < 1 || n_max > h->cfg.k_max) { set_error("n_max out of range 1..k_max"); return PE_ERR_ARG; }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    // Pass A: real rows 0 .. n_b-2 of every request (right-padded to n_max-1
+    // rows) through the layers, which writes their cache rows; no LM head.
+    // The FC runs here for all n_max hidden rows of every request.
+    // Pass B: the parallel pass with the last real row as row 0 and the K-1
+    // placeholders, at entry offset n_b - 1; it attends over pass A's rows.
+    PassSpec a;
+    a.B = B; a.Kp = n_max - 1; a.j0 = 0; a.k_check = n_max + K - 1;
+    a.run_fc = true; a.fc_rows = n_max;
+    a.tok = tokens; a.tok_stride = n_max; a.tok_jstride = 1;
+    a.n_lead = n_max - 1;
+    a.row_lim = n_real; a.lim_add = -1;
+    a.n_real = n_real; a.n_max = n_max;
+    a.seq_eff_out = true;
+    a.head = false;
+    if (n_max > 1) {
+        rc = enqueue_pass(h, a, target_hidden, positions, seq_lens, page_table, max_pages, num_pages, k_cache,
+                          v_cache, status, s, launches);
+        if (rc != PE_OK) return rc;
+    }
+    PassSpec b;
+    b.B = B; b.Kp = K; b.j0 = 0; b.k_check = n_max + K - 1;
+    b.run_fc = n_max == 1; b.fc_rows = n_max;
+    b.tok = tokens; b.tok_stride = n_max; b.tok_jstride = 1;
+    b.n_lead = 1;
+    b.row_off = n_real; b.off_add = -1;
+    b.n_real = n_real; b.n_max = n_max;
+    b.status_in = n_max > 1;
+    b.seq_eff_out = true;
+    b.drafts = drafts; b.drafts_stride = K;
+    b.logits = logits_dbg; b.logits_ld = h->cfg.vocab;
+    rc = enqueue_pass(h, b, target_hidden, positions, seq_lens, page_table, max_pages, num_pages, k_cache, v_cache,
+                      status, s, launches);
+    if (rc != PE_OK) return rc;
+    h->last_launches = launches;
+    return PE_OK;
+}
+
 int pe_profile_start(pe_handle* h, int32_t kernel_kind, int32_t max_launches) {
     if (h == nullptr || kernel_kind < 0 || kernel_kind >= PE_KERNEL_COUNT || max_launches < 1) {
         set_error("bad profiling arguments");
@@ -958,6 +1026,27 @@ int pe_verify_rebuild(pe_handle* h, int32_t B, int32_t K, const int32_t* drafts,
     return launch_verify_rebuild(B, K, drafts, target_tokens, page_table, max_pages, num_pages, 16, positions,
                                  seq_lens, positions_out, seq_lens_out, accepted, bonus, emitted, slot_mapping,
                                  rollback_slots, status, static_cast<cudaStream_t>(stream));
+}
+
+int pe_verify_rebuild_refeed(pe_handle* h, int32_t B, int32_t K, const int32_t* drafts,
+                             const int32_t* target_tokens, const int32_t* page_table, int32_t max_pages,
+                             int32_t num_pages, const int32_t* n_real, const int32_t* positions,
+                             const int32_t* seq_lens, int32_t* n_real_out, int32_t* positions_out,
+                             int32_t* seq_lens_out, int32_t* accepted, int32_t* bonus, int32_t* emitted,
+                             int32_t* slot_mapping, int32_t* rollback_slots, int32_t* status, void* stream) {
+    (void)h;
+    if (B < 1) { set_error("B must be >= 1"); return PE_ERR_ARG; }
+    if (K < 1 || K > 16) { set_error("K must be in 1..16"); return PE_ERR_ARG; }
+    if (max_pages < 1 || num_pages < 1) { set_error("max_pages and num_pages must be >= 1"); return PE_ERR_ARG; }
+    if (!drafts || !target_tokens || !page_table || !n_real || !positions || !seq_lens || !n_real_out ||
+        !positions_out || !seq_lens_out || !accepted || !bonus || !slot_mapping || !rollback_slots || !status) {
+        set_error("null tensor argument");
+        return PE_ERR_ARG;
+    }
+    return launch_verify_rebuild_refeed(B, K, drafts, target_tokens, page_table, max_pages, num_pages, 16, n_real,
+                                        positions, seq_lens, n_real_out, positions_out, seq_lens_out, accepted, bonus,
+                                        emitted, slot_mapping, rollback_slots, status,
+                                        static_cast<cudaStream_t>(stream));
 }
 
 int pe_linear_scratch(int32_t dtype, int32_t M, int32_t N, int32_t Kd, int64_t* ws_floats, int32_t* n_tickets) {

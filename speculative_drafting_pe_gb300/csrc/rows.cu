@@ -60,9 +60,19 @@ constexpr int kMaxG = 8;   // 4-element groups per thread: H <= 4 * 8 * 256
 // 0..S+k_check-1 (every entry the step writes).
 __device__ int request_status(const RowBuildParams& p, int b) {
     const int S = p.seq_lens[b];
-    const int tok = p.last_token[static_cast<size_t>(b) * p.tok_stride];
     const int Q = p.positions[b];
-    if (S < 0 || Q < 0 || tok < 0 || tok >= p.V) return PE_REQ_BAD_INPUT;
+    int n_tok = 1;
+    if (p.n_real != nullptr) {
+        n_tok = p.n_real[b];
+        if (n_tok < 1 || n_tok > p.n_max) return PE_REQ_BAD_INPUT;
+    }
+    if (S < 0 || Q < 0) return PE_REQ_BAD_INPUT;
+    int bad_tok = 0;
+    for (int i = threadIdx.x; i < n_tok; i += blockDim.x) {
+        const int tok = p.last_token[static_cast<size_t>(b) * p.tok_stride + static_cast<size_t>(i) * p.tok_jstride];
+        if (tok < 0 || tok >= p.V) bad_tok = 1;
+    }
+    if (__syncthreads_or(bad_tok)) return PE_REQ_BAD_INPUT;
     if (static_cast<long long>(S) + p.k_check > static_cast<long long>(p.max_pages) * p.page_size)
         return PE_REQ_CAPACITY;
     const int n_pages = (S + p.k_check + p.page_size - 1) / p.page_size;
@@ -92,7 +102,7 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
         if (g < ng) {
             ge[i] = load4(static_cast<const T*>(p.norm_e) + 4 * g);
             gh[i] = load4(static_cast<const T*>(p.norm_h) + 4 * g);
-            if (j > 0) {
+            if (j >= p.n_lead || p.row_lim != nullptr) {   // placeholder (or a padding row's stand-in)
                 ev[i] = load4(static_cast<const T*>(p.emb_mask) + 4 * g);
                 hv[i] = load4(static_cast<const T*>(p.h_shared) + 4 * g);
             }
@@ -102,8 +112,13 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
     pdl_wait();
     const int st = p.status_in ? p.status[b] : request_status(p, b);
     const bool ok = st == PE_REQ_OK;
+    // per-request row offset (re-fed rows), only for a request that passed
+    // the checks (its n_real is in range)
+    auto off_of = [&](int q) { return p.row_off != nullptr ? p.row_off[q] + p.off_add : 0; };
+    const int o_b = ok ? off_of(b) : 0;
+    const bool pad = ok && p.row_lim != nullptr && j >= p.row_lim[b] + p.lim_add;
     if (j == 0 && tid == 0 && !p.status_in) p.status[b] = st;
-    if (j == 0 && tid == 0 && p.seq_eff != nullptr) p.seq_eff[b] = p.seq_lens[b] + p.j0;
+    if (j == 0 && tid == 0 && p.seq_eff != nullptr) p.seq_eff[b] = p.seq_lens[b] + p.j0 + o_b;
     if (tid == 0) p.amax[r] = 0ull;
     if (r == 0 && p.order != nullptr) {
         // requests by decreasing length (ties by index, so a permutation):
@@ -131,8 +146,9 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
         __syncthreads();
         const long long cap = static_cast<long long>(p.max_pages) * p.page_size;
         for (int q = tid; q < p.B; q += blockDim.x) {
-            const int sq = p.seq_lens[q] + p.j0;
-            const bool fits = sq >= p.j0 && static_cast<long long>(sq) + p.K <= cap;
+            const int oq = p.row_off != nullptr ? max(0, min(p.n_max, off_of(q))) : 0;
+            const int sq = p.seq_lens[q] + p.j0 + oq;
+            const bool fits = sq >= p.j0 + oq && static_cast<long long>(sq) + p.K <= cap;
             const int tiles = fits ? (sq + p.K + kPieceTile - 1) / kPieceTile : 0;
             s_t[q] = tiles;
             atomicAdd(&s_total, tiles);
@@ -185,7 +201,8 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
             const int t = s_t[q];
             const int n = pieces_of(t);
             const int per_piece = s_sz[q];
-            const int len = t > 0 ? p.seq_lens[q] + p.j0 + p.K : 0;
+            const int oq = p.row_off != nullptr ? max(0, min(p.n_max, off_of(q))) : 0;
+            const int len = t > 0 ? p.seq_lens[q] + p.j0 + oq + p.K : 0;
             p.attn_plan[1 + q] = n;
             p.attn_plan[1 + p.B + q] = s_off[k];
             for (int i = 0; i < n; ++i) {
@@ -198,10 +215,12 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
             }
         }
     }
-    if (j == 0) {
+    if (j < p.n_lead && !pad) {
+        const size_t r_src = static_cast<size_t>(o_b + j);
         const T* emb = static_cast<const T*>(p.embed) +
-                       static_cast<size_t>(ok ? p.last_token[static_cast<size_t>(b) * p.tok_stride] : 0) * H;
-        const float* h0 = p.h + static_cast<size_t>(b) * p.hid_stride;
+                       static_cast<size_t>(ok ? p.last_token[static_cast<size_t>(b) * p.tok_stride + r_src * p.tok_jstride]
+                                              : 0) * H;
+        const float* h0 = p.h + static_cast<size_t>(b) * p.hid_bstride + r_src * p.hid_stride;
 #pragma unroll
         for (int i = 0; i < kMaxG; ++i) {
             const int g = tid + i * kRowThreads;
@@ -236,8 +255,8 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
 
     if (tid == 0) {
         int slot = -1;
-        if (ok) {
-            const int e = p.seq_lens[b] + p.j0 + j;
+        if (ok && !pad) {
+            const int e = p.seq_lens[b] + p.j0 + o_b + j;
             const int pg = p.page_table[static_cast<size_t>(b) * p.max_pages + e / p.page_size];
             slot = pg * p.page_size + e % p.page_size;
         }
@@ -246,7 +265,7 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
     // RoPE table for this row: angle = (Q_b + j) * inv_freq_i in double,
     // reduced to [-pi, pi] in double, then sin/cos in float.
     const int half = p.hd / 2;
-    const double pos = static_cast<double>(ok ? p.positions[b] + p.j0 + j : 0);
+    const double pos = static_cast<double>(ok ? p.positions[b] + p.j0 + o_b + j : 0);
     for (int i = tid; i < half; i += blockDim.x) {
         const double a = pos * p.inv_freq[i];
         const double two_pi = 6.283185307179586476925286766559;

@@ -206,6 +206,22 @@ def make_step_inputs(wl, device="cpu", seed=None, B=None, K=None):
                       num_pages, k_cache, v_cache, alpha, K)
 
 
+def make_refeed_inputs(wl, n_max, device="cpu", seed=None):
+    """Re-fed real rows for a workload: n_real [B] uniform in 1..n_max,
+    tokens [B, n_max] uniform ids and target hidden states [B, n_max, 3H]
+    ~ N(0, 1) (entries past n_real[b] are drawn too and left unused).
+    Pair with make_step_inputs(wl, K=wl.K + n_max) so that the page tables
+    cover every entry the pass writes."""
+    shape = wl.shape
+    seed = wl.seed if seed is None else seed
+    rng = _np_rng(seed + 505)
+    n_real = rng.integers(1, n_max + 1, size=wl.B).astype(np.int32)
+    tokens = rng.integers(0, shape.vocab, size=(wl.B, n_max)).astype(np.int32)
+    g = _torch_gen(seed + 606, device)
+    th = torch.randn(wl.B, n_max, 3 * shape.hidden, generator=g, device=device, dtype=torch.float32)
+    return (torch.as_tensor(tokens).to(device), torch.as_tensor(n_real).to(device), th.to(shape.torch_dtype))
+
+
 def plant_targets(drafts, alpha, vocab, seed):
     """Target argmax tokens g [B, K+1] that agree with `drafts` [B, K]
     independently per position with probability alpha[b]; g[:, K] uniform."""
