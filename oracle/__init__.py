@@ -25,6 +25,7 @@ from .drafter import (  # noqa: F401
     top2_gap,
 )
 from .fp8 import e4m3_decode, dequant_rows, dequant_weights, E4M3_MAX  # noqa: F401
+from .sampling import softmax_t, sample_inverse_cdf, sample_drafts, verify_stochastic  # noqa: F401
 from .verify import (  # noqa: F401
     accept_length,
     verify,

@@ -686,6 +686,97 @@ def test_refeed_rebuild_status_cases():
     np.testing.assert_array_equal(out["n_real"][2:], n[2:])
 
 
+# --------------------------------------------------------------- sampling and stochastic acceptance
+
+def test_inverse_cdf_on_a_grid_of_uniforms():
+    w = np.array([0.2, 0.0, 0.5, 0.3])
+    for u, want in [(0.0, 0), (0.1999, 0), (0.2001, 2), (0.6999, 2), (0.7001, 3), (0.9999, 3)]:
+        i, m = oracle.sample_inverse_cdf(w, u)
+        assert i == want, (u, i)
+        assert m >= 0.0
+    i, m = oracle.sample_inverse_cdf(w * 7.0, 0.45)          # weights need not be normalised
+    assert i == 2 and abs(m - 0.25) < 1e-12                  # 0.45 is 0.25 from both 0.2 and 0.7
+
+
+def test_sampled_drafts_follow_the_tempered_softmax():
+    rng = np.random.default_rng(16)
+    logits = rng.normal(size=(1, 1, 6)) * 2.0
+    T = 0.7
+    n = 100_000
+    u = rng.random(n)
+    d = np.array([oracle.sample_inverse_cdf(oracle.softmax_t(logits[0, 0], T), x)[0] for x in u])
+    p = oracle.softmax_t(logits[0, 0], T)
+    freq = np.bincount(d, minlength=6) / n
+    assert (np.abs(freq - p) < 4 * np.sqrt(p * (1 - p) / n) + 1e-12).all()
+    ref = torch.softmax(torch.tensor(logits[0, 0]) / T, dim=0).numpy()
+    np.testing.assert_allclose(p, ref, rtol=1e-13)
+
+
+def _spec_case(rng, K, V, B):
+    dl = rng.normal(size=(B, K, V)) * 1.5
+    tl = rng.normal(size=(B, K + 1, V)) * 1.5
+    return dl, tl
+
+
+def test_speculative_sampling_emits_the_target_distribution():
+    # The first emitted token (the accepted draft d_0 or the draw at the
+    # first rejection) is distributed as p_0, whatever q_0 is; the acceptance
+    # rate of position 0 is sum_x min(p_0(x), q_0(x)).
+    rng = np.random.default_rng(17)
+    K, V, n = 3, 6, 100_000
+    dl, tl = _spec_case(rng, K, V, 1)
+    T = 0.9
+    dl_b, tl_b = np.repeat(dl, n, 0), np.repeat(tl, n, 0)
+    d, _ = oracle.sample_drafts(dl_b, T, rng.random((n, K)))
+    out = oracle.verify_stochastic(d, dl_b, tl_b, T, rng.random((n, K)), rng.random(n))
+    first = out["emitted"][:, 0]
+    p0 = oracle.softmax_t(tl[0, 0], T)
+    q0 = oracle.softmax_t(dl[0, 0], T)
+    freq = np.bincount(first, minlength=V) / n
+    assert (np.abs(freq - p0) < 4 * np.sqrt(p0 * (1 - p0) / n) + 1e-12).all(), (freq, p0)
+    acc = (out["accepted"] >= 1).mean()
+    want = np.minimum(p0, q0).sum()
+    assert abs(acc - want) < 4 * np.sqrt(want * (1 - want) / n)
+    assert ((out["accepted"] >= 0) & (out["accepted"] <= K)).all()
+
+
+def test_stochastic_acceptance_with_q_equal_p_accepts_everything():
+    rng = np.random.default_rng(18)
+    K, V, B = 4, 9, 500
+    dl, _ = _spec_case(rng, K, V, B)
+    tl = np.concatenate([dl, rng.normal(size=(B, 1, V))], axis=1)
+    d, _ = oracle.sample_drafts(dl, 1.3, rng.random((B, K)))
+    out = oracle.verify_stochastic(d, dl, tl, 1.3, rng.random((B, K)), rng.random(B))
+    assert (out["accepted"] == K).all()
+    np.testing.assert_array_equal(out["emitted"][:, :K], d)
+
+
+def test_stochastic_acceptance_at_low_temperature_is_greedy_acceptance():
+    # T -> 0: every softmax becomes the one-hot of its argmax, the sampled
+    # drafts are the argmax drafts and the rule reduces to the greedy one:
+    # longest prefix with d == g, then the target's argmax token.
+    rng = np.random.default_rng(19)
+    K, V, B = 5, 40, 300
+    dl, tl = _spec_case(rng, K, V, B)
+    # every row's argmax leads its runner-up by at least 1 (one-hot at T = 1e-3)
+    for arr in (dl, tl):
+        flat = arr.reshape(-1, V)
+        flat[np.arange(len(flat)), flat.argmax(-1)] += 1.0
+    agree = rng.random((B, K)) < 0.6                          # plant agreement on the argmax
+    for b in range(B):
+        for j in range(K):
+            if agree[b, j]:
+                tl[b, j, np.argmax(dl[b, j])] = tl[b, j].max() + 1.0
+    T = 1e-3
+    d, _ = oracle.sample_drafts(dl, T, rng.random((B, K)))
+    np.testing.assert_array_equal(d, dl.argmax(-1))
+    out = oracle.verify_stochastic(d, dl, tl, T, rng.random((B, K)), rng.random(B))
+    g = tl.argmax(-1)
+    a, bonus = oracle.verify(d, g)
+    np.testing.assert_array_equal(out["accepted"], a)
+    np.testing.assert_array_equal(out["final"], bonus)
+
+
 # --------------------------------------------------------------- verify / rebuild
 
 def _brute_accept(d, g):
