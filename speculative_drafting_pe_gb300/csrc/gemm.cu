@@ -25,15 +25,16 @@ namespace pe {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kThreadsW8 = 320;              // + warps 6..9: FP8 -> bf16 weight converters
+constexpr int kConvThreads = 64;             // warps 6..7: FP8 -> bf16 weight converters
+constexpr int kThreadsW8 = kThreads + kConvThreads;
 constexpr int kMaxClusterSplits = 8;         // cluster split-K: at most 8 CTAs per tile
-constexpr int kConvStages = 2;               // bf16 copies of FP8 weight stages (W8)
+constexpr int kConvStages = 2;               // most bf16 copies of FP8 weight stages (W8; plan: 1 or 2)
 constexpr uint32_t kConvBytes = 2 * kABytes; // 128 rows x 128 k as two 64-k SW128 tiles
 
-__host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn, int inv_floats, bool w8) {
+__host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn, int inv_floats, bool w8, int cstages) {
     const size_t b_stage = static_cast<size_t>(bn) * kRowBytes * (w8 ? 2 : 1);
     size_t off = static_cast<size_t>(stages) * (kABytes + b_stage);
-    if (w8) off += static_cast<size_t>(kConvStages) * kConvBytes;
+    if (w8) off += static_cast<size_t>(cstages) * kConvBytes;
     off += static_cast<size_t>(2 * stages + 4 + 2 * kConvStages) * 8;   // mbarriers
     off += 16;                                        // TMEM base + flags
     off = (off + 15) & ~static_cast<size_t>(15);
@@ -64,12 +65,11 @@ __device__ __forceinline__ void scale_row(float (&v)[kChunk], float s) {
     }
 }
 
-// One FP8 weight stage (128 rows x 128 E4M3 codes, 128-byte swizzle) widened
-// to bf16 as two 64-k tiles in the same swizzle: the 16-byte chunk c of row r
-// sits at r*128 + ((c ^ (r & 7)) << 4) in every tile. Thread t (0..127) owns
-// row t. E4M3 -> bf16 is exact (every E4M3 value is a bf16 value).
-__device__ __forceinline__ void widen_fp8_stage(const uint8_t* raw, uint8_t* conv, int t) {
-    const int r = t;
+// One row of an FP8 weight stage (128 rows x 128 E4M3 codes, 128-byte
+// swizzle) widened to bf16 as two 64-k tiles in the same swizzle: the 16-byte
+// chunk c of row r sits at r*128 + ((c ^ (r & 7)) << 4) in every tile.
+// E4M3 -> bf16 is exact (every E4M3 value is a bf16 value).
+__device__ __forceinline__ void widen_fp8_row(const uint8_t* raw, uint8_t* conv, int r) {
     const int sw = r & 7;
     const uint8_t* src = raw + r * kRowBytes;
 #pragma unroll
@@ -234,7 +234,7 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile
 // bf16 x bf16 product: A and B of one kind::f16 MMA share a type).
 
 template <typename T, int EPI, bool W8>
-__global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, W8 ? 1 : 2)
+__global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
            const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -246,7 +246,8 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, W8 ? 1 : 2)
     uint8_t* sA = smem;
     uint8_t* sB = smem + static_cast<size_t>(stages) * kABytes;
     uint8_t* sC = sB + static_cast<size_t>(stages) * b_bytes;         // W8: bf16 weight copies
-    uint64_t* full = reinterpret_cast<uint64_t*>(sC + (W8 ? static_cast<size_t>(kConvStages) * kConvBytes : 0));
+    const int cstages = W8 ? p.cstages : 0;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sC + static_cast<size_t>(cstages) * kConvBytes);
     uint64_t* empty = full + stages;
     uint64_t* tfull = empty + stages;      // [2] accumulator ready
     uint64_t* tempty = tfull + 2;          // [2] accumulator drained by the epilogue
@@ -291,8 +292,8 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, W8 ? 1 : 2)
             mbar_init(&tempty[a], 128);
         }
         if constexpr (W8) {
-            for (int c = 0; c < kConvStages; ++c) {
-                mbar_init(&cfull[c], 128);
+            for (int c = 0; c < cstages; ++c) {
+                mbar_init(&cfull[c], kConvThreads);
                 mbar_init(&cempty[c], 1);
             }
         }
@@ -428,7 +429,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, W8 ? 1 : 2)
                             }
                         }
                         umma_commit(&cempty[c]);
-                        if (++c == kConvStages) {
+                        if (++c == cstages) {
                             c = 0;
                             cph ^= 1u;
                         }
@@ -451,7 +452,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, W8 ? 1 : 2)
             }
         }
         __syncwarp();
-    } else if (W8 && warp >= 6) {
+    } else if (W8 && warp >= 6) {   // warps 6..7
         // converters: widen each weight stage into the next bf16 copy, in the
         // MMA's order; the MMA releases the raw stage, so the codes stay put
         // until the copy is complete
@@ -471,15 +472,16 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, W8 ? 1 : 2)
                         ok = false;
                         break;
                     }
-                    widen_fp8_stage(sA + static_cast<size_t>(s) * kABytes, sC + static_cast<size_t>(c) * kConvBytes,
-                                    t);
+                    for (int r = t; r < kBM; r += kConvThreads)
+                        widen_fp8_row(sA + static_cast<size_t>(s) * kABytes, sC + static_cast<size_t>(c) * kConvBytes,
+                                      r);
                     fence_proxy_async_smem();   // the MMA (async proxy) reads what these threads wrote
                     mbar_arrive(&cfull[c]);
                     if (++s == stages) {
                         s = 0;
                         ph ^= 1u;
                     }
-                    if (++c == kConvStages) {
+                    if (++c == cstages) {
                         c = 0;
                         cph ^= 1u;
                     }
@@ -647,15 +649,19 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     // faster per step, at 176 rows its two stages were much slower)
     const size_t stage = kABytes + static_cast<size_t>(g.bn) * kRowBytes * (w8 ? 2 : 1);
     const int inv_floats = (epi == EPI_QKV || epi == EPI_SWIGLU) ? inv_slots(N) : 0;
-    // FP8 weights: one CTA per SM, the ring in what the bf16 copies, the
-    // staging tile and the folded-norm scales leave of ~215 KB
-    const size_t budget = w8 ? 215 * 1024 - static_cast<size_t>(kConvStages) * kConvBytes -
-                                   static_cast<size_t>(kChunk) * kPitch * 4 - static_cast<size_t>(inv_floats) * 4 - 2048
+    // FP8 weights: up to 64 token rows, one bf16 copy and a ring that keeps
+    // the CTA within ~112 KB (two CTAs per SM, so the next kernel's CTAs can
+    // start streaming beside it, as in the bf16 path); wider token tiles
+    // take two copies and one CTA per SM (~215 KB)
+    g.cstages = w8 ? (g.bn <= 64 ? 1 : 2) : 0;
+    const size_t fixed = static_cast<size_t>(g.cstages) * kConvBytes + static_cast<size_t>(kChunk) * kPitch * 4 +
+                         static_cast<size_t>(inv_floats) * 4 + 2048;
+    const size_t budget = w8 ? (g.cstages == 1 ? 112 * 1024 : 215 * 1024) - fixed
                              : (g.bn <= 128 ? 100 * 1024 : 190 * 1024);
     int st = static_cast<int>(budget / stage);
     g.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
-    g.smem_bytes = gemm_smem_bytes(g.stages, g.bn, inv_floats, w8);
-    const int ctas_per_sm = (!w8 && g.smem_bytes <= 113 * 1024) ? 2 : 1;
+    g.smem_bytes = gemm_smem_bytes(g.stages, g.bn, inv_floats, w8, g.cstages);
+    const int ctas_per_sm = g.smem_bytes <= 113 * 1024 ? 2 : 1;
     int splits = 1;
     if (epi != EPI_ARGMAX) {
         if (cluster) {
@@ -712,6 +718,7 @@ int launch_gemm(int dtype, int epi, const CUtensorMap& A, const CUtensorMap& A2,
     p.kb_per_split = plan.kb_per_split;
     p.bn = plan.bn;
     p.stages = plan.stages;
+    p.cstages = plan.cstages;
     p.cluster = plan.cluster ? 1 : 0;
     p.persistent = plan.persistent ? 1 : 0;
     if (plan.w8) {
