@@ -111,7 +111,8 @@ typedef struct pe_weights {
  * bytes) standing for W[m, k] = q[m, k] * scale[m]. The codes are widened to
  * bf16 in shared memory (exactly: every E4M3 value is a bf16 value), the
  * tensor cores multiply bf16 by bf16 with fp32 accumulation, and the epilogue
- * applies scale[m]. Each array below is fp32 [rows of that matrix]. */
+ * applies scale[m]. Each array below is fp32 [rows of that matrix]. Codes
+ * must be finite: the NaN codes 0x7F / 0xFF are not decoded as NaN. */
 typedef struct pe_layer_scales {
     const float* w_qkv;     /* [(nq+2nkv)*hd] */
     const float* w_o;       /* [H] */
@@ -261,6 +262,37 @@ int pe_verify_rebuild_refeed(pe_handle* h, int32_t B, int32_t K, const int32_t* 
                              const int32_t* seq_lens, int32_t* n_real_out, int32_t* positions_out,
                              int32_t* seq_lens_out, int32_t* accepted, int32_t* bonus, int32_t* emitted,
                              int32_t* slot_mapping, int32_t* rollback_slots, int32_t* status, void* stream);
+
+/* Sampled drafting and stochastic acceptance (the pages' "standard
+ * acceptance criterion" when decoding samples, as their deployment does at
+ * temperature 0.3: "在 Amazon SageMaker AI 上使用 P-EAGLE 并行化推测解码",
+ * "逐步草稿过程"). With q_j = softmax(draft logits of row j / T) and
+ * p_j = softmax(target logits of position j / T), speculative sampling
+ * accepts draft d_j while u_j < p_j(d_j) / q_j(d_j), and emits at the first
+ * rejection a token drawn from max(0, p_j - q_j) (normalised), or after K
+ * acceptances a bonus token drawn from p_K; the emitted tokens are then
+ * distributed as sampling the target alone. Every draw is inverse-CDF
+ * sampling with a caller-supplied uniform u in [0, 1): the smallest index
+ * whose running weight, summed in index order, exceeds u times the total.
+ *
+ * pe_sample_drafts: drafts[b, j] ~ q_j from logits [B, K, V] fp32 (the
+ *  logits output of pe_draft / pe_draft_refeed; P-EAGLE's rows come from one
+ *  pass, so each row is drawn independently), u [B, K] fp32; status [B]
+ *  (nullable: requests not PE_REQ_OK get -1).
+ * pe_verify_stochastic: draft_logits [B, K, V], target_logits [B, K+1, V]
+ *  fp32, u_accept [B, K], u_final [B] fp32; accepted [B] OUT a_b,
+ *  final_token [B] OUT the drawn token (it takes the place of the greedy
+ *  bonus); emitted, the metadata rebuild, rollback and status exactly as
+ *  pe_verify_rebuild given a_b. Uses the handle's workspace (h required;
+ *  B <= max_batch, K <= k_max). temperature > 0. */
+int pe_sample_drafts(pe_handle* h, int32_t B, int32_t K, const float* logits, float temperature, const float* u,
+                     const int32_t* status, int32_t* drafts, void* stream);
+int pe_verify_stochastic(pe_handle* h, int32_t B, int32_t K, const int32_t* drafts, const float* draft_logits,
+                         const float* target_logits, float temperature, const float* u_accept, const float* u_final,
+                         const int32_t* page_table, int32_t max_pages, int32_t num_pages, const int32_t* positions,
+                         const int32_t* seq_lens, int32_t* positions_out, int32_t* seq_lens_out, int32_t* accepted,
+                         int32_t* final_token, int32_t* emitted, int32_t* slot_mapping, int32_t* rollback_slots,
+                         int32_t* status, void* stream);
 
 /* The draft pass's tcgen05 GEMM engine on its own (plain store epilogue):
  *   y[n, m] = sum_k w[m, k] * x[n, k]

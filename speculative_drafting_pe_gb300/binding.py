@@ -26,6 +26,7 @@ EXPORTS = (
     "pe_step_graph_create", "pe_step_graph_launch", "pe_step_graph_launch_count", "pe_step_graph_destroy",
     "pe_linear_noalloc", "pe_test_stall_chain", "pe_draft_sequential", "pe_step_graph_create_ex",
     "pe_init_drafter_fp8", "pe_linear_fp8", "pe_draft_refeed", "pe_verify_rebuild_refeed",
+    "pe_sample_drafts", "pe_verify_stochastic",
 )
 KERNEL_KINDS = ("fc", "row_build", "rmsnorm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "argmax",
                 "layer_chain")
@@ -105,6 +106,11 @@ def load():
     lib.pe_verify_rebuild_refeed.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                              _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.pe_verify_rebuild_refeed.restype = ctypes.c_int
+    lib.pe_sample_drafts.argtypes = [_vp, _i32, _i32, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]
+    lib.pe_sample_drafts.restype = ctypes.c_int
+    lib.pe_verify_stochastic.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i32, _i32,
+                                         _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.pe_verify_stochastic.restype = ctypes.c_int
     lib.pe_draft_sequential.argtypes = lib.pe_draft.argtypes
     lib.pe_draft_sequential.restype = ctypes.c_int
     lib.pe_verify_rebuild.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -274,6 +280,41 @@ class Drafter:
                                       _p(k_cache), _p(v_cache), _p(drafts), _p(logits), _p(status),
                                       _stream_ptr(stream)))
         return drafts, status
+
+    def sample_drafts(self, logits, temperature, u, status=None, drafts=None, stream=None):
+        """drafts [B, K] ~ softmax(logits / T) per row by inverse CDF with u [B, K]."""
+        B, K, V = logits.shape
+        dev = self.device
+        _need(logits, torch.float32, dev, "logits")
+        _need(u, torch.float32, dev, "u")
+        if drafts is None:
+            drafts = torch.empty(B, K, dtype=torch.int32, device=dev)
+        _check(load().pe_sample_drafts(self._h, B, K, _p(logits), float(temperature), _p(u), _p(status), _p(drafts),
+                                       _stream_ptr(stream)))
+        return drafts
+
+    def verify_stochastic(self, drafts, draft_logits, target_logits, temperature, u_accept, u_final, page_table,
+                          num_pages, positions, seq_lens, stream=None):
+        """Speculative-sampling acceptance + metadata rebuild. Returns a dict
+        of int32 device tensors: accepted, final, emitted, positions,
+        seq_lens, slot_mapping, rollback_slots, status."""
+        B, K = drafts.shape
+        dev = self.device
+        for name, t in (("drafts", drafts), ("page_table", page_table), ("positions", positions),
+                        ("seq_lens", seq_lens)):
+            _need(t, torch.int32, dev, name)
+        for name, t in (("draft_logits", draft_logits), ("target_logits", target_logits), ("u_accept", u_accept),
+                        ("u_final", u_final)):
+            _need(t, torch.float32, dev, name)
+        e = lambda *s: torch.empty(*s, dtype=torch.int32, device=dev)
+        o = dict(accepted=e(B), final=e(B), emitted=e(B, K + 1), positions=e(B), seq_lens=e(B),
+                 slot_mapping=e(B, K), rollback_slots=e(B, K), status=e(B))
+        _check(load().pe_verify_stochastic(
+            self._h, B, K, _p(drafts), _p(draft_logits), _p(target_logits), float(temperature), _p(u_accept),
+            _p(u_final), _p(page_table), page_table.shape[1], num_pages, _p(positions), _p(seq_lens),
+            _p(o["positions"]), _p(o["seq_lens"]), _p(o["accepted"]), _p(o["final"]), _p(o["emitted"]),
+            _p(o["slot_mapping"]), _p(o["rollback_slots"]), _p(o["status"]), _stream_ptr(stream)))
+        return o
 
     def profile_start(self, kind, max_launches):
         """Time every launch of one kernel kind (name from KERNEL_KINDS) with

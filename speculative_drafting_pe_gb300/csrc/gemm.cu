@@ -16,9 +16,6 @@
 // split to arrive at the tile's ticket sums the partials in split order
 // (0, 1, ..., S-1), so the result does not depend on arrival order, then
 // applies the epilogue and resets the ticket for the next launch.
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
-
 #include "gemm_epi.cuh"
 
 namespace pe {
@@ -65,10 +62,28 @@ __device__ __forceinline__ void scale_row(float (&v)[kChunk], float s) {
     }
 }
 
+// Two E4M3 codes (bytes `lo_sel`/`hi_sel` of w) widened to a bf16 pair with
+// integer operations only: PRMT places each code in the low byte of a 16-bit
+// lane and replicates its sign bit into the high byte; shifted left by 4, the
+// code's exponent and mantissa land in bf16's exponent and mantissa fields
+// and a copy of the sign in bit 15, so the masked lane is the bf16 of
+// value * 2^-120 (an E4M3 subnormal lands on a bf16 subnormal, zero on
+// zero). One exact bf16 multiply by 2^120 restores the value. The NaN codes
+// (S.1111.111) are not decoded as NaN: weights must be finite.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w, uint32_t sel) {
+    uint32_t t;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(w), "r"(sel));
+    const uint32_t v = (t << 4) & 0x87F087F0u;
+    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v);
+    const uint32_t k = 0x7B807B80u;   // bf16 pair (2^120, 2^120)
+    b = __hmul2(b, *reinterpret_cast<const __nv_bfloat162*>(&k));
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+
 // One row of an FP8 weight stage (128 rows x 128 E4M3 codes, 128-byte
 // swizzle) widened to bf16 as two 64-k tiles in the same swizzle: the 16-byte
 // chunk c of row r sits at r*128 + ((c ^ (r & 7)) << 4) in every tile.
-// E4M3 -> bf16 is exact (every E4M3 value is a bf16 value).
+// E4M3 -> bf16 is exact (every finite E4M3 value is a bf16 value).
 __device__ __forceinline__ void widen_fp8_row(const uint8_t* raw, uint8_t* conv, int r) {
     const int sw = r & 7;
     const uint8_t* src = raw + r * kRowBytes;
@@ -79,14 +94,8 @@ __device__ __forceinline__ void widen_fp8_row(const uint8_t* raw, uint8_t* conv,
         uint32_t o[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xFFFFu);
-                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-                const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-                o[2 * i + h] = *reinterpret_cast<const uint32_t*>(&b);
-            }
+            o[2 * i] = e4m3x2_to_bf16x2(w[i], 0x9180u);       // bytes 0, 1
+            o[2 * i + 1] = e4m3x2_to_bf16x2(w[i], 0xB3A2u);   // bytes 2, 3
         }
         uint8_t* dst = conv + (c >> 2) * kABytes + r * kRowBytes;
         const int j0 = 2 * (c & 3);

@@ -289,6 +289,27 @@ int launch_verify_rebuild(int B, int K, const int32_t* drafts, const int32_t* ta
                           int32_t* accepted, int32_t* bonus, int32_t* emitted, int32_t* slot_mapping,
                           int32_t* rollback, int32_t* status, cudaStream_t s);
 
+// metadata rebuild for an acceptance decided elsewhere: accepted [B] and the
+// final token [B] are inputs (emitted, slots, rollback, status as above)
+int launch_rebuild_given_acceptance(int B, int K, const int32_t* drafts, const int32_t* page_table, int max_pages,
+                                    int num_pages, int page_size, const int32_t* positions, const int32_t* seq_lens,
+                                    int32_t* positions_out, int32_t* seq_lens_out, const int32_t* accepted,
+                                    const int32_t* final_tok, int32_t* emitted, int32_t* slot_mapping,
+                                    int32_t* rollback, int32_t* status, cudaStream_t s);
+
+// ---------------------------------------------------------------- sampling (stochastic acceptance)
+
+// drafts[r] ~ softmax(logits[r] / T) by inverse CDF with u[r], rows r = b * K + j
+// (status[b] not OK: -1); one CTA per row
+int launch_sample_rows(const float* logits, int rows, int V, float temperature, const float* u,
+                       const int32_t* status, int K, int32_t* drafts, cudaStream_t s);
+// speculative-sampling acceptance: per-row softmax statistics into `stats`
+// ([B*K + B*(K+1)] float2), then per request the accepted length and the
+// final token (residual draw or bonus)
+int launch_stochastic_accept(int B, int K, int V, float temperature, const int32_t* drafts, const float* dlogits,
+                             const float* tlogits, const float* u_accept, const float* u_final, float2* stats,
+                             int32_t* accepted, int32_t* final_tok, cudaStream_t s);
+
 // the same for re-fed real rows: n_real in/out, slot_mapping [B, 2K], rollback [B, K]
 int launch_verify_rebuild_refeed(int B, int K, const int32_t* drafts, const int32_t* target,
                                  const int32_t* page_table, int max_pages, int num_pages, int page_size,

@@ -46,6 +46,7 @@ struct pe_handle {
     int* row_slot = nullptr;
     int32_t* attn_order = nullptr;   // [max_batch] requests by decreasing seq_len
     int32_t* seq_eff = nullptr;      // [max_batch] S_b + j0 of the current sequential pass
+    float2* samp_stats = nullptr;    // [max_batch * (2 k_max + 1)] softmax (max, sum) per logit row
     float2* rope_cs = nullptr;
     double* inv_freq = nullptr;
     float* gemm_ws = nullptr;
@@ -231,7 +232,7 @@ void free_handle(pe_handle* h) {
     void* ptrs[] = {h->h,    h->resid,    h->u,        h->xn,         h->ss,      h->q,            h->attn,      h->act,
                     h->amax, h->row_slot, h->attn_order, h->rope_cs, h->inv_freq, h->gemm_ws, h->gemm_tickets, h->attn_ws,
                     h->attn_tickets, h->err, h->chain_ctr, h->chain_ws, h->chain_tickets, h->attn_items,
-                    h->attn_plan, h->seq_eff};
+                    h->attn_plan, h->seq_eff, h->samp_stats};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     delete h;
@@ -416,6 +417,8 @@ int init_drafter(const pe_config* cfg, const pe_weights* weights, const pe_weigh
     if (a == PE_OK) a = dev_alloc(&h->row_slot, R * 4);
     if (a == PE_OK) a = dev_alloc(&h->attn_order, static_cast<size_t>(max_batch) * 4);
     if (a == PE_OK) a = dev_alloc(&h->seq_eff, static_cast<size_t>(max_batch) * 4);
+    if (a == PE_OK)
+        a = dev_alloc(&h->samp_stats, static_cast<size_t>(max_batch) * (2 * cfg->k_max + 1) * sizeof(float2));
     if (a == PE_OK) a = dev_alloc(&h->rope_cs, R * (hd / 2) * sizeof(float2));
     if (a == PE_OK) a = dev_alloc(&h->inv_freq, (hd / 2) * sizeof(double));
     if (a == PE_OK) a = dev_alloc(&h->gemm_ws, h->gemm_ws_floats * 4);
@@ -1047,6 +1050,41 @@ int pe_verify_rebuild_refeed(pe_handle* h, int32_t B, int32_t K, const int32_t* 
                                         positions, seq_lens, n_real_out, positions_out, seq_lens_out, accepted, bonus,
                                         emitted, slot_mapping, rollback_slots, status,
                                         static_cast<cudaStream_t>(stream));
+}
+
+int pe_sample_drafts(pe_handle* h, int32_t B, int32_t K, const float* logits, float temperature, const float* u,
+                     const int32_t* status, int32_t* drafts, void* stream) {
+    if (h == nullptr) { set_error("null handle"); return PE_ERR_ARG; }
+    if (B < 1 || B > h->max_batch || K < 1 || K > h->cfg.k_max) { set_error("B or K out of range"); return PE_ERR_ARG; }
+    if (!logits || !u || !drafts) { set_error("null tensor argument"); return PE_ERR_ARG; }
+    if (!(temperature > 0.f)) { set_error("temperature must be > 0"); return PE_ERR_ARG; }
+    return launch_sample_rows(logits, B * K, h->cfg.vocab, temperature, u, status, K, drafts,
+                              static_cast<cudaStream_t>(stream));
+}
+
+int pe_verify_stochastic(pe_handle* h, int32_t B, int32_t K, const int32_t* drafts, const float* draft_logits,
+                         const float* target_logits, float temperature, const float* u_accept, const float* u_final,
+                         const int32_t* page_table, int32_t max_pages, int32_t num_pages, const int32_t* positions,
+                         const int32_t* seq_lens, int32_t* positions_out, int32_t* seq_lens_out, int32_t* accepted,
+                         int32_t* final_token, int32_t* emitted, int32_t* slot_mapping, int32_t* rollback_slots,
+                         int32_t* status, void* stream) {
+    if (h == nullptr) { set_error("null handle"); return PE_ERR_ARG; }
+    if (B < 1 || B > h->max_batch || K < 1 || K > h->cfg.k_max) { set_error("B or K out of range"); return PE_ERR_ARG; }
+    if (!(temperature > 0.f)) { set_error("temperature must be > 0"); return PE_ERR_ARG; }
+    if (max_pages < 1 || num_pages < 1) { set_error("max_pages and num_pages must be >= 1"); return PE_ERR_ARG; }
+    if (!drafts || !draft_logits || !target_logits || !u_accept || !u_final || !page_table || !positions ||
+        !seq_lens || !positions_out || !seq_lens_out || !accepted || !final_token || !slot_mapping ||
+        !rollback_slots || !status) {
+        set_error("null tensor argument");
+        return PE_ERR_ARG;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = launch_stochastic_accept(B, K, h->cfg.vocab, temperature, drafts, draft_logits, target_logits, u_accept,
+                                      u_final, h->samp_stats, accepted, final_token, s);
+    if (rc != PE_OK) return rc;
+    return launch_rebuild_given_acceptance(B, K, drafts, page_table, max_pages, num_pages, 16, positions, seq_lens,
+                                           positions_out, seq_lens_out, accepted, final_token, emitted, slot_mapping,
+                                           rollback_slots, status, s);
 }
 
 int pe_linear_scratch(int32_t dtype, int32_t M, int32_t N, int32_t Kd, int64_t* ws_floats, int32_t* n_tickets) {

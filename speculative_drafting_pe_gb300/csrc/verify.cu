@@ -27,7 +27,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                      const int32_t* positions, const int32_t* seq_lens, int32_t* positions_out,
                      int32_t* seq_lens_out, int32_t* __restrict__ accepted, int32_t* __restrict__ bonus,
                      int32_t* __restrict__ emitted, int32_t* __restrict__ slot_mapping,
-                     int32_t* __restrict__ rollback, int32_t* __restrict__ status) {
+                     int32_t* __restrict__ rollback, int32_t* __restrict__ status, const int32_t* acc_in,
+                     const int32_t* bonus_in) {
     pdl_launch_dependents();
     pdl_wait();
     const int b = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -36,10 +37,18 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const unsigned full = 0xffffffffu;
 
     const int dj = lane < K ? drafts[static_cast<size_t>(b) * K + lane] : 0;
-    const int gj = lane <= K ? target[static_cast<size_t>(b) * (K + 1) + lane] : 0;
-    const unsigned mism = __ballot_sync(full, lane < K && dj != gj);
-    const int a = mism ? (__ffs(mism) - 1) : K;
-    const int bon = __shfl_sync(full, gj, a);
+    int a, bon;
+    if (acc_in != nullptr) {
+        // acceptance decided elsewhere (stochastic acceptance): a and the
+        // final token are given
+        a = min(max(acc_in[b], 0), K);
+        bon = bonus_in[b];
+    } else {
+        const int gj = lane <= K ? target[static_cast<size_t>(b) * (K + 1) + lane] : 0;
+        const unsigned mism = __ballot_sync(full, lane < K && dj != gj);
+        a = mism ? (__ffs(mism) - 1) : K;
+        bon = __shfl_sync(full, gj, a);
+    }
 
     const int S = seq_lens[b];
     const int Q = positions[b];
@@ -74,8 +83,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     if (emitted != nullptr && lane <= K)
         emitted[static_cast<size_t>(b) * (K + 1) + lane] = lane < a ? dj : (lane == a ? bon : -1);
     if (lane == 0) {
-        accepted[b] = a;
-        bonus[b] = bon;
+        if (acc_in == nullptr) {
+            accepted[b] = a;
+            bonus[b] = bon;
+        }
         status[b] = st;
         seq_lens_out[b] = ok ? S2 : S;
         positions_out[b] = ok ? Q2 : Q;
@@ -180,7 +191,22 @@ int launch_verify_rebuild(int B, int K, const int32_t* drafts, const int32_t* ta
     const dim3 grid((B + kWarpsPerBlock - 1) / kWarpsPerBlock), block(kWarpsPerBlock * 32);
     PE_CUDA_TRY(launch_ex(k_verify_rebuild, grid, block, 0, s, false, B, K, drafts, target, page_table, max_pages,
                           num_pages, page_size, positions, seq_lens, positions_out, seq_lens_out, accepted, bonus,
-                          emitted, slot_mapping, rollback, status));
+                          emitted, slot_mapping, rollback, status, static_cast<const int32_t*>(nullptr),
+                          static_cast<const int32_t*>(nullptr)));
+    return PE_OK;
+}
+
+int launch_rebuild_given_acceptance(int B, int K, const int32_t* drafts, const int32_t* page_table, int max_pages,
+                                    int num_pages, int page_size, const int32_t* positions, const int32_t* seq_lens,
+                                    int32_t* positions_out, int32_t* seq_lens_out, const int32_t* accepted,
+                                    const int32_t* final_tok, int32_t* emitted, int32_t* slot_mapping,
+                                    int32_t* rollback, int32_t* status, cudaStream_t s) {
+    const dim3 grid((B + kWarpsPerBlock - 1) / kWarpsPerBlock), block(kWarpsPerBlock * 32);
+    PE_CUDA_TRY(launch_ex(k_verify_rebuild, grid, block, 0, s, false, B, K, drafts,
+                          static_cast<const int32_t*>(nullptr), page_table, max_pages, num_pages, page_size,
+                          positions, seq_lens, positions_out, seq_lens_out, static_cast<int32_t*>(nullptr),
+                          static_cast<int32_t*>(nullptr), emitted, slot_mapping, rollback, status, accepted,
+                          final_tok));
     return PE_OK;
 }
 

@@ -43,6 +43,24 @@ def test_linear_fp8_matches_float64(M, N, Kd):
     assert err <= 1e-4 * np.abs(ref).max(), (err, np.abs(ref).max())
 
 
+def test_linear_fp8_every_finite_code_exactly():
+    # every finite E4M3 code (subnormals, zeros, +-448 included) in every
+    # position of a 16-byte chunk: with x = one-hot rows, y reads the decoded
+    # weights back through the tensor cores exactly
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    M, Kd = 128, 256
+    rng = np.random.default_rng(3)
+    q = np.stack([np.roll(np.resize(codes, Kd), 17 * m) for m in range(M)]).astype(np.uint8)
+    scale = rng.uniform(0.5, 2.0, size=M).astype(np.float32)
+    w = torch.as_tensor(q, device="cuda")
+    s = torch.as_tensor(scale, device="cuda")
+    x = torch.eye(Kd, device="cuda", dtype=torch.bfloat16)[:64]
+    y = binding.linear_fp8(w, s, x.contiguous())
+    torch.cuda.synchronize()
+    ref = oracle.dequant_rows(q, scale)[:, :64].T
+    np.testing.assert_array_equal(y.cpu().numpy().astype(np.float64), ref.astype(np.float32).astype(np.float64))
+
+
 def _fp8_setup(shape, seed, wl=None, device="cuda"):
     W = synth.make_weights(shape, seed, device=device)
     Wq, sc = synth.quantize_weights_fp8(W)
