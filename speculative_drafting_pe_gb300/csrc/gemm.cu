@@ -25,8 +25,8 @@ constexpr int kThreads = 192;
 constexpr int kConvThreads = 64;             // warps 6..7: FP8 -> bf16 weight converters
 constexpr int kThreadsW8 = kThreads + kConvThreads;
 constexpr int kMaxClusterSplits = 8;         // cluster split-K: at most 8 CTAs per tile
-constexpr int kConvStages = 2;               // most bf16 copies of FP8 weight stages (W8; plan: 1 or 2)
-constexpr uint32_t kConvBytes = 2 * kABytes; // 128 rows x 128 k as two 64-k SW128 tiles
+constexpr int kConvStages = 2;               // W8: bf16 copies of half a weight stage, double-buffered
+constexpr uint32_t kConvBytes = kABytes;     // 128 rows x 64 k: one SW128 bf16 tile
 
 __host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn, int inv_floats, bool w8, int cstages) {
     const size_t b_stage = static_cast<size_t>(bn) * kRowBytes * (w8 ? 2 : 1);
@@ -80,15 +80,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w, uint32_t sel) {
     return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-// One row of an FP8 weight stage (128 rows x 128 E4M3 codes, 128-byte
-// swizzle) widened to bf16 as two 64-k tiles in the same swizzle: the 16-byte
-// chunk c of row r sits at r*128 + ((c ^ (r & 7)) << 4) in every tile.
+// Half `half` of one row of an FP8 weight stage (128 rows x 128 E4M3 codes,
+// 128-byte swizzle) widened to bf16: codes k = 64 * half .. + 63 (chunks
+// c = 4 * half .. + 3) become one 64-k tile in the same swizzle (the 16-byte
+// chunk c of row r sits at r*128 + ((c ^ (r & 7)) << 4) in both tiles).
 // E4M3 -> bf16 is exact (every finite E4M3 value is a bf16 value).
-__device__ __forceinline__ void widen_fp8_row(const uint8_t* raw, uint8_t* conv, int r) {
+__device__ __forceinline__ void widen_fp8_row_half(const uint8_t* raw, uint8_t* conv, int r, int half) {
     const int sw = r & 7;
     const uint8_t* src = raw + r * kRowBytes;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 4 * half; c < 4 * half + 4; ++c) {
         const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[8];
@@ -97,7 +98,7 @@ __device__ __forceinline__ void widen_fp8_row(const uint8_t* raw, uint8_t* conv,
             o[2 * i] = e4m3x2_to_bf16x2(w[i], 0x9180u);       // bytes 0, 1
             o[2 * i + 1] = e4m3x2_to_bf16x2(w[i], 0xB3A2u);   // bytes 2, 3
         }
-        uint8_t* dst = conv + (c >> 2) * kABytes + r * kRowBytes;
+        uint8_t* dst = conv + r * kRowBytes;
         const int j0 = 2 * (c & 3);
         *reinterpret_cast<uint4*>(dst + ((j0 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<uint4*>(dst + (((j0 + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
@@ -238,9 +239,10 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile
 //
 // W8 (FP8 weights, bf16 activations): a stage holds 128 k of E4M3 weight
 // codes (one 16 KB TMA box) and the matching two 64-k bf16 token tiles; the
-// converter warps 6..9 widen the codes into one of two bf16 weight copies,
-// which the MMA reads as two K-major SW128 tiles (the tensor cores see a
-// bf16 x bf16 product: A and B of one kind::f16 MMA share a type).
+// converter warps 6..7 widen each half stage (64 k) into one of two bf16
+// tiles, alternately, so that one half converts while the MMA reads the
+// other (the tensor cores see a bf16 x bf16 product: A and B of one
+// kind::f16 MMA share a type).
 
 template <typename T, int EPI, bool W8>
 __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
@@ -254,8 +256,8 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
     const uint32_t b_bytes = W8 ? 2 * b_box : b_box;                  // token bytes per stage
     uint8_t* sA = smem;
     uint8_t* sB = smem + static_cast<size_t>(stages) * kABytes;
-    uint8_t* sC = sB + static_cast<size_t>(stages) * b_bytes;         // W8: bf16 weight copies
-    const int cstages = W8 ? p.cstages : 0;
+    uint8_t* sC = sB + static_cast<size_t>(stages) * b_bytes;         // W8: bf16 copies of half stages
+    const int cstages = W8 ? kConvStages : 0;
     uint64_t* full = reinterpret_cast<uint64_t*>(sC + static_cast<size_t>(cstages) * kConvBytes);
     uint64_t* empty = full + stages;
     uint64_t* tfull = empty + stages;      // [2] accumulator ready
@@ -418,30 +420,30 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
                         ok = false;
                         break;
                     }
-                    if constexpr (W8) {
-                        if (!mbar_wait(&cfull[c], cph, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
-                            ok = false;
-                            break;
-                        }
-                    }
                     tc_fence_after_sync();
                     const uint32_t b_addr = smem_u32(sB + static_cast<size_t>(s) * b_bytes);
                     if constexpr (W8) {
-                        const uint32_t a_addr = smem_u32(sC + static_cast<size_t>(c) * kConvBytes);
-#pragma unroll
-                        for (int half = 0; half < 2; ++half) {
+                        // each half stage as soon as its bf16 copy is ready
+                        for (int half = 0; half < 2 && ok; ++half) {
+                            if (!mbar_wait(&cfull[c], cph, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after_sync();
+                            const uint32_t a_addr = smem_u32(sC + static_cast<size_t>(c) * kConvBytes);
 #pragma unroll
                             for (int kk = 0; kk < kRowBytes / 32; ++kk) {
-                                UmmaKind<T>::mma(d_tmem, umma_desc_sw128(a_addr + half * kABytes + kk * 32),
+                                UmmaKind<T>::mma(d_tmem, umma_desc_sw128(a_addr + kk * 32),
                                                  umma_desc_sw128(b_addr + half * b_box + kk * 32), idesc,
                                                  (kb > kb0 || half > 0 || kk > 0) ? 1u : 0u);
                             }
+                            umma_commit(&cempty[c]);
+                            if (++c == cstages) {
+                                c = 0;
+                                cph ^= 1u;
+                            }
                         }
-                        umma_commit(&cempty[c]);
-                        if (++c == cstages) {
-                            c = 0;
-                            cph ^= 1u;
-                        }
+                        if (!ok) break;
                     } else {
                         const uint32_t a_addr = smem_u32(sA + static_cast<size_t>(s) * kABytes);
 #pragma unroll
@@ -475,24 +477,29 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 int m_tile, n_tile, split, kb0, kb1;
                 decode(u, m_tile, n_tile, split, kb0, kb1);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(&full[s], ph, p.err, PE_DEVERR_GEMM_TIMEOUT) ||
-                        !mbar_wait(&cempty[c], cph ^ 1u, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
+                for (int kb = kb0; kb < kb1 && ok; ++kb) {
+                    if (!mbar_wait(&full[s], ph, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
                         ok = false;
                         break;
                     }
-                    for (int r = t; r < kBM; r += kConvThreads)
-                        widen_fp8_row(sA + static_cast<size_t>(s) * kABytes, sC + static_cast<size_t>(c) * kConvBytes,
-                                      r);
-                    fence_proxy_async_smem();   // the MMA (async proxy) reads what these threads wrote
-                    mbar_arrive(&cfull[c]);
+                    for (int half = 0; half < 2; ++half) {
+                        if (!mbar_wait(&cempty[c], cph ^ 1u, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
+                            ok = false;
+                            break;
+                        }
+                        for (int r = t; r < kBM; r += kConvThreads)
+                            widen_fp8_row_half(sA + static_cast<size_t>(s) * kABytes,
+                                               sC + static_cast<size_t>(c) * kConvBytes, r, half);
+                        fence_proxy_async_smem();   // the MMA (async proxy) reads what these threads wrote
+                        mbar_arrive(&cfull[c]);
+                        if (++c == cstages) {
+                            c = 0;
+                            cph ^= 1u;
+                        }
+                    }
                     if (++s == stages) {
                         s = 0;
                         ph ^= 1u;
-                    }
-                    if (++c == cstages) {
-                        c = 0;
-                        cph ^= 1u;
                     }
                 }
             }
@@ -658,14 +665,14 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     // faster per step, at 176 rows its two stages were much slower)
     const size_t stage = kABytes + static_cast<size_t>(g.bn) * kRowBytes * (w8 ? 2 : 1);
     const int inv_floats = (epi == EPI_QKV || epi == EPI_SWIGLU) ? inv_slots(N) : 0;
-    // FP8 weights: up to 64 token rows, one bf16 copy and a ring that keeps
-    // the CTA within ~112 KB (two CTAs per SM, so the next kernel's CTAs can
-    // start streaming beside it, as in the bf16 path); wider token tiles
-    // take two copies and one CTA per SM (~215 KB)
-    g.cstages = w8 ? (g.bn <= 64 ? 1 : 2) : 0;
+    // FP8 weights: two 16 KB bf16 copies of half stages; up to 64 token rows
+    // the ring keeps the CTA within ~112 KB (two CTAs per SM, so the next
+    // kernel's CTAs can start streaming beside it, as in the bf16 path);
+    // wider token tiles take one CTA per SM (~215 KB)
+    g.cstages = w8 ? kConvStages : 0;
     const size_t fixed = static_cast<size_t>(g.cstages) * kConvBytes + static_cast<size_t>(kChunk) * kPitch * 4 +
                          static_cast<size_t>(inv_floats) * 4 + 2048;
-    const size_t budget = w8 ? (g.cstages == 1 ? 112 * 1024 : 215 * 1024) - fixed
+    const size_t budget = w8 ? (g.bn <= 64 ? 112 * 1024 : 215 * 1024) - fixed
                              : (g.bn <= 128 ? 100 * 1024 : 190 * 1024);
     int st = static_cast<int>(budget / stage);
     g.stages = st < 2 ? 2 : (st > 8 ? 8 : st);

@@ -41,7 +41,7 @@ struct GemmParams {
     int N;              // token rows
     int Kd;             // reduction length
     int m_tiles, n_tiles, splits, kb_total, kb_per_split, bn, stages;
-    int cstages;        // FP8 weights: bf16 copies of weight stages in shared memory (1 or 2)
+    int cstages;        // FP8 weights: bf16 copies of half weight stages in shared memory
     // STORE / RESID: fp32 [N, ld_out]
     float* out_f32;
     int ld_out;
@@ -93,7 +93,7 @@ struct GemmParams {
 
 struct GemmPlan {
     bool w8;            // FP8 (E4M3) weights widened to bf16 in shared memory; 128 k per stage
-    int cstages;        // W8: bf16 weight copies (1 up to 64 token rows, then 2)
+    int cstages;        // W8: bf16 copies of half weight stages (double-buffered)
     int bn, n_tiles, m_tiles, splits, kb_total, kb_per_split, stages;
     int units;
     size_t smem_bytes;

@@ -17,7 +17,7 @@ from parity import weights_to
 
 pytestmark = pytest.mark.gpu
 
-MARGIN = 1e-3
+MARGIN = 5e-6          # well above float32 rounding of the GPU's ordered sums (~1e-7 of the total)
 TINY_V = synth.DrafterShape("stoch", 256, 4, 2, 64, 512, 5000)
 
 
@@ -32,7 +32,7 @@ def _logits(B, K, V, seed, scale=2.0, extra=0):
     return torch.randn(B, K + extra, V, generator=g, device="cuda") * scale
 
 
-@pytest.mark.parametrize("V,T", [(5000, 1.0), (5000, 0.3), (151936, 0.3)])
+@pytest.mark.parametrize("V,T", [(5000, 1.0), (5000, 0.3), (151936, 0.3)])   # 0.3: the pages' temperature
 def test_sample_drafts_match_oracle(V, T):
     B, K = 6, 5
     shape = synth.DrafterShape("stoch", 256, 4, 2, 64, 512, V)
@@ -44,7 +44,7 @@ def test_sample_drafts_match_oracle(V, T):
     ref, margin = oracle.sample_drafts(lg.double().cpu().numpy(), T, u.double().cpu().numpy())
     dn = d.cpu().numpy()
     sure = margin > MARGIN
-    assert sure.mean() > 0.8
+    assert sure.mean() > 0.6
     np.testing.assert_array_equal(dn[sure], ref[sure])
     assert ((dn >= 0) & (dn < V)).all()
 
@@ -85,7 +85,7 @@ def _meta_inputs(B, K, seed):
     return v, t(v["page_table"]), v["num_pages"], t(v["positions"]), t(v["seq_lens"])
 
 
-@pytest.mark.parametrize("V,T", [(5000, 1.0), (5000, 0.3), (151936, 0.7)])
+@pytest.mark.parametrize("V,T", [(5000, 1.0), (5000, 0.3), (151936, 0.3)])
 def test_verify_stochastic_matches_oracle(V, T):
     B, K = 24, 5
     shape = synth.DrafterShape("stoch", 256, 4, 2, 64, 512, V)
@@ -99,7 +99,7 @@ def test_verify_stochastic_matches_oracle(V, T):
     ref = oracle.verify_stochastic(dn, dl.double().cpu().numpy(), tl.double().cpu().numpy(), T,
                                    ua.double().cpu().numpy(), uf.double().cpu().numpy())
     sure = ref["margin"] > MARGIN
-    assert sure.mean() > 0.7
+    assert sure.mean() > 0.6
     a = out["accepted"].cpu().numpy()
     np.testing.assert_array_equal(a[sure], ref["accepted"][sure])
     np.testing.assert_array_equal(out["final"].cpu().numpy()[sure], ref["final"][sure])
