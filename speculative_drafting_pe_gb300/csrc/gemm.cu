@@ -22,7 +22,7 @@ namespace pe {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kConvThreads = 64;             // warps 6..7: FP8 -> bf16 weight converters
+constexpr int kConvThreads = 128;            // warps 6..9: FP8 -> bf16 weight converters
 constexpr int kThreadsW8 = kThreads + kConvThreads;
 constexpr int kMaxClusterSplits = 8;         // cluster split-K: at most 8 CTAs per tile
 constexpr int kConvStages = 2;               // W8: bf16 copies of half a weight stage, double-buffered
@@ -239,7 +239,7 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile
 //
 // W8 (FP8 weights, bf16 activations): a stage holds 128 k of E4M3 weight
 // codes (one 16 KB TMA box) and the matching two 64-k bf16 token tiles; the
-// converter warps 6..7 widen each half stage (64 k) into one of two bf16
+// converter warps 6..9 widen each half stage (64 k) into one of two bf16
 // tiles, alternately, so that one half converts while the MMA reads the
 // other (the tensor cores see a bf16 x bf16 product: A and B of one
 // kind::f16 MMA share a type).
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
             }
         }
         __syncwarp();
-    } else if (W8 && warp >= 6) {   // warps 6..7
+    } else if (W8 && warp >= 6) {   // warps 6..9
         // converters: widen each weight stage into the next bf16 copy, in the
         // MMA's order; the MMA releases the raw stage, so the codes stay put
         // until the copy is complete
