@@ -108,6 +108,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t row_stride = static_cast<size_t>(p.nq) * HD;
 
     pdl_launch_dependents();
+    // Before the dependency wait: set-up that reads nothing an earlier kernel
+    // writes (barriers, TMEM, the query tile's zero padding), and an L2
+    // prefetch of this CTA's first K/V pages. The prefetch reads the order
+    // list, lengths and page table as they are now - possibly still being
+    // written by earlier kernels of the stream - which is harmless: a wrong
+    // guess only warms the wrong lines; everything used below is read again
+    // after the wait.
+    if (tid == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&kv_full[s], 1);
+            // free once the P.V of the stage's tile has completed (one MMA
+            // commit; it is issued after the S that read K)
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&p_full[s], 128);
+        }
+        mbar_init(&o_done[0], 1);
+        mbar_init(&o_done[1], 1);
+        fence_mbar_init();
+    }
+    {
+        // zero the padding query rows Rq..127 (the TMA box fills rows < Rq)
+        const int Rq0 = p.K * (p.nq / p.nkv);
+        for (int idx = tid; idx < (kRows - Rq0) * 8 * L::kSub; idx += kThreads) {
+            const int sub = idx / ((kRows - Rq0) * 8);
+            const int rem = idx - sub * (kRows - Rq0) * 8;
+            const int r = Rq0 + rem / 8, c = rem % 8;
+            sts128(smem_u32(sm + L::kQ + sub * kRows * 128 + r * 128 + c * 16), 0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, 256);
+        tmem_relinquish();
+    }
+    if (tid == 4 * 32 && p.items == nullptr) {
+        const int pair = blockIdx.x;
+        const int kv_g = pair % p.nkv;
+        int b_g = p.order != nullptr ? p.order[pair / p.nkv] : pair / p.nkv;
+        b_g = b_g < 0 || b_g >= p.B ? 0 : b_g;
+        const int S_g = max(0, p.seq_lens[b_g]);
+        const int ea = static_cast<int>(blockIdx.y) * p.chunk;
+        const int eb = min(S_g + p.K, ea + p.chunk);
+        const int n_pf = min(kStages * (kTile / 16), eb > ea ? (eb - ea + 15) / 16 : 0);
+        const int32_t* pt_g = p.page_table + static_cast<size_t>(b_g) * p.max_pages;
+        for (int i = 0; i < n_pf; ++i) {
+            const int pi = (ea >> 4) + i;
+            const int pg = pi < p.max_pages ? pt_g[pi] : -1;
+            if (pg < 0 || pg >= p.num_pages) continue;
+            for (int sb = 0; sb < L::kSub; ++sb) {
+                tma_prefetch_l2_4d(&tmK, sb * 64, 0, kv_g, pg + p.layer_page0);
+                tma_prefetch_l2_4d(&tmV, sb * 64, 0, kv_g, pg + p.layer_page0);
+            }
+        }
+    }
     pdl_wait();
     int b, kvh, e0, e_end;
     bool single;                               // this CTA alone covers its (request, kv head)
@@ -140,42 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t* pt = p.page_table + static_cast<size_t>(b) * p.max_pages;
     const int last_page = (total - 1) >> 4;
 
-    if (tid == 0) {
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-        mbar_init(q_full, 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&kv_full[s], 1);
-            // free once the P.V of the stage's tile has completed (one MMA
-            // commit; it is issued after the S that read K)
-            mbar_init(&kv_empty[s], 1);
-        }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&s_full[s], 1);
-            mbar_init(&p_full[s], 128);
-        }
-        mbar_init(&o_done[0], 1);
-        mbar_init(&o_done[1], 1);
-        fence_mbar_init();
-    }
     // page coordinates of this CTA's tiles; pages past the request's last
     // entry get a negative (out-of-range, zero-filled) coordinate
     for (int i = tid; i < n_tiles * (kTile / 16); i += kThreads) {
         const int pi = (e0 >> 4) + i;
         s_pages[i] = pi <= last_page ? pt[pi] + p.layer_page0 : -1;
-    }
-    // zero the padding query rows Rq..127 (the TMA box fills rows < Rq)
-    for (int idx = tid; idx < (kRows - Rq) * 8 * L::kSub; idx += kThreads) {
-        const int sub = idx / ((kRows - Rq) * 8);
-        const int rem = idx - sub * (kRows - Rq) * 8;
-        const int r = Rq + rem / 8, c = rem % 8;
-        sts128(smem_u32(sm + L::kQ + sub * kRows * 128 + r * 128 + c * 16), 0u, 0u, 0u, 0u);
-    }
-    fence_proxy_async_smem();
-    if (warp == 5) {
-        tmem_alloc(tmem_slot, 256);
-        tmem_relinquish();
     }
     tc_fence_before_sync();
     __syncthreads();
