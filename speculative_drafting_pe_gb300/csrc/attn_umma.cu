@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     pdl_launch_dependents();
     // Before the dependency wait: set-up that reads nothing an earlier kernel
-    // writes (barriers, TMEM, the query tile's zero padding), and an L2
+    // writes (barriers, the query tile's zero padding), and an L2
     // prefetch of this CTA's first K/V pages. The prefetch reads the order
     // list, lengths and page table as they are now - possibly still being
     // written by earlier kernels of the stream - which is harmless: a wrong
@@ -144,10 +144,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             sts128(smem_u32(sm + L::kQ + sub * kRows * 128 + r * 128 + c * 16), 0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
-    }
-    if (warp == 5) {
-        tmem_alloc(tmem_slot, 256);
-        tmem_relinquish();
     }
     if (tid == 4 * 32 && p.items == nullptr) {
         const int pair = blockIdx.x;
@@ -206,6 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = tid; i < n_tiles * (kTile / 16); i += kThreads) {
         const int pi = (e0 >> 4) + i;
         s_pages[i] = pi <= last_page ? pt[pi] + p.layer_page0 : -1;
+    }
+    // TMEM after the early return of CTAs without a piece (a CTA must free
+    // what it allocates)
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, 256);
+        tmem_relinquish();
     }
     tc_fence_before_sync();
     __syncthreads();
