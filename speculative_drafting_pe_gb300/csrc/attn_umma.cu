@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
     }
-    if (tid == 4 * 32 && p.items == nullptr) {
+    if (tid == 4 * 32 && p.items == nullptr && p.l2_prefetch) {
         const int pair = blockIdx.x;
         const int kv_g = pair % p.nkv;
         int b_g = p.order != nullptr ? p.order[pair / p.nkv] : pair / p.nkv;
@@ -730,6 +730,7 @@ AttnPlan plan_attention_umma(int B, int K, int nq, int nkv, int hd, int max_page
     }
     a.chunk = chunk;
     a.max_splits = ceil_div(max_entries, chunk);         // one cluster of this many CTAs per (request, kv head)
+    a.one_wave = static_cast<long long>(pairs) * a.max_splits <= num_sms;
     a.ws_floats = 0;
     a.tickets = 0;
     (void)K;

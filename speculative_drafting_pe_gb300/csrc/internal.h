@@ -254,6 +254,7 @@ struct AttnParams {
     const int4* items;
     const int* plan;
     int grid;                 // CTAs launched (>= the item count)
+    int l2_prefetch;          // CTAs warm L2 with their first K/V pages before the dependency wait
 };
 struct AttnPlan {
     int chunk, max_splits;
@@ -263,6 +264,7 @@ struct AttnPlan {
     int piece_slots;          // CTAs resident at once (SMs x CTAs per SM)
     int piece_min_tiles;
     int grid;                 // piece_slots + B * nkv
+    bool one_wave;            // every CTA of the launch is resident at once
 };
 AttnPlan plan_attention(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms);
 int launch_attention(int dtype, const AttnParams& p, cudaStream_t s, bool pdl);

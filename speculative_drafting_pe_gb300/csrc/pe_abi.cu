@@ -796,6 +796,7 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
             ap.items = p_at.pieces ? h->attn_items : nullptr;
             ap.plan = h->attn_plan;
             ap.grid = p_at.grid;
+            ap.l2_prefetch = p_at.one_wave ? 1 : 0;   // with a second wave, early prefetches only compete
             // with length-aware pieces the merge kernel follows in the same
             // profiled interval (one attention per layer)
             rc = run(
