@@ -48,6 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--max-prefix", type=int, default=0,
                     help="cap the workload's prefix lengths (same GEMM shapes, smaller KV cache: for small ncu captures)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0, help="time box of the oracle CPU baseline")
+    ap.add_argument("--fp8", action="store_true",
+                    help="the main line with FP8 (E4M3) GEMM weights and per-row scales (bf16 activations and KV)")
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -412,8 +414,11 @@ def bench_ours(args):
         wl = dataclasses.replace(wl, prefix=(min(wl.prefix[0], cap), min(wl.prefix[1], cap)))
     K_max = max(wl.K, 11) if wl.B == 1 and wl.shape.name.startswith("qwen") else wl.K
     W = synth.make_weights(wl.shape, wl.seed, device=dev)
+    scales = None
+    if args.fp8:
+        W, scales = synth.quantize_weights_fp8(W)
     inp = synth.make_step_inputs(wl, device=dev)
-    drafter = binding.Drafter(wl.shape, W, max_batch=wl.B, k_max=K_max)
+    drafter = binding.Drafter(wl.shape, W, max_batch=wl.B, k_max=K_max, fp8_scales=scales)
     stream = torch.cuda.current_stream()
     B, K = wl.B, wl.K
     seq_np = inp.seq_lens.cpu().numpy()
@@ -512,7 +517,8 @@ def bench_ours(args):
         torch.cuda.synchronize()
         cold_ms = sum(a.elapsed_time(b) for a, b in evs) / n_cold
         cold = {"ms_per_step": cold_ms, "steps_s": 1e3 / cold_ms,
-                "step_hbm_frac": step_bytes(wl, seq_np) / (cold_ms / 1e3) / 1e9 / load_peaks()[0]["hbm_gbs"],
+                "step_hbm_frac": step_bytes(wl, seq_np, fp8=args.fp8) / (cold_ms / 1e3) / 1e9 /
+                                 load_peaks()[0]["hbm_gbs"],
                 "steps": n_cold, "flush": "256 MB buffer written between timed steps, outside the timed events"}
         del flush
 
@@ -584,7 +590,7 @@ def bench_ours(args):
     # ---------------- every workload of the metric (C2, C3, C4): one line each
     sweep = None
     fp8_lines = None
-    if not args.no_sweep and world == 1 and args.max_prefix == 0:
+    if not args.no_sweep and world == 1 and args.max_prefix == 0 and not args.fp8:
         peaks0, _ = load_peaks()
         del sg, sg_e
         drafter.close()
@@ -604,7 +610,8 @@ def bench_ours(args):
         return
 
     peaks, peaks_src = load_peaks()
-    dom_bytes, dom_flops = algorithmic_work(dominant, wl, seq_np, chained=shares.get("layer_chain", 0.0) > 0.0)
+    dom_bytes, dom_flops = algorithmic_work(dominant, wl, seq_np, chained=shares.get("layer_chain", 0.0) > 0.0,
+                                            fp8=args.fp8)
     dom_avg_s = (dom_ms / 1e3) / max(dom_n, 1)
     t_hbm = dom_bytes / (peaks["hbm_gbs"] * 1e9)
     t_tc = dom_flops / (peaks["bf16_tflops_sustained"] * 1e12)
@@ -616,7 +623,7 @@ def bench_ours(args):
         achieved = dom_flops / dom_avg_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops_sustained"]}
-    roof.update({"traffic": read_profile_traffic(dominant, args.workload), "kernel": dominant,
+    roof.update({"traffic": None if args.fp8 else read_profile_traffic(dominant, args.workload), "kernel": dominant,
                  "launches_timed": dom_n, "avg_launch_us": dom_avg_s * 1e6,
                  "algorithmic_bytes_per_launch": dom_bytes, "algorithmic_flops_per_launch": dom_flops,
                  "timed_in": "a second timed region of the same steps launched directly (events cannot sit inside "
@@ -634,14 +641,15 @@ def bench_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": wl.shape.dtype,
+        "dtype": "fp8w" if args.fp8 else wl.shape.dtype,
         "data": "synthetic (seeded inputs, random-init drafter weights)",
-        "config": {"workload": workload_desc(wl), "name": wl.name, "B": B, "K": K,
+        "config": {"workload": workload_desc(wl) + (", FP8 (E4M3) GEMM weights with per-row scales" if args.fp8 else ""),
+                   "name": wl.name, "B": B, "K": K,
                    "l2": "no flush: each step streams >1 GB of weights, larger than the 126 MB L2",
                    "parallelism": f"replicas x{world} (requests shard with no exchange)" if world > 1 else "1 GPU"},
         "draft_tok_s": value * B * K,
-        "step_hbm_gbs": step_bytes(wl, seq_np) / (ms_per_step / 1e3) / 1e9,
-        "step_hbm_frac": step_bytes(wl, seq_np) / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"],
+        "step_hbm_gbs": step_bytes(wl, seq_np, fp8=args.fp8) / (ms_per_step / 1e3) / 1e9,
+        "step_hbm_frac": step_bytes(wl, seq_np, fp8=args.fp8) / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"],
         "mean_accepted": float(acc.mean()),
         "direct_launch_ms_per_step": direct_ms,
         "roofline": roof,
