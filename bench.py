@@ -242,7 +242,12 @@ def oracle_worker(args):
     wl = synth.WORKLOADS[args.workload]
     W = synth.make_weights(wl.shape, wl.seed)
     inp = synth.make_step_inputs(wl)
-    Wn = synth.weights_to_numpy(W)
+    if args.fp8:
+        Wq, sc = synth.quantize_weights_fp8(W)
+        Wn = oracle.dequant_weights(*synth.fp8_to_numpy(Wq, sc))
+        del Wq, sc
+    else:
+        Wn = synth.weights_to_numpy(W)
     del W
     a = dict(last_token=inp.last_token.numpy(), target_hidden=inp.target_hidden.float().numpy(),
              positions=inp.positions.numpy(), seq_lens=inp.seq_lens.numpy(), page_table=inp.page_table.numpy(),
@@ -266,14 +271,14 @@ def oracle_worker(args):
                       "cores": len(os.sched_getaffinity(0))}))
 
 
-def run_oracle_subprocess(workload, seconds, max_steps):
+def run_oracle_subprocess(workload, seconds, max_steps, fp8=False):
     cores = len(os.sched_getaffinity(0))
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = str(cores)
     env["CUDA_VISIBLE_DEVICES"] = ""
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker", "--workload", workload,
-           "--cpu-seconds", str(seconds), "--steps", str(max_steps)]
+           "--cpu-seconds", str(seconds), "--steps", str(max_steps)] + (["--fp8"] if fp8 else [])
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=seconds * 6 + 600)
     if r.returncode != 0:
         raise RuntimeError("oracle worker failed: " + r.stderr[-2000:])
@@ -680,7 +685,7 @@ def bench_ours(args):
                             "activations and KV); step_bytes counts one byte per weight plus the scales")
     if world == 1 and not args.no_cpu_baseline:
         try:
-            res = run_oracle_subprocess(args.workload, args.cpu_seconds, 1000)
+            res = run_oracle_subprocess(args.workload, args.cpu_seconds, 1000, fp8=args.fp8)
             line["cpu_baseline"] = cpu_baseline_obj(res, wl)
         except Exception as exc:  # the baseline is reported, never required
             line["cpu_baseline"] = {"value": None, "unit": "steps/s", "cores": len(os.sched_getaffinity(0)),
