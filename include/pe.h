@@ -393,7 +393,7 @@ int pe_test_stall_chain(pe_handle* h, void* stream);
 #define PE_KERNEL_ROW_BUILD  1
 #define PE_KERNEL_RMSNORM    2   /* reserved: RMSNorm is folded into the GEMM epilogues and never launched */
 #define PE_KERNEL_QKV        3
-#define PE_KERNEL_ATTENTION  4
+#define PE_KERNEL_ATTENTION  4   /* with length-aware pieces also the merge kernel that follows it */
 #define PE_KERNEL_O_PROJ     5
 #define PE_KERNEL_GATE_UP    6
 #define PE_KERNEL_DOWN       7
@@ -404,13 +404,16 @@ int pe_test_stall_chain(pe_handle* h, void* stream);
 
 /* Measurement hook: after pe_profile_start, every launch of `kernel_kind`
  * made by pe_draft (up to max_launches of them) is bracketed by CUDA events
- * recorded on the launch stream. pe_profile_stop waits for those events and returns the summed
+ * recorded on the launch stream; an attention that runs as length-aware
+ * pieces is bracketed together with its merge kernel (one interval per
+ * layer). pe_profile_stop waits for those events and returns the summed
  * device time (ms) and the number of intervals timed. */
 int pe_profile_start(pe_handle* h, int32_t kernel_kind, int32_t max_launches);
 int pe_profile_stop(pe_handle* h, float* total_ms, int32_t* launches);
 const char* pe_kernel_name(int32_t kind);
 
-/* Number of kernels the last pe_draft call enqueued (for launch accounting). */
+/* Number of kernels the last pe_draft call enqueued (for launch accounting;
+ * merge kernels included). */
 int pe_last_launch_count(const pe_handle* h);
 
 void pe_destroy(pe_handle* h);

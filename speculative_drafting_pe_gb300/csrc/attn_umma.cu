@@ -10,8 +10,7 @@
 // requests issued longest first (an order the row build computes), the
 // splits of a pair combined through distributed shared memory; or
 // length-aware pieces - one CTA per item of the row build's piece list, no
-// cluster, the pieces of a request with several combined by the last of them
-// to finish (merge_pieces, in piece order). A tile
+// cluster, a request with several pieces combined by k_attn_merge. A tile
 // is 64 cache entries (4 pages). Roles (192 threads):
 //   warp 4   TMA: the packed query rows once (3-D map over q), then K and V
 //            pages of every tile (4-D map over the paged cache) into a
@@ -30,8 +29,7 @@
 // In the cluster layout the entry splits of one (request, kv head) form one
 // thread-block cluster and are combined through distributed shared memory in
 // split order; a piece of a request with several writes its partial (O,
-// running max, sum) to scratch, and the last piece of its (request, kv head)
-// to finish combines them.
+// running max, sum) to scratch for k_attn_merge.
 #include <cfloat>
 
 #include "common.cuh"
@@ -83,73 +81,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Combines the piece partials of (request b, kv head kvh): with M the
-// largest running max of the pieces, a row's output is
-// sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i. Work item = (query row,
-// pair of dims), items t, t + nthreads, ...; the pieces are read eight at a
-// time (all loads of a batch in flight) and folded in piece order with a
-// running max.
-constexpr int kMergeBatch = 8;
-
-template <int HD>
-__device__ void merge_pieces(const AttnParams& p, int b, int kvh, bool req_ok, int t, int nthreads) {
-    const int n = p.plan[1 + b];
-    const int G = p.nq / p.nkv;
-    const int K = p.K;
-    const int Rq = K * G;
-    const int off = p.plan[1 + p.B + b];
-    const int Rq4 = (Rq + 3) & ~3;
-    const size_t pf = attn_piece_floats(Rq, HD);
-    for (int item = t; item < Rq * (HD / 2); item += nthreads) {
-        const int r = item / (HD / 2);
-        const int d = (item - r * (HD / 2)) * 2;
-        float M = -INFINITY, den = 0.f, n0 = 0.f, n1 = 0.f;
-        for (int i0 = 0; i0 < n; i0 += kMergeBatch) {
-            float mv[kMergeBatch], lv[kMergeBatch];
-            float2 ov[kMergeBatch];
-#pragma unroll
-            for (int u = 0; u < kMergeBatch; ++u) {
-                mv[u] = -INFINITY;
-                lv[u] = 0.f;
-                ov[u] = make_float2(0.f, 0.f);
-                const int slot = p.nkv * (off + i0 + u) + kvh;
-                if (i0 + u < n && slot < p.grid) {
-                    const float* w = p.ws + static_cast<size_t>(slot) * pf;
-                    mv[u] = __ldcg(w + Rq * HD + r);
-                    lv[u] = __ldcg(w + Rq * HD + Rq4 + r);
-                    ov[u] = __ldcg(reinterpret_cast<const float2*>(w + r * HD + d));
-                }
-            }
-            float bm = M;
-#pragma unroll
-            for (int u = 0; u < kMergeBatch; ++u)
-                if (lv[u] > 0.f) bm = fmaxf(bm, mv[u]);
-            if (bm > M) {
-                // earlier sums are relative to M: bring them to the new maximum
-                const float f = exp2f(M - bm);     // 0 while nothing has been added
-                den *= f;
-                n0 *= f;
-                n1 *= f;
-                M = bm;
-            }
-#pragma unroll
-            for (int u = 0; u < kMergeBatch; ++u) {
-                if (lv[u] > 0.f) {
-                    const float f = exp2f(mv[u] - M);
-                    den = fmaf(lv[u], f, den);
-                    n0 = fmaf(f, ov[u].x, n0);
-                    n1 = fmaf(f, ov[u].y, n1);
-                }
-            }
-        }
-        const float inv = (req_ok && den > 0.f) ? 1.f / den : 0.f;
-        const int j = r / G, g = r - (r / G) * G;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(b * K + j) * p.nq * HD +
-                             static_cast<size_t>(kvh * G + g) * HD + d;
-        *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(n0 * inv, n1 * inv);
-    }
-}
-
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_umma(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -167,7 +98,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmem);
     int* s_pages = reinterpret_cast<int*>(sm + L::kPages);
     __shared__ float s_m[kRows], s_l[kRows];   // this split's per-row running max (log2) and sum
-    __shared__ int s_last;                     // pieces: this CTA is the last piece of its pair to finish
 
     const int C = gridDim.y;                   // cluster size = entry splits per (request, kv head)
     const int G = p.nq / p.nkv;
@@ -492,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (p.items != nullptr) {
             // piece partial to global scratch: O [Rq][hd], then the running
-            // max (log2) and sum of each row, for merge_pieces
+            // max (log2) and sum of each row, for k_attn_merge
             float* w = p.ws + static_cast<size_t>(blockIdx.x) * attn_piece_floats(Rq, HD);
 #pragma unroll
             for (int c = 0; c < HD / 16; ++c) {
@@ -533,27 +463,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (!ok) __nanosleep(100000);    // a wait gave up: let copies still in flight land
-    if (p.items != nullptr && !single) {
-        // Length-aware pieces of a request with several: the last piece of
-        // this (request, kv head) to finish combines every piece's partial,
-        // read in piece order (the result does not depend on which piece
-        // arrives last): with M the largest running max, a row's output is
-        // sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i.
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            int* ticket = p.tickets + static_cast<size_t>(b) * p.nkv + kvh;
-            const int old = atomicAdd(ticket, 1);
-            const int last = old == p.plan[1 + b] - 1 ? 1 : 0;
-            if (last) atomicExch(ticket, 0);
-            s_last = last;
-        }
-        __syncthreads();
-        if (s_last) {
-            __threadfence();
-            merge_pieces<HD>(p, b, kvh, req_ok, tid, kThreads);
-        }
-    }
     if (C > 1) {
         __syncthreads();
         cluster_sync_all();
@@ -603,6 +512,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem, 256);
     }
+}
+
+// Combines the pieces of each (request, kv head) that has more than one:
+// with M the largest running max of the pieces, a row's output is
+// sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i. One thread per (query row,
+// pair of dims); the pieces are read eight at a time (all loads of a batch in
+// flight) and folded in piece order with a running max.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeBatch = 8;
+
+template <int HD>
+__global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const AttnParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int b = static_cast<int>(blockIdx.x) / p.nkv;
+    const int kvh = static_cast<int>(blockIdx.x) - b * p.nkv;
+    const int n = p.plan[1 + b];
+    if (n <= 1) return;                        // written by its only piece
+    const int G = p.nq / p.nkv;
+    const int K = p.K;
+    const int Rq = K * G;
+    const int item = static_cast<int>(blockIdx.y) * kMergeThreads + static_cast<int>(threadIdx.x);
+    const int r = item / (HD / 2);
+    if (r >= Rq) return;
+    const int d = (item - r * (HD / 2)) * 2;
+    const int off = p.plan[1 + p.B + b];
+    const int Rq4 = (Rq + 3) & ~3;
+    const size_t pf = attn_piece_floats(Rq, HD);
+    float M = -INFINITY, den = 0.f, n0 = 0.f, n1 = 0.f;
+    for (int i0 = 0; i0 < n; i0 += kMergeBatch) {
+        float mv[kMergeBatch], lv[kMergeBatch];
+        float2 ov[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            mv[u] = -INFINITY;
+            lv[u] = 0.f;
+            ov[u] = make_float2(0.f, 0.f);
+            const int slot = p.nkv * (off + i0 + u) + kvh;
+            if (i0 + u < n && slot < p.grid) {
+                const float* w = p.ws + static_cast<size_t>(slot) * pf;
+                mv[u] = w[Rq * HD + r];
+                lv[u] = w[Rq * HD + Rq4 + r];
+                ov[u] = *reinterpret_cast<const float2*>(w + r * HD + d);
+            }
+        }
+        float bm = M;
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u)
+            if (lv[u] > 0.f) bm = fmaxf(bm, mv[u]);
+        if (bm > M) {
+            // earlier sums are relative to M: bring them to the new maximum
+            const float f = exp2f(M - bm);     // 0 while nothing has been added
+            den *= f;
+            n0 *= f;
+            n1 *= f;
+            M = bm;
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            if (lv[u] > 0.f) {
+                const float f = exp2f(mv[u] - M);
+                den = fmaf(lv[u], f, den);
+                n0 = fmaf(f, ov[u].x, n0);
+                n1 = fmaf(f, ov[u].y, n1);
+            }
+        }
+    }
+    const bool req_ok = p.status[b] == PE_REQ_OK;
+    const float inv = (req_ok && den > 0.f) ? 1.f / den : 0.f;
+    const int j = r / G, g = r - (r / G) * G;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(b * K + j) * p.nq * HD +
+                         static_cast<size_t>(kvh * G + g) * HD + d;
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(n0 * inv, n1 * inv);
 }
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -762,6 +744,23 @@ int launch_attention_umma(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     if (p.hd == 64) return launch_hd<64>(tq, tk, tv, p, s, pdl);
     set_error("attention: head_dim must be 64 or 128");
     return PE_ERR_UNSUPPORTED;
+}
+
+int launch_attention_merge(const AttnParams& p, cudaStream_t s, bool pdl) {
+    if (p.items == nullptr) return PE_OK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.B * p.nkv, ceil_div(p.K * (p.nq / p.nkv) * (p.hd / 2), kMergeThreads));
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (p.hd == 128) PE_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_attn_merge<128>, p));
+    else PE_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_attn_merge<64>, p));
+    return PE_OK;
 }
 
 }  // namespace pe

@@ -250,8 +250,7 @@ struct AttnParams {
     // length-aware pieces (tcgen05 kernel; null: one cluster of max_splits
     // CTAs per (request, kv head)): CTA i serves items[i] while i < plan[0];
     // a piece of a request with several writes its partial (O, running max,
-    // sum) to ws[i], and the last piece of its (request, kv head) to finish
-    // (tickets[b * nkv + kv head], zero between launches) combines them
+    // sum) to ws[i] and k_attn_merge combines them
     const int4* items;
     const int* plan;
     int grid;                 // CTAs launched (>= the item count)
@@ -261,7 +260,7 @@ struct AttnPlan {
     int chunk, max_splits;
     size_t ws_floats;
     int tickets;
-    bool pieces;              // length-aware pieces (merged by the last piece of each pair)
+    bool pieces;              // length-aware pieces + merge kernel
     int piece_slots;          // CTAs resident at once (SMs x CTAs per SM)
     int piece_min_tiles;
     int grid;                 // piece_slots + B * nkv
@@ -275,6 +274,8 @@ int encode_tmap_kv(CUtensorMap* map, const void* cache, int hd, int nkv, int num
 AttnPlan plan_attention_umma(int B, int K, int nq, int nkv, int hd, int max_pages, int page_size, int num_sms);
 int launch_attention_umma(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                           cudaStream_t s, bool pdl);
+// combines the pieces of every (request, kv head) with more than one
+int launch_attention_merge(const AttnParams& p, cudaStream_t s, bool pdl);
 // floats of one piece partial in the attention scratch: O [Rq][hd], then the
 // running max [Rq] and sum [Rq], each block a multiple of 16 bytes
 __host__ __device__ inline size_t attn_piece_floats(int Rq, int hd) {

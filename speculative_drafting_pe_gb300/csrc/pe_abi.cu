@@ -797,10 +797,16 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
             ap.plan = h->attn_plan;
             ap.grid = p_at.grid;
             ap.l2_prefetch = p_at.one_wave ? 1 : 0;   // with a second wave, early prefetches only compete
-            rc = run(PE_KERNEL_ATTENTION, [&] {
-                if (!attn_umma) return launch_attention(dt, ap, s, pdl);
-                return launch_attention_umma(tm_q, tm_kc, tm_vc, ap, s, pdl);
-            });
+            // with length-aware pieces the merge kernel follows in the same
+            // profiled interval (one attention per layer)
+            rc = run(
+                PE_KERNEL_ATTENTION,
+                [&] {
+                    if (!attn_umma) return launch_attention(dt, ap, s, pdl);
+                    const int r = launch_attention_umma(tm_q, tm_kc, tm_vc, ap, s, pdl);
+                    return (r == PE_OK && p_at.pieces) ? launch_attention_merge(ap, s, pdl) : r;
+                },
+                p_at.pieces ? 2 : 1);
             if (rc != PE_OK) return rc;
         }
         if (use_chain) {

@@ -1,7 +1,6 @@
 """Length-aware attention pieces (used from 16 (request, kv head) pairs on):
 each request's cache entries cut into pieces of about the same tile count,
-the partials of a request with several pieces combined by the last of its
-pieces to finish.
+the partials of a request with several pieces combined by the merge kernel.
 Checked against the oracle on mini shapes that switch the mode on, with
 failed requests among the batch."""
 
@@ -21,10 +20,9 @@ MINI_HD128 = synth.DrafterShape("mini-hd128", 384, 4, 1, 128, 960, 3001)   # G =
 MINI_MHA = synth.DrafterShape("mini-mha", 256, 2, 2, 128, 512, 3000)       # G = 1: odd query-row counts
 
 # per-GEMM pass with logits: FC, row build, 4 x (QKV, attention, O, gate/up,
-# down), LM head, logits scaling, argmax; the pieces are merged inside the
-# attention kernel (no extra launch)
+# down), LM head, logits scaling, argmax; pieces add one merge per layer
 LAUNCHES_WITH_LOGITS = 25
-MERGES = 0
+MERGES = 4
 
 
 def _draft(shape, W, inp, K):
