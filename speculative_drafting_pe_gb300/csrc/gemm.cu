@@ -645,10 +645,10 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     }
     const int rows_per_tile = epi == EPI_SWIGLU ? 64 : kBM;
     g.m_tiles = ceil_div(M, rows_per_tile);
-    if ((epi == EPI_RESID || epi == EPI_QKV) && cluster && N > 256 && !w8) {
-        // O, down and QKV have few weight tiles (16 and 40 at the Qwen
-        // shape): narrower token tiles, down to 128 rows, when that lets the
-        // tiles fill one wave of SMs
+    if (epi == EPI_RESID && cluster && N > 256 && !w8) {
+        // O and down have few weight tiles (16 at the Qwen shape): narrower
+        // token tiles, down to 128 rows, when that lets the tiles fill one
+        // wave of SMs
         const int n_fill = num_sms / g.m_tiles;
         if (n_fill > g.n_tiles) {
             const int bn2 = round_up(ceil_div(N, n_fill), 16);
@@ -657,6 +657,44 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
                 g.n_tiles = ceil_div(N, bn2);
             }
         }
+    }
+    if (epi == EPI_RESID && cluster && N > 128 && N <= 256 && !w8) {
+        // one token tile of 129-256 rows takes the large ring (one CTA per
+        // SM); two tiles of <= 128 rows measured faster (224 rows: O 140 ->
+        // 88 us, down 150 -> 98 us per step)
+        g.n_tiles = 2;
+        g.bn = round_up(ceil_div(N, 2), 16);
+    }
+    if ((epi == EPI_SWIGLU || epi == EPI_ARGMAX) && cluster && N > 128 && N <= 512 && !w8) {
+        // gate/up and the LM head (equal token tiles: they share the
+        // activation tile shape) up to 512 rows: tiles of <= 128 rows
+        // (352 and 384 rows: gate/up 156 -> 117 us and LM head 184 -> 175 us
+        // per step against 176/192-row tiles; at 896 rows 128-row tiles were
+        // slower)
+        g.n_tiles = ceil_div(N, 128);
+        g.bn = round_up(ceil_div(N, g.n_tiles), 16);
+    }
+    if (epi == EPI_QKV && cluster && N > 128 && !w8) {
+        // QKV (40 weight tiles at the Qwen shape): the token tile that
+        // minimises ceil(tiles / SMs) * tile width, the busiest SM's share of
+        // the work (ties to the narrower tile). Measured: at 1408 rows 96-row
+        // tiles (600 tiles, two CTAs per SM) 263 -> 203 us per step against
+        // 240-row tiles; at 224 rows 80-row tiles 155 -> 118 us against one
+        // 224-row tile; at 352 rows it picks 128 (3 tiles of 128, as tuned).
+        int best_bn = g.bn, best_nt = g.n_tiles;
+        long long best = static_cast<long long>(ceil_div(g.m_tiles * g.n_tiles, num_sms)) * g.bn;
+        for (int cand = 96; cand < g.bn; cand += 16) {
+            const int nt = ceil_div(N, cand);
+            const int bn2 = round_up(ceil_div(N, nt), 16);
+            const long long cost = static_cast<long long>(ceil_div(g.m_tiles * nt, num_sms)) * bn2;
+            if (cost < best || (cost == best && bn2 < best_bn)) {
+                best = cost;
+                best_bn = bn2;
+                best_nt = nt;
+            }
+        }
+        g.bn = best_bn;
+        g.n_tiles = best_nt;
     }
     g.tiles = g.m_tiles * g.n_tiles;
     // shared-memory ring: ~100 KB (two CTAs per SM, so the next kernel's CTAs
