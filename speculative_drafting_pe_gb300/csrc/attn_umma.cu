@@ -19,13 +19,16 @@
 //   warp 5   TMEM allocation; lane 0 issues  S_t = Q K_t^T  (M=128, N=64,
 //            K=hd, both operands K-major) into one of two TMEM score
 //            buffers, and  O += P_t V_t  (M=128, N=hd, K=64) into the TMEM
-//            output accumulator. V_t is read where TMA put it, as an
-//            MN-major operand (entries are the reduction dimension, the
-//            64-dim rows the N dimension), so it is never transposed.
+//            output accumulator, with P_t read from TMEM as the A operand.
+//            V_t is read where TMA put it, as an MN-major operand (entries
+//            are the reduction dimension, the 64-dim rows the N dimension),
+//            so it is never transposed.
 //   warps 0-3  one thread per query row (= TMEM lane): read the row of S_t
 //            from TMEM, mask, keep the running max, write P_t = exp2(S - m)
-//            as bf16 into shared memory, and rescale the TMEM output row
-//            only when the running max grows by more than 2^8.
+//            as bf16 pairs over the columns of S_t it has just read (the
+//            next S MMA into that buffer is issued after this tile's P.V,
+//            and a CTA's MMAs run in issue order), and rescale the TMEM
+//            output row only when the running max grows by more than 2^8.
 // In the cluster layout the entry splits of one (request, kv head) form one
 // thread-block cluster and are combined through distributed shared memory in
 // split order; a piece of a request with several writes its partial (O,
@@ -56,12 +59,10 @@ struct Layout {
     static constexpr int kSub = HD / 64;                    // 128-byte sub-tiles per row
     static constexpr int kQBytes = kSub * kRows * 128;      // Q: kSub x [128 rows x 128 B]
     static constexpr int kKVBytes = kSub * kTile * 128;     // K or V tile: kSub x [64 entries x 128 B]
-    static constexpr int kPBytes = kRows * 128;             // P: [128 rows x 64 entries]
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kQBytes;
     static constexpr int kV = kK + kStages * kKVBytes;
-    static constexpr int kP = kV + kStages * kKVBytes;
-    static constexpr int kBar = kP + 2 * kPBytes;
+    static constexpr int kBar = kV + kStages * kKVBytes;
     static constexpr int kNumBars = 1 + 2 * kStages + 6;   // q_full, kv_full[], kv_empty[], s_full[2], p_full[2], o_done[2]
     static constexpr int kTmem = kBar + kNumBars * 8;
     static constexpr int kPages = kTmem + 16;
@@ -284,15 +285,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t p_addr = smem_u32(sm + L::kP + (t & 1) * L::kPBytes);
+                // P_t in TMEM over the columns of S_t (bf16 pairs, 8 columns
+                // per 16 entries)
+                const uint32_t p_tmem = tmem + static_cast<uint32_t>((t & 1) * kTile);
                 const uint32_t v_addr = smem_u32(sm + L::kV + (t % kStages) * L::kKVBytes);
                 // V_t as the MN-major B operand: 16 entries (two 8-row swizzle
                 // atoms, 1024 B apart) per MMA, 64-dim blocks kTile*128 B apart
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                    UmmaKind<__nv_bfloat16>::mma(t_o, umma_desc_sw128(p_addr + kk * 32),
-                                                 umma_desc_sw128_mn(v_addr + kk * 16 * 128, kTile * 128), idesc_o,
-                                                 (t > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_a_tmem(t_o, p_tmem + static_cast<uint32_t>(kk * 8),
+                                     umma_desc_sw128_mn(v_addr + kk * 16 * 128, kTile * 128), idesc_o,
+                                     (t > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(&o_done[t & 1]);
                 umma_commit(&kv_empty[t % kStages]);   // K and V of this stage are read
             }
@@ -367,23 +370,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st16(t_o + lane_off + static_cast<uint32_t>(c * 16), o16);
                 }
             }
-            // P_t row (bf16) into the K-major P tile: p = 2^(s * scale - m)
+            // P_t row (bf16 pairs) into TMEM over S_t, which this thread has
+            // read: p = 2^(s * scale - m)
             const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-            const uint32_t prow = smem_u32(sm + L::kP + (t & 1) * L::kPBytes) + static_cast<uint32_t>(row * 128);
             float psum = 0.f;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float pv[8];
+            for (int h = 0; h < 2; ++h) {
+                float pk[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    pv[i] = ex2_approx(fmaf(sv[c * 8 + i], sl2, neg_m));
-                    psum += pv[i];
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2_approx(fmaf(sv[h * 32 + 2 * i], sl2, neg_m));
+                    const float p1 = ex2_approx(fmaf(sv[h * 32 + 2 * i + 1], sl2, neg_m));
+                    psum += p0;
+                    psum += p1;
+                    pk[i] = __uint_as_float(pack_bf16(p0, p1));
                 }
-                sts128(prow + static_cast<uint32_t>((c ^ (row & 7)) << 4), pack_bf16(pv[0], pv[1]),
-                       pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
+                tmem_st16(tmem + lane_off + static_cast<uint32_t>((t & 1) * kTile + h * 16), pk);
             }
             l += psum;
-            fence_proxy_async_smem();     // generic-proxy writes (P) -> visible to the tensor core
             tc_fence_before_sync();
             mbar_arrive(&p_full[t & 1]);
         }

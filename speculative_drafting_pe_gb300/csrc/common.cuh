@@ -241,6 +241,15 @@ template <> struct UmmaKind<__nv_bfloat16> {
             "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
     }
 };
+// The same MMA with the A operand (M=128 rows x K=16, bf16 pairs packed per
+// 32-bit column, row i in lane i) read from tensor memory at `a_tmem`.
+__device__ __forceinline__ void umma_bf16_a_tmem(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
 template <> struct UmmaKind<float> {
     static constexpr uint32_t kFmt = 2;
     __device__ static __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,

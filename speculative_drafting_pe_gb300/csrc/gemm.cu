@@ -310,6 +310,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
         }
         sflag[0] = 0;
         sflag[1] = 0;
+        sflag[2] = 0;   // set when any wait of this CTA gives up
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -380,6 +381,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
                 for (; kb < kb1; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
                         ok = false;
+                        sflag[2] = 1;
                         break;
                     }
                     mbar_arrive_expect_tx(&full[s], kABytes + b_bytes);
@@ -411,6 +413,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
                 // wait until the epilogue has drained this accumulator's previous use
                 if (!mbar_wait(&tempty[acc], static_cast<uint32_t>(use & 1) ^ 1u, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
                     ok = false;
+                    sflag[2] = 1;
                     break;
                 }
                 tc_fence_after_sync();
@@ -418,6 +421,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&full[s], ph, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
                         ok = false;
+                        sflag[2] = 1;
                         break;
                     }
                     tc_fence_after_sync();
@@ -427,6 +431,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
                         for (int half = 0; half < 2 && ok; ++half) {
                             if (!mbar_wait(&cfull[c], cph, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
                                 ok = false;
+                        sflag[2] = 1;
                                 break;
                             }
                             tc_fence_after_sync();
@@ -480,11 +485,13 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
                 for (int kb = kb0; kb < kb1 && ok; ++kb) {
                     if (!mbar_wait(&full[s], ph, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
                         ok = false;
+                        sflag[2] = 1;
                         break;
                     }
                     for (int half = 0; half < 2; ++half) {
                         if (!mbar_wait(&cempty[c], cph ^ 1u, p.err, PE_DEVERR_GEMM_TIMEOUT)) {
                             ok = false;
+                        sflag[2] = 1;
                             break;
                         }
                         for (int r = t; r < kBM; r += kConvThreads)
@@ -536,7 +543,10 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
             if constexpr (W8) wsc = w8_row_scale<EPI>(p, m_tile, (warp & 3) * 32 + lane);
             const bool ok = mbar_wait(&tfull[acc], static_cast<uint32_t>(use & 1), p.err, PE_DEVERR_GEMM_TIMEOUT);
             tc_fence_after_sync();
-            if (!ok) sflag[0] = 1;
+            if (!ok) {
+                sflag[0] = 1;
+                sflag[2] = 1;
+            }
             named_bar_sync(1, 128);
             if (sflag[0]) break;
             epilogue_tile<T, EPI, W8>(p, tmem_base + static_cast<uint32_t>(acc) * acc_cols, stile, sflag,
@@ -562,9 +572,9 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
 
     tc_fence_before_sync();
     __syncthreads();
-    if (threadIdx.x == 0 && p.err != nullptr && (*reinterpret_cast<volatile unsigned*>(p.err) & PE_DEVERR_GEMM_TIMEOUT)) {
-        // A wait gave up: let any bulk copy still in flight land before this
-        // CTA's shared memory is released.
+    if (threadIdx.x == 0 && *reinterpret_cast<volatile int*>(&sflag[2])) {
+        // A wait of this CTA gave up: let any bulk copy still in flight land
+        // before its shared memory is released.
         __nanosleep(100000);
     }
     __syncthreads();
