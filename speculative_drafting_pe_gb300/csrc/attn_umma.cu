@@ -708,6 +708,7 @@ AttnPlan plan_attention_umma(int B, int K, int nq, int nkv, int hd, int max_page
         if (pairs < slots) {
             a.pieces = true;
             a.piece_slots = pairs <= slots / 2 ? slots - pairs : slots;
+            a.piece_wave = pairs <= slots / 2 ? slots : 0;
             a.piece_min_tiles = kPieceMinTiles;
             a.grid = a.piece_slots + pairs;
             a.chunk = chunk;

@@ -209,13 +209,15 @@ struct RowBuildParams {
     int32_t* order;            // OUT [B] or null: requests by decreasing seq_len (ties by index)
     // Length-aware attention pieces (null: none). Block 0 cuts every
     // request's S + K cache entries into n_b pieces of about the same tile
-    // count (total tiles / piece_slots, at least piece_min_tiles) and writes
+    // count (total tiles / piece_slots, at least piece_min_tiles; with
+    // piece_wave > 0 the smallest count from total tiles / piece_wave up
+    // whose pieces still number at most piece_wave) and writes
     // one item {b, kv head, first entry, end entry} per (piece, kv head),
     // longest requests first; item (nkv * (off_b + i) + kv head) is piece i
     // of request b. attn_plan: [0] item count, [1 + b] n_b, [1 + B + b] off_b.
     int4* attn_items;
     int* attn_plan;
-    int nkv, piece_slots, piece_min_tiles;
+    int nkv, piece_slots, piece_min_tiles, piece_wave;
 };
 int launch_row_build(int dtype, const RowBuildParams& p, cudaStream_t s, bool pdl);
 
@@ -263,6 +265,7 @@ struct AttnPlan {
     bool pieces;              // length-aware pieces + merge kernel
     int piece_slots;          // CTAs resident at once (SMs x CTAs per SM)
     int piece_min_tiles;
+    int piece_wave;           // > 0: the pieces fit one wave of this many CTAs
     int grid;                 // piece_slots + B * nkv
     bool one_wave;            // every CTA of the launch is resident at once
 };

@@ -679,6 +679,7 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
         rp.nkv = nkv;
         rp.piece_slots = p_at.piece_slots;
         rp.piece_min_tiles = p_at.piece_min_tiles;
+        rp.piece_wave = p_at.piece_wave;
         if ((rc = run(PE_KERNEL_ROW_BUILD, [&] { return launch_row_build(dt, rp, s, pdl); })) != PE_OK) return rc;
     }
     const int32_t* rp_seq = ps.j0 > 0 || ps.seq_eff_out || ps.row_off != nullptr ? h->seq_eff : seq_lens;

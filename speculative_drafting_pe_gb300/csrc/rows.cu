@@ -157,6 +157,29 @@ __global__ void __launch_bounds__(kRowThreads) k_row_build(const RowBuildParams 
         const long long all = static_cast<long long>(s_total) * p.nkv;
         int tc = static_cast<int>((all + p.piece_slots - 1) / p.piece_slots);
         tc = tc < p.piece_min_tiles ? p.piece_min_tiles : tc;
+        if (p.piece_wave > 0) {
+            // piece_slots leaves one slot per (request, kv head) for the
+            // rounding up of every request's piece count; smaller pieces
+            // often still fit the wave: take the smallest size from the
+            // even share up whose count does
+            __shared__ int s_cnt;
+            int lo = static_cast<int>((all + p.piece_wave - 1) / p.piece_wave);
+            lo = lo < p.piece_min_tiles ? p.piece_min_tiles : lo;
+            for (int c = lo; c < tc; ++c) {
+                if (tid == 0) s_cnt = 0;
+                __syncthreads();
+                int part = 0;
+                for (int q = tid; q < p.B; q += blockDim.x) part += s_t[q] > 0 ? (s_t[q] + c - 1) / c : 1;
+                if (part > 0) atomicAdd(&s_cnt, part);
+                __syncthreads();
+                const bool fits = static_cast<long long>(s_cnt) * p.nkv <= p.piece_wave;
+                __syncthreads();
+                if (fits) {
+                    tc = c;
+                    break;
+                }
+            }
+        }
         auto pieces_of = [&](int t) { return t > 0 ? (t + tc - 1) / tc : 1; };
         for (int q = tid; q < p.B; q += blockDim.x) {
             const int t = s_t[q];
