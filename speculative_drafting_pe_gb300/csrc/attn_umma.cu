@@ -474,36 +474,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t rank = cluster_ctarank();
         const uint32_t o_base = smem_u32(sm + L::kK), m_base = smem_u32(s_m), l_base = smem_u32(s_l);
         const int my_rows = (Rq - static_cast<int>(rank) + C - 1) / C;
-        for (int item = tid; item < my_rows * (HD / 2); item += kThreads) {
-            const int r = static_cast<int>(rank) + (item / (HD / 2)) * C;
-            const int d = (item - (item / (HD / 2)) * (HD / 2)) * 2;
-            // every peer's max, sum and output pair in flight at once, then
-            // combined in split order
+        // Per row, once: the weight 2^(m_sp - M) of every split with a
+        // positive sum (M the largest running max), and 1 / sum_sp l_sp w_sp;
+        // kept in this CTA's query tile, which no MMA or peer reads any more
+        float* s_w = reinterpret_cast<float*>(sm + L::kQ);                  // [row][kMaxCluster]
+        float* s_rinv = s_w + kRows * kMaxCluster;                           // [row]
+        uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_rinv + kRows);     // [row] splits with l > 0
+        if (tid < my_rows) {
+            const int r = static_cast<int>(rank) + tid * C;
             float mv[kMaxCluster], lv[kMaxCluster];
-            float2 ov[kMaxCluster];
 #pragma unroll
             for (int sp = 0; sp < kMaxCluster; ++sp) {
                 if (sp < C) {
                     mv[sp] = dsmem_ld(dsmem_addr(m_base + 4u * r, static_cast<uint32_t>(sp)));
                     lv[sp] = dsmem_ld(dsmem_addr(l_base + 4u * r, static_cast<uint32_t>(sp)));
-                    ov[sp] = dsmem_ld2(dsmem_addr(o_base + 4u * (r * HD + d), static_cast<uint32_t>(sp)));
                 }
             }
             float M = -INFINITY;
 #pragma unroll
             for (int sp = 0; sp < kMaxCluster; ++sp)
                 if (sp < C) M = fmaxf(M, mv[sp]);
-            float den = 0.f, n0 = 0.f, n1 = 0.f;
+            float den = 0.f;
+            uint32_t mask = 0u;
 #pragma unroll
             for (int sp = 0; sp < kMaxCluster; ++sp) {
                 if (sp < C && lv[sp] > 0.f) {
                     const float w = exp2f(mv[sp] - M);
                     den = fmaf(lv[sp], w, den);
+                    s_w[tid * kMaxCluster + sp] = w;
+                    mask |= 1u << sp;
+                }
+            }
+            s_rinv[tid] = (req_ok && den > 0.f) ? 1.f / den : 0.f;
+            s_mask[tid] = mask;
+        }
+        __syncthreads();
+        for (int item = tid; item < my_rows * (HD / 2); item += kThreads) {
+            const int rl = item / (HD / 2);
+            const int r = static_cast<int>(rank) + rl * C;
+            const int d = (item - rl * (HD / 2)) * 2;
+            const uint32_t mask = s_mask[rl];
+            // every weighted split's output pair in flight at once, then
+            // combined in split order
+            float2 ov[kMaxCluster];
+#pragma unroll
+            for (int sp = 0; sp < kMaxCluster; ++sp)
+                if (sp < C && ((mask >> sp) & 1u))
+                    ov[sp] = dsmem_ld2(dsmem_addr(o_base + 4u * (r * HD + d), static_cast<uint32_t>(sp)));
+            float n0 = 0.f, n1 = 0.f;
+#pragma unroll
+            for (int sp = 0; sp < kMaxCluster; ++sp) {
+                if (sp < C && ((mask >> sp) & 1u)) {
+                    const float w = s_w[rl * kMaxCluster + sp];
                     n0 = fmaf(w, ov[sp].x, n0);
                     n1 = fmaf(w, ov[sp].y, n1);
                 }
             }
-            const float inv = (req_ok && den > 0.f) ? 1.f / den : 0.f;
+            const float inv = s_rinv[rl];
             const int j = r / G, g = r - (r / G) * G;
             __nv_bfloat16* dst = out + static_cast<size_t>(b * K + j) * row_stride + static_cast<size_t>(kvh * G + g) * HD + d;
             *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(n0 * inv, n1 * inv);
