@@ -16,6 +16,8 @@
 // split to arrive at the tile's ticket sums the partials in split order
 // (0, 1, ..., S-1), so the result does not depend on arrival order, then
 // applies the epilogue and resets the ticket for the next launch.
+#include <type_traits>
+
 #include "gemm_epi.cuh"
 
 namespace pe {
@@ -28,14 +30,15 @@ constexpr int kMaxClusterSplits = 8;         // cluster split-K: at most 8 CTAs 
 constexpr int kConvStages = 2;               // W8: bf16 copies of half a weight stage, double-buffered
 constexpr uint32_t kConvBytes = kABytes;     // 128 rows x 64 k: one SW128 bf16 tile
 
-__host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn, int inv_floats, bool w8, int cstages) {
+__host__ __device__ inline size_t gemm_smem_bytes(int stages, int bn, int inv_floats, bool w8, int cstages,
+                                                  int egroups = 1) {
     const size_t b_stage = static_cast<size_t>(bn) * kRowBytes * (w8 ? 2 : 1);
     size_t off = static_cast<size_t>(stages) * (kABytes + b_stage);
     if (w8) off += static_cast<size_t>(cstages) * kConvBytes;
     off += static_cast<size_t>(2 * stages + 4 + 2 * kConvStages) * 8;   // mbarriers
     off += 16;                                        // TMEM base + flags
     off = (off + 15) & ~static_cast<size_t>(15);
-    off += static_cast<size_t>(kChunk) * kPitch * 4;  // epilogue staging tile
+    off += static_cast<size_t>(kChunk) * kPitch * 4 * egroups;  // epilogue staging tile per warp group
     off += static_cast<size_t>(inv_floats) * 4;       // folded-norm column scales
     return off + 1024;                                // base alignment slack
 }
@@ -105,10 +108,14 @@ __device__ __forceinline__ void widen_fp8_row_half(const uint8_t* raw, uint8_t* 
     }
 }
 
+// With `ngrp` groups of epilogue warps (barrier `bar`, staging tile `stile`
+// of their own), group `grp` takes the tile's 16-column chunks grp, grp +
+// ngrp, ...; the scratch split-K path runs with one group only.
 template <typename T, int EPI, bool W8>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_acc, float* stile, int* sflag,
                                               float* part, const float* inv, float xg_g, float wsc, int m_tile,
-                                              int n_tile, int split, int warp, int lane) {
+                                              int n_tile, int split, int warp, int lane, int grp = 0,
+                                              int ngrp = 1, int bar = 1) {
     const int quad = warp & 3;               // TMEM lane quadrant this warp may read
     const int ml = quad * 32 + lane;         // tile row = TMEM lane
     const uint32_t t_row = t_acc + (static_cast<uint32_t>(quad * 32) << 16);
@@ -117,7 +124,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_ac
     if (p.splits > 1 && p.cluster) {
         // cluster split-K: leave this split's partial tile in shared memory
         // (the stage ring is free once the accumulator is complete)
-        for (int c0 = 0; c0 < bn; c0 += kChunk) {
+        for (int c0 = grp * kChunk; c0 < bn; c0 += ngrp * kChunk) {
             float v[kChunk];
             tmem_ld16(t_row + c0, v);
 #pragma unroll
@@ -175,14 +182,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_ac
         }
         finish_norm_partials<EPI>(p, stile, m_tile, n_base, 1, bn, ml);
     } else {
-        for (int c0 = 0; c0 < bn; c0 += kChunk) {
+        for (int c0 = grp * kChunk; c0 < bn; c0 += ngrp * kChunk) {
             float v[kChunk];
             tmem_ld16(t_row + c0, v);
             scale_row<W8>(v, wsc);
             scale_cols(v, inv, c0, 1, kChunk);
-            apply_chunk<T, EPI>(p, v, ml, m_tile, ColMap{n_base + c0, 1, kChunk, c0}, stile, xg_g);
+            apply_chunk<T, EPI>(p, v, ml, m_tile, ColMap{n_base + c0, 1, kChunk, c0}, stile, xg_g, bar);
         }
-        finish_norm_partials<EPI>(p, stile, m_tile, n_base, 1, bn, ml);
+        finish_norm_partials<EPI>(p, stile, m_tile, n_base, 1, bn, ml, bar, grp, ngrp);
     }
 }
 
@@ -193,7 +200,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_ac
 template <typename T, int EPI, bool W8>
 __device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile, const float* part,
                                                const float* inv, float xg_g, float wsc, int m_tile, int n_tile,
-                                               int warp, int lane) {
+                                               int warp, int lane, int grp = 0, int ngrp = 1, int bar = 1) {
     const int ml = (warp & 3) * 32 + lane;
     const int bn = p.bn;
     const int C = p.splits;
@@ -201,7 +208,7 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile
     const uint32_t base = smem_u32(part);
     const int first = static_cast<int>(rank);
     const int owned = first < bn ? (bn - first + C - 1) / C : 0;
-    for (int j0 = 0; j0 < owned; j0 += kChunk) {
+    for (int j0 = grp * kChunk; j0 < owned; j0 += ngrp * kChunk) {
         const int cnt = min(kChunk, owned - j0);
         const int c0 = first + j0 * C;     // tile column of chunk column 0
         float v[kChunk];
@@ -230,9 +237,9 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile
         }
         scale_row<W8>(v, wsc);
         scale_cols(v, inv, c0, C, cnt);
-        apply_chunk<T, EPI>(p, v, ml, m_tile, ColMap{n_tile * bn + c0, C, cnt, j0}, stile, xg_g);
+        apply_chunk<T, EPI>(p, v, ml, m_tile, ColMap{n_tile * bn + c0, C, cnt, j0}, stile, xg_g, bar);
     }
-    finish_norm_partials<EPI>(p, stile, m_tile, n_tile * bn + first, C, owned, ml);
+    finish_norm_partials<EPI>(p, stile, m_tile, n_tile * bn + first, C, owned, ml, bar, grp, ngrp);
 }
 
 // ------------------------------------------------------------ kernel
@@ -244,8 +251,10 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile
 // other (the tensor cores see a bf16 x bf16 product: A and B of one
 // kind::f16 MMA share a type).
 
-template <typename T, int EPI, bool W8>
-__global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
+// EG = 2 (bf16 weights, one CTA per SM): a second group of epilogue warps
+// 6..9; the two groups take a tile's 16-column chunks in turn.
+template <typename T, int EPI, bool W8, int EG>
+__global__ void __launch_bounds__(W8 || EG == 2 ? kThreadsW8 : kThreads, EG == 2 ? 1 : 2)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
            const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -267,7 +276,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cempty + kConvStages);
     int* sflag = reinterpret_cast<int*>(tmem_slot + 1);
     float* stile = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(sflag + 3) + 15) & ~uintptr_t(15));
-    float* s_inv = stile + kChunk * kPitch;   // [inv_slots(N)] in the QKV and gate/up GEMMs
+    float* s_inv = stile + kChunk * kPitch * EG;   // [inv_slots(N)] in the QKV and gate/up GEMMs
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -300,7 +309,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 128);
+            mbar_init(&tempty[a], 128 * EG);
         }
         if constexpr (W8) {
             for (int c = 0; c < cstages; ++c) {
@@ -325,8 +334,9 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
     pdl_launch_dependents();
     // Everything but the producer and the converters waits here for the
     // previous kernel in the stream (a no-op without programmatic dependent
-    // launch); the converters only touch weights.
-    if (warp != 0 && warp < 6) pdl_wait();
+    // launch); the converters only touch weights. Warps 6..9 of the EG = 2
+    // kernel are epilogue warps: they read the previous kernel's outputs.
+    if (warp != 0 && (warp < 6 || EG == 2)) pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -515,8 +525,11 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
         // Folded RMSNorm: the scales of every token row, computed once while
         // the first mainloop runs (published by the barrier after the first
         // accumulator wait), unless there are too many rows for shared memory.
+        const int grp = (EG == 2 && warp >= 6) ? 1 : 0;     // epilogue warp group
+        const int bar = 1 + grp;                             // its named barrier (128 threads)
+        float* stile_g = stile + grp * kChunk * kPitch;      // its staging tile
         if constexpr (epi_norm_scaled<EPI>()) {
-            if (inv_all) fold_norm_scales(p, s_inv, 0, p.N, threadIdx.x - 64);
+            if (inv_all) fold_norm_scales(p, s_inv, 0, p.N, threadIdx.x - 64, 128 * EG);
         }
         int it = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
@@ -531,7 +544,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
                 if constexpr (epi_norm_scaled<EPI>()) {
                     // double-buffered: the previous tile's epilogue may still read the other half
                     float* buf = s_inv + (it & 1) * kMaxBn;
-                    fold_norm_scales(p, buf, n_tile * bn, bn, threadIdx.x - 64);
+                    fold_norm_scales(p, buf, n_tile * bn, bn, threadIdx.x - 64);   // (one warp group)
                     inv = buf;
                 }
             }
@@ -547,11 +560,12 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
                 sflag[0] = 1;
                 sflag[2] = 1;
             }
-            named_bar_sync(1, 128);
+            // both groups: the scales and sflag written before it are published
+            named_bar_sync(EG == 2 ? 3 : 1, 128 * EG);
             if (sflag[0]) break;
-            epilogue_tile<T, EPI, W8>(p, tmem_base + static_cast<uint32_t>(acc) * acc_cols, stile, sflag,
+            epilogue_tile<T, EPI, W8>(p, tmem_base + static_cast<uint32_t>(acc) * acc_cols, stile_g, sflag,
                                       reinterpret_cast<float*>(smem), inv, xg_g, wsc, m_tile, n_tile, split, warp,
-                                      lane);
+                                      lane, grp, EG, bar);
             tc_fence_before_sync();
             mbar_arrive(&tempty[acc]);
         }
@@ -562,10 +576,11 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
         decode(blockIdx.x, m_tile, n_tile, split, kb0, kb1);
         __syncthreads();              // this CTA's partial is in shared memory
         cluster_sync_all();           // ... and so are the peers'
-        if (warp >= 2 && warp < 6 && !sflag[0]) {
+        if (warp >= 2 && warp < (EG == 2 ? 10 : 6) && !sflag[0]) {
+            const int grp = (EG == 2 && warp >= 6) ? 1 : 0;
             const float* inv = inv_all ? s_inv + n_tile * bn : (norm_scaled<EPI>(p) ? s_inv : nullptr);
-            cluster_reduce<T, EPI, W8>(p, stile, reinterpret_cast<const float*>(smem), inv, xg_g, wsc, m_tile,
-                                       n_tile, warp, lane);
+            cluster_reduce<T, EPI, W8>(p, stile + grp * kChunk * kPitch, reinterpret_cast<const float*>(smem), inv,
+                                       xg_g, wsc, m_tile, n_tile, warp, lane, grp, EG, 1 + grp);
         }
         cluster_sync_all();           // peers are done reading this CTA's partial
     }
@@ -584,10 +599,10 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreads, 2)
     }
 }
 
-template <typename T, int EPI, bool W8>
+template <typename T, int EPI, bool W8, int EG>
 int launch_typed(const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B, const GemmPlan& plan,
                  const GemmParams& p, cudaStream_t stream, bool pdl) {
-    auto kern = k_gemm<T, EPI, W8>;
+    auto kern = k_gemm<T, EPI, W8, EG>;
     static size_t smem_set[64] = {};
     int dev = 0;
     PE_CUDA_TRY(cudaGetDevice(&dev));
@@ -599,7 +614,7 @@ int launch_typed(const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap&
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);
-    cfg.blockDim = dim3(W8 ? kThreadsW8 : kThreads);
+    cfg.blockDim = dim3(W8 || EG == 2 ? kThreadsW8 : kThreads);
     cfg.dynamicSmemBytes = plan.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -622,12 +637,27 @@ int launch_typed(const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap&
 template <typename T, bool W8>
 int launch_dispatch(int epi, const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B,
                     const GemmPlan& plan, const GemmParams& p, cudaStream_t stream, bool pdl) {
+    if constexpr (!W8 && std::is_same<T, __nv_bfloat16>::value) {
+        if (plan.epi_groups == 2) {
+            switch (epi) {
+                case EPI_STORE: return launch_typed<T, EPI_STORE, W8, 2>(A, A2, B, plan, p, stream, pdl);
+                case EPI_QKV: return launch_typed<T, EPI_QKV, W8, 2>(A, A2, B, plan, p, stream, pdl);
+                case EPI_RESID: return launch_typed<T, EPI_RESID, W8, 2>(A, A2, B, plan, p, stream, pdl);
+                case EPI_SWIGLU: return launch_typed<T, EPI_SWIGLU, W8, 2>(A, A2, B, plan, p, stream, pdl);
+                default: set_error("GEMM epilogue without a second epilogue warp group"); return PE_ERR_ARG;
+            }
+        }
+    }
+    if (plan.epi_groups != 1) {
+        set_error("GEMM plan with two epilogue warp groups for FP8 or fp32 weights");
+        return PE_ERR_ARG;
+    }
     switch (epi) {
-        case EPI_STORE: return launch_typed<T, EPI_STORE, W8>(A, A2, B, plan, p, stream, pdl);
-        case EPI_QKV: return launch_typed<T, EPI_QKV, W8>(A, A2, B, plan, p, stream, pdl);
-        case EPI_RESID: return launch_typed<T, EPI_RESID, W8>(A, A2, B, plan, p, stream, pdl);
-        case EPI_SWIGLU: return launch_typed<T, EPI_SWIGLU, W8>(A, A2, B, plan, p, stream, pdl);
-        case EPI_ARGMAX: return launch_typed<T, EPI_ARGMAX, W8>(A, A2, B, plan, p, stream, pdl);
+        case EPI_STORE: return launch_typed<T, EPI_STORE, W8, 1>(A, A2, B, plan, p, stream, pdl);
+        case EPI_QKV: return launch_typed<T, EPI_QKV, W8, 1>(A, A2, B, plan, p, stream, pdl);
+        case EPI_RESID: return launch_typed<T, EPI_RESID, W8, 1>(A, A2, B, plan, p, stream, pdl);
+        case EPI_SWIGLU: return launch_typed<T, EPI_SWIGLU, W8, 1>(A, A2, B, plan, p, stream, pdl);
+        case EPI_ARGMAX: return launch_typed<T, EPI_ARGMAX, W8, 1>(A, A2, B, plan, p, stream, pdl);
         default: set_error("unknown GEMM epilogue"); return PE_ERR_ARG;
     }
 }
@@ -763,13 +793,23 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     g.persistent = g.splits == 1 && g.units > 1;
     g.grid = g.persistent ? (g.units < num_sms * ctas_per_sm ? g.units : num_sms * ctas_per_sm) : g.units;
     g.ws_floats = (g.splits > 1 && !g.cluster) ? static_cast<size_t>(g.tiles) * g.splits * g.bn * kBM : 0;
+    // One CTA per SM (token tiles over 128 rows) leaves room for a second
+    // group of epilogue warps, whose share of each tile's 16-column chunks
+    // halves the epilogue after the last MMA (bf16 weights; the norm scales
+    // of every token row must fit in shared memory; not the LM head)
+    g.epi_groups = 1;
+    if (cluster && !w8 && elem_bytes == 2 && ctas_per_sm == 1 && epi != EPI_ARGMAX && N <= kMaxInvAll &&
+        (g.splits == 1 || g.cluster)) {
+        g.epi_groups = 2;
+        g.smem_bytes = gemm_smem_bytes(g.stages, g.bn, inv_floats, w8, g.cstages, 2);
+    }
     return g;
 }
 
 int gemm_store_kernels_load() {
     cudaFuncAttributes fa;
-    PE_CUDA_TRY(cudaFuncGetAttributes(&fa, k_gemm<__nv_bfloat16, EPI_STORE, false>));
-    PE_CUDA_TRY(cudaFuncGetAttributes(&fa, k_gemm<float, EPI_STORE, false>));
+    PE_CUDA_TRY(cudaFuncGetAttributes(&fa, k_gemm<__nv_bfloat16, EPI_STORE, false, 1>));
+    PE_CUDA_TRY(cudaFuncGetAttributes(&fa, k_gemm<float, EPI_STORE, false, 1>));
     return PE_OK;
 }
 

@@ -36,9 +36,10 @@ struct ColMap {
     __device__ __forceinline__ int col(int i) const { return n0 + i * cs; }
 };
 
+// `bar`: the named barrier (128 threads) of the epilogue warps applying it.
 template <typename T, int EPI>
 __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v)[kChunk], int ml, int m_tile,
-                                            const ColMap& cm, float* stile, float xg_g) {
+                                            const ColMap& cm, float* stile, float xg_g, int bar = 1) {
     auto col_ok = [&](int i) { return i < cm.cnt && cm.col(i) < p.N; };
     if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
         // all loads of the chunk first, then all stores (the destinations of
@@ -130,10 +131,10 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
         if ((lane & 1) == 0 && col_ok(c) && k[0] != 0ull) atomicMax(p.amax + cm.col(c), k[0]);
     } else if constexpr (EPI == EPI_SWIGLU) {
         // rows 0..63 of the tile are gate rows, 64..127 the matching up rows
-        named_bar_sync(1, 128);
+        named_bar_sync(bar, 128);
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) stile[i * kPitch + ml] = v[i];
-        named_bar_sync(1, 128);
+        named_bar_sync(bar, 128);
         const int fl = ml & 63;
         const int f = m_tile * 64 + fl;
         const int ibeg = (ml >> 6) * (kChunk / 2);
@@ -171,10 +172,10 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
 #pragma unroll
             for (int i = 0; i < kChunk; ++i)
                 cs[i] = col_ok(i) ? p.rope_cs[static_cast<size_t>(cm.col(i)) * half + fi] : make_float2(1.f, 0.f);
-            named_bar_sync(1, 128);
+            named_bar_sync(bar, 128);
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) stile[i * kPitch + ml] = v[i];
-            named_bar_sync(1, 128);
+            named_bar_sync(bar, 128);
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) {
                 const float y = stile[i * kPitch + partner];
@@ -210,14 +211,15 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const float (&v
 
 // Folded RMSNorm, consumer side: inv[j] = 1/rms of token row n0 + j for
 // j < count, from the producer's partial sums of squares (row n's partials
-// are contiguous, zero-padded to a multiple of 4). Thread t of the 128
-// epilogue threads takes j = t, t + 128, ...; the loads of four such rows are
-// in flight together, and each sum runs in partial order.
-__device__ __forceinline__ void fold_norm_scales(const GemmParams& p, float* inv, int n0, int count, int t) {
+// are contiguous, zero-padded to a multiple of 4). Thread t of the nthr
+// epilogue threads takes j = t, t + nthr, ...; the loads of four such rows
+// are in flight together, and each sum runs in partial order.
+__device__ __forceinline__ void fold_norm_scales(const GemmParams& p, float* inv, int n0, int count, int t,
+                                                 int nthr = 128) {
     constexpr int kCols = 4;
     constexpr int kVec = 4;   // float4 loads per row per round
     const int nvec = p.ss_ld >> 2;
-    for (int j0 = t; j0 < count; j0 += 128 * kCols) {
+    for (int j0 = t; j0 < count; j0 += nthr * kCols) {
         float ss[kCols];
 #pragma unroll
         for (int c = 0; c < kCols; ++c) ss[c] = 0.f;
@@ -225,7 +227,7 @@ __device__ __forceinline__ void fold_norm_scales(const GemmParams& p, float* inv
             float4 x[kCols][kVec];
 #pragma unroll
             for (int c = 0; c < kCols; ++c) {
-                const int j = j0 + c * 128;
+                const int j = j0 + c * nthr;
                 const bool ok = j < count && n0 + j < p.N;
                 const float4* src = reinterpret_cast<const float4*>(p.ss_in + static_cast<size_t>(n0 + j) * p.ss_ld);
 #pragma unroll
@@ -245,7 +247,7 @@ __device__ __forceinline__ void fold_norm_scales(const GemmParams& p, float* inv
         }
 #pragma unroll
         for (int c = 0; c < kCols; ++c) {
-            const int j = j0 + c * 128;
+            const int j = j0 + c * nthr;
             if (j < count) inv[j] = n0 + j < p.N ? rsqrtf(ss[c] * p.ss_scale + p.ss_eps) : 1.f;
         }
     }
@@ -276,16 +278,19 @@ __device__ __forceinline__ void scale_cols(float (&v)[kChunk], const float* inv,
 
 // Folded RMSNorm, producer side, after all chunks of a tile: the partial sum
 // of squares of each of the tile's `count` columns (token row n0 + j * cs) is
-// the four warps' slot values added in warp order.
+// the four warps' slot values added in warp order. With `ngrp` groups of
+// epilogue warps taking the 16-column chunks in turn, group `grp` (barrier
+// `bar`, its own slots in `stile`) writes the columns of its chunks.
 template <int EPI>
 __device__ __forceinline__ void finish_norm_partials(const GemmParams& p, const float* stile, int m_tile, int n0,
-                                                     int cs, int count, int ml) {
+                                                     int cs, int count, int ml, int bar = 1, int grp = 0,
+                                                     int ngrp = 1) {
     if constexpr (EPI == EPI_RESID) {
         if (p.xg == nullptr) return;
-        named_bar_sync(1, 128);
+        named_bar_sync(bar, 128);
         for (int j = ml; j < count; j += 128) {
             const int n = n0 + j * cs;
-            if (n < p.N)
+            if (n < p.N && (j / kChunk) % ngrp == grp)
                 p.ss_out[static_cast<size_t>(n) * p.ss_ld + m_tile] =
                     ((stile[j] + stile[kMaxBn + j]) + stile[2 * kMaxBn + j]) + stile[3 * kMaxBn + j];
         }

@@ -102,6 +102,7 @@ struct GemmPlan {
     bool cluster;       // splits of a tile form one thread-block cluster
     bool persistent;    // grid < units: CTAs loop over tiles
     int grid;           // CTAs launched
+    int epi_groups;     // groups of four epilogue warps (2: 320 threads, one CTA per SM)
 };
 
 GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster, bool w8 = false);

@@ -7,8 +7,8 @@ import torch
 import oracle
 from speculative_drafting_pe_gb300 import binding, synth
 
-from parity import (assert_drafts_match, assert_kv_close, assert_logits_close, oracle_batch, oracle_request,
-                    read_new_kv, weights_to)
+from parity import (GAP_MIN, LOGIT_RTOL, assert_drafts_match, assert_kv_close, assert_logits_close, oracle_batch,
+                    oracle_request, read_new_kv, weights_to)
 
 pytestmark = pytest.mark.gpu
 
@@ -212,6 +212,54 @@ def test_batched_full_size_sampled(name):
         assert_kv_close(k_got, ref["k_new"][:, 0], "k rows")
         assert_kv_close(v_got, ref["v_new"][:, 0], "v rows")
     dr.close()
+
+
+@pytest.mark.parametrize("name", ["qwen-b32-k11", "qwen-b128-k7", "qwen-b128-k11", "gptoss-b64-k10"])
+def test_batched_every_request_matches_the_request_alone(name):
+    # Every request of a full-size batch (not a sample) against the same
+    # request drafted alone at B=1, whose path the full-size B=1 tests pin
+    # to the oracle: the batched launches (other token tiles, split-K,
+    # epilogue warp groups, attention pieces) may change rounding only.
+    wl = synth.WORKLOADS[name]
+    dev = torch.device("cuda")
+    W = synth.make_weights(wl.shape, wl.seed, device=dev)
+    inp = synth.make_step_inputs(wl, device=dev)
+    V = wl.shape.vocab
+    dr = binding.Drafter(wl.shape, W, max_batch=wl.B, k_max=wl.K)
+    kc, vc = inp.k_cache.clone(), inp.v_cache.clone()
+    lg = torch.empty(wl.B, wl.K, V, device=dev)
+    d, st = dr.draft(inp.last_token, inp.target_hidden, inp.positions, inp.seq_lens, inp.page_table,
+                     inp.num_pages, kc, vc, wl.K, logits=lg)
+    torch.cuda.synchronize()
+    assert dr.device_errors() == 0
+    assert (st.cpu().numpy() == 0).all()
+    dr.close()
+    one = binding.Drafter(wl.shape, W, max_batch=1, k_max=wl.K)
+    kc1, vc1 = inp.k_cache.clone(), inp.v_cache.clone()   # each request writes only its own pages
+    lg1 = torch.empty(1, wl.K, V, device=dev)
+    bad_logits, bad_drafts = [], []
+    for b in range(wl.B):
+        s = slice(b, b + 1)
+        d1, st1 = one.draft(inp.last_token[s], inp.target_hidden[s], inp.positions[s], inp.seq_lens[s],
+                            inp.page_table[s], inp.num_pages, kc1, vc1, wl.K, logits=lg1)
+        err = (lg[b] - lg1[0]).abs().amax(dim=-1)
+        scale = lg1[0].abs().amax(dim=-1)
+        if bool((err > LOGIT_RTOL * scale).any()):
+            bad_logits.append(b)
+        top2 = lg1[0].topk(2, dim=-1).values
+        sure = (top2[:, 0] - top2[:, 1]) > GAP_MIN
+        if bool(((d[b] != d1[0]) & sure).any()):
+            bad_drafts.append(b)
+    torch.cuda.synchronize()
+    assert one.device_errors() == 0
+    assert not bad_logits, f"requests whose batched logits differ from the request alone: {bad_logits}"
+    assert not bad_drafts, f"requests whose batched drafts differ where the gap is clear: {bad_drafts}"
+    for b in range(wl.B):
+        k_b, v_b = read_new_kv(inp, kc, vc, b, wl.K)
+        k_1, v_1 = read_new_kv(inp, kc1, vc1, b, wl.K)
+        assert_kv_close(k_b, k_1, f"k rows of request {b}")
+        assert_kv_close(v_b, v_1, f"v rows of request {b}")
+    one.close()
 
 
 @pytest.mark.parametrize("name", ["qwen-b1-k7", "qwen-b128-k11"])
