@@ -750,8 +750,21 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
     g.cstages = w8 ? kConvStages : 0;
     const size_t fixed = static_cast<size_t>(g.cstages) * kConvBytes + static_cast<size_t>(kChunk) * kPitch * 4 +
                          static_cast<size_t>(inv_floats) * 4 + 2048;
+    // The ~190 KB ring (one CTA per SM, which brings the second epilogue
+    // group) for bf16 tiles of up to 128 rows too where it measured faster:
+    // QKV from 65 rows while its tiles fit one wave (B=32, K=11: 133 -> 108
+    // us per step; 600 tiles at 1408 rows were slower), gate/up from 49 to
+    // 128 rows (one token tile: 88 rows 100 -> 84 us; slower below 48 and at
+    // two or three tiles), O and down at 129-256 rows (their two tiles:
+    // 224 rows O 89 -> 77, down 100 -> 85 us)
+    bool big = false;
+    if (cluster && !w8 && elem_bytes == 2 && g.bn <= 128) {
+        if (epi == EPI_QKV) big = N > 64 && g.tiles <= num_sms;
+        else if (epi == EPI_SWIGLU) big = N > 48 && N <= 128;
+        else if (epi == EPI_RESID) big = N > 128 && N <= 256;
+    }
     const size_t budget = w8 ? (g.bn <= 64 ? 112 * 1024 : 215 * 1024) - fixed
-                             : (g.bn <= 128 ? 100 * 1024 : 190 * 1024);
+                             : ((g.bn <= 128 && !big) ? 100 * 1024 : 190 * 1024);
     int st = static_cast<int>(budget / stage);
     g.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
     g.smem_bytes = gemm_smem_bytes(g.stages, g.bn, inv_floats, w8, g.cstages);
