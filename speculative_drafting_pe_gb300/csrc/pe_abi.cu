@@ -596,12 +596,13 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
 
     // B-operand maps: the box height is the token tile of the GEMM that reads
     // the map (QKV, O and down may take narrower tiles than gate/up and the LM head)
-    CUtensorMap tm_th, tm_u, tm_xq, tm_xn, tm_attn, tm_act;
-    if (p_qkv0.bn != p_qkv.bn || p_lm.bn != p_gu.bn) { set_error("GEMM token tiles disagree"); return PE_ERR_UNSUPPORTED; }
+    CUtensorMap tm_th, tm_u, tm_xq, tm_xn, tm_xn_lm, tm_attn, tm_act;
+    if (p_qkv0.bn != p_qkv.bn) { set_error("GEMM token tiles disagree"); return PE_ERR_UNSUPPORTED; }
     if (ps.run_fc && (rc = act_map(h, &tm_th, target_hidden, fc_n, 3 * H, p_fc.bn)) != PE_OK) return rc;
     if ((rc = act_map(h, &tm_u, h->u, R, 2 * H, p_qkv.bn)) != PE_OK) return rc;      // layer 0's QKV
     if ((rc = act_map(h, &tm_xq, h->xn, R, H, p_qkv.bn)) != PE_OK) return rc;       // QKV of layers 1-3
-    if ((rc = act_map(h, &tm_xn, h->xn, R, H, p_gu.bn)) != PE_OK) return rc;        // gate/up, LM head
+    if ((rc = act_map(h, &tm_xn, h->xn, R, H, p_gu.bn)) != PE_OK) return rc;        // gate/up
+    if ((rc = act_map(h, &tm_xn_lm, h->xn, R, H, p_lm.bn)) != PE_OK) return rc;     // LM head (its own token tile)
     if ((rc = act_map(h, &tm_attn, h->attn, R, qd, p_o.bn)) != PE_OK) return rc;       // B operand of O
     if ((rc = act_map(h, &tm_act, h->act, R, F, p_down.bn)) != PE_OK) return rc;       // B operand of down
     CUtensorMap tm_kc, tm_vc, tm_q;
@@ -735,7 +736,7 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
         cp.nphases = 4;
         const CUtensorMap* a1[4] = {&h->tm_o[l], &h->tm_gate[l], &h->tm_down[l], l < 3 ? &h->tm_qkv[l + 1] : &h->tm_lm};
         const CUtensorMap* a2[4] = {&h->tm_o[l], &h->tm_up[l], &h->tm_down[l], l < 3 ? &h->tm_qkv[l + 1] : &h->tm_lm};
-        const CUtensorMap* bm[4] = {&tm_attn, &tm_xn, &tm_act, &tm_xn};
+        const CUtensorMap* bm[4] = {&tm_attn, &tm_xn, &tm_act, l < 3 ? &tm_xn : &tm_xn_lm};
         const GemmParams gps[4] = {gp_o(l), gp_gu(l), gp_down(l), l < 3 ? gp_qkv(l + 1) : gp_lm()};
         const int epis[4] = {EPI_RESID, EPI_SWIGLU, EPI_RESID, l < 3 ? EPI_QKV : EPI_ARGMAX};
         const int mt[4] = {(H + 127) / 128, F / 64, (H + 127) / 128, l < 3 ? qkv_rows / 128 : (V + 127) / 128};
@@ -836,7 +837,7 @@ int enqueue_pass(pe_handle* h, const PassSpec& ps, const void* target_hidden, co
     if (!use_chain) {
         GemmParams p = gp_lm();
         rc = run(PE_KERNEL_LM_HEAD,
-                 [&] { return launch_gemm(dt, EPI_ARGMAX, h->tm_lm, h->tm_lm, tm_xn, p_lm, p, s, pdl); });
+                 [&] { return launch_gemm(dt, EPI_ARGMAX, h->tm_lm, h->tm_lm, tm_xn_lm, p_lm, p, s, pdl); });
         if (rc != PE_OK) return rc;
     }
     if (ps.logits != nullptr) {
