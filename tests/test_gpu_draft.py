@@ -262,6 +262,32 @@ def test_batched_every_request_matches_the_request_alone(name):
     one.close()
 
 
+@pytest.mark.parametrize("name", ["qwen-b32-k7", "qwen-b128-k11", "gptoss-b64-k10"])
+def test_full_size_batches_are_deterministic(name):
+    # The same batch drafted twice (two epilogue warp groups, attention
+    # pieces, split-K clusters): every logit, draft and cache row must repeat
+    # bit for bit; a read racing with an earlier kernel's writes would not.
+    wl = synth.WORKLOADS[name]
+    dev = torch.device("cuda")
+    W = synth.make_weights(wl.shape, wl.seed, device=dev)
+    inp = synth.make_step_inputs(wl, device=dev)
+    dr = binding.Drafter(wl.shape, W, max_batch=wl.B, k_max=wl.K)
+    runs = []
+    for _ in range(2):
+        kc, vc = inp.k_cache.clone(), inp.v_cache.clone()
+        lg = torch.empty(wl.B, wl.K, wl.shape.vocab, device=dev)
+        d, st = dr.draft(inp.last_token, inp.target_hidden, inp.positions, inp.seq_lens, inp.page_table,
+                         inp.num_pages, kc, vc, wl.K, logits=lg)
+        torch.cuda.synchronize()
+        runs.append((lg, d, kc, vc))
+    assert dr.device_errors() == 0
+    (l1, d1, k1, v1), (l2, d2, k2, v2) = runs
+    assert torch.equal(d1, d2)
+    assert torch.equal(l1, l2)
+    assert torch.equal(k1, k2) and torch.equal(v1, v2)
+    dr.close()
+
+
 @pytest.mark.parametrize("name", ["qwen-b1-k7", "qwen-b128-k11"])
 def test_step_graph_without_logits_matches_oracle(name):
     # The exact call the benchmark times: draft (no logits output) + verify
