@@ -313,7 +313,7 @@ int pe_linear_fp8(int32_t M, int32_t N, int32_t Kd, const void* w, const float* 
                   float* ws, int32_t* tickets, void* stream);
 
 /* pe_linear for callers that cannot allocate device memory (this entry point
- * has no counterpart in the paper). Some callers may not call cudaMalloc
+ * has no counterpart in the method's description). Some callers may not call cudaMalloc
  * where they run a GEMM: code running while another thread captures a CUDA
  * graph in global capture mode, where cudaMalloc is prohibited, or runtimes
  * whose device memory is fully reserved by their own allocator. This variant
@@ -375,7 +375,7 @@ void pe_step_graph_destroy(pe_step_graph* g);
 int pe_device_errors(pe_handle* h, void* stream, uint32_t* out_bits);
 
 /* Test support for the bounded-wait give-up path (no counterpart in the
- * paper; host-side fault injection, nothing on the device is made to fault).
+ * method's description; host-side fault injection, nothing on the device is made to fault).
  * Enqueues on `stream` a write that primes the arrival tickets of the first
  * phase of the handle's persistent layer chain so that its shared tiles never
  * complete. The next pe_draft's chain launches then wait for a phase that
