@@ -405,23 +405,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             __nv_bfloat16* dst = out + static_cast<size_t>(b * K + j) * row_stride + static_cast<size_t>(kvh * G + g) * HD;
             const float inv = (req_ok && have_o && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
-            for (int c = 0; c < HD / 16; ++c) {
-                float o16[16];
+            for (int c = 0; c < HD / 64; ++c) {
+                float o64[64];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) o16[i] = 0.f;
-                if (have_o) tmem_ld16(t_o + lane_off + static_cast<uint32_t>(c * 16), o16);
+                for (int i = 0; i < 64; ++i) o64[i] = 0.f;
+                if (have_o) tmem_ld64(t_o + lane_off + static_cast<uint32_t>(c * 64), o64);
                 if (row_ok) {
-                    uint4 w0, w1;
-                    w0.x = pack_bf16(o16[0] * inv, o16[1] * inv);
-                    w0.y = pack_bf16(o16[2] * inv, o16[3] * inv);
-                    w0.z = pack_bf16(o16[4] * inv, o16[5] * inv);
-                    w0.w = pack_bf16(o16[6] * inv, o16[7] * inv);
-                    w1.x = pack_bf16(o16[8] * inv, o16[9] * inv);
-                    w1.y = pack_bf16(o16[10] * inv, o16[11] * inv);
-                    w1.z = pack_bf16(o16[12] * inv, o16[13] * inv);
-                    w1.w = pack_bf16(o16[14] * inv, o16[15] * inv);
-                    *reinterpret_cast<uint4*>(dst + c * 16) = w0;
-                    *reinterpret_cast<uint4*>(dst + c * 16 + 8) = w1;
+#pragma unroll
+                    for (int h = 0; h < 8; ++h) {
+                        const float* o8 = o64 + h * 8;
+                        uint4 w;
+                        w.x = pack_bf16(o8[0] * inv, o8[1] * inv);
+                        w.y = pack_bf16(o8[2] * inv, o8[3] * inv);
+                        w.z = pack_bf16(o8[4] * inv, o8[5] * inv);
+                        w.w = pack_bf16(o8[6] * inv, o8[7] * inv);
+                        *reinterpret_cast<uint4*>(dst + c * 64 + h * 8) = w;
+                    }
                 }
             }
         } else if (p.items != nullptr) {
@@ -429,16 +428,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             // max (log2) and sum of each row, for k_attn_merge
             float* w = p.ws + static_cast<size_t>(blockIdx.x) * attn_piece_floats(Rq, HD);
 #pragma unroll
-            for (int c = 0; c < HD / 16; ++c) {
-                float o16[16];
+            for (int c = 0; c < HD / 64; ++c) {
+                float o64[64];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) o16[i] = 0.f;
-                if (have_o) tmem_ld16(t_o + lane_off + static_cast<uint32_t>(c * 16), o16);
+                for (int i = 0; i < 64; ++i) o64[i] = 0.f;
+                if (have_o) tmem_ld64(t_o + lane_off + static_cast<uint32_t>(c * 64), o64);
                 if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < 16; i += 4)
-                        *reinterpret_cast<float4*>(w + row * HD + c * 16 + i) =
-                            make_float4(o16[i], o16[i + 1], o16[i + 2], o16[i + 3]);
+                    for (int i = 0; i < 64; i += 4)
+                        *reinterpret_cast<float4*>(w + row * HD + c * 64 + i) =
+                            make_float4(o64[i], o64[i + 1], o64[i + 2], o64[i + 3]);
                 }
             }
             if (row_ok) {
@@ -446,17 +445,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 w[Rq * HD + ((Rq + 3) & ~3) + row] = l;
             }
         } else {
-            // split partial into this CTA's shared memory (the K stage ring is free)
+            // split partial into this CTA's shared memory (the K stage ring is
+            // free): row r's 16-byte chunk q at chunk q ^ (r & 7), so that the
+            // eight rows of a quarter warp store to distinct banks
             float* s_o = reinterpret_cast<float*>(sm + L::kK);   // [Rq][hd] fp32
 #pragma unroll
-            for (int c = 0; c < HD / 16; ++c) {
-                float o16[16];
+            for (int c = 0; c < HD / 64; ++c) {
+                float o64[64];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) o16[i] = 0.f;
-                if (have_o) tmem_ld16(t_o + lane_off + static_cast<uint32_t>(c * 16), o16);
+                for (int i = 0; i < 64; ++i) o64[i] = 0.f;
+                if (have_o) tmem_ld64(t_o + lane_off + static_cast<uint32_t>(c * 64), o64);
                 if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) s_o[row * HD + c * 16 + i] = o16[i];
+                    for (int q = 0; q < 16; ++q) {
+                        const int qs = (c * 16 + q) ^ (row & 7);
+                        *reinterpret_cast<float4*>(s_o + row * HD + qs * 4) =
+                            make_float4(o64[4 * q], o64[4 * q + 1], o64[4 * q + 2], o64[4 * q + 3]);
+                    }
                 }
             }
             if (row_ok) {
@@ -514,13 +519,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = static_cast<int>(rank) + rl * C;
             const int d = (item - rl * (HD / 2)) * 2;
             const uint32_t mask = s_mask[rl];
+            // the pair's float index in the partial (its 16-byte chunk swizzled by the row)
+            const int oi = r * HD + ((((d >> 2) ^ (r & 7)) << 2) | (d & 3));
             // every weighted split's output pair in flight at once, then
             // combined in split order
             float2 ov[kMaxCluster];
 #pragma unroll
             for (int sp = 0; sp < kMaxCluster; ++sp)
                 if (sp < C && ((mask >> sp) & 1u))
-                    ov[sp] = dsmem_ld2(dsmem_addr(o_base + 4u * (r * HD + d), static_cast<uint32_t>(sp)));
+                    ov[sp] = dsmem_ld2(dsmem_addr(o_base + 4u * oi, static_cast<uint32_t>(sp)));
             float n0 = 0.f, n1 = 0.f;
 #pragma unroll
             for (int sp = 0; sp < kMaxCluster; ++sp) {
