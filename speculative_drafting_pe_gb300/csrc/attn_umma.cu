@@ -98,7 +98,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* o_done = p_full + 2;         // [2]: P.V of tiles with this parity complete
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmem);
     int* s_pages = reinterpret_cast<int*>(sm + L::kPages);
-    __shared__ float s_m[kRows], s_l[kRows];   // this split's per-row running max (log2) and sum
+    // Cluster combine: the running max (log2) and sum of row r from split sp,
+    // held by the CTA that combines row r (rank r mod C) at (r / C) * C + sp
+    __shared__ float2 s_ml[kRows + kMaxCluster];
 
     const int C = gridDim.y;                   // cluster size = entry splits per (request, kv head)
     const int G = p.nq / p.nkv;
@@ -465,8 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (row_ok) {
-                s_m[row] = m_used;
-                s_l[row] = l;
+                // this split's max and sum of the row, straight into the table
+                // of the CTA that combines it (published by the cluster barrier)
+                const uint32_t at = smem_u32(&s_ml[(row / C) * C + static_cast<int>(cluster_ctarank())]);
+                dsmem_st2(dsmem_addr(at, static_cast<uint32_t>(row % C)), m_used, l);
             }
         }
     }
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync_all();
         // CTA `rank` combines rows rank, rank + C, ... from all C partials, in split order
         const uint32_t rank = cluster_ctarank();
-        const uint32_t o_base = smem_u32(sm + L::kK), m_base = smem_u32(s_m), l_base = smem_u32(s_l);
+        const uint32_t o_base = smem_u32(sm + L::kK);
         const int my_rows = (Rq - static_cast<int>(rank) + C - 1) / C;
         // Per row, once: the weight 2^(m_sp - M) of every split with a
         // positive sum (M the largest running max), and 1 / sum_sp l_sp w_sp;
@@ -486,13 +490,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* s_rinv = s_w + kRows * kMaxCluster;                           // [row]
         uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_rinv + kRows);     // [row] splits with l > 0
         if (tid < my_rows) {
-            const int r = static_cast<int>(rank) + tid * C;
             float mv[kMaxCluster], lv[kMaxCluster];
 #pragma unroll
             for (int sp = 0; sp < kMaxCluster; ++sp) {
                 if (sp < C) {
-                    mv[sp] = dsmem_ld(dsmem_addr(m_base + 4u * r, static_cast<uint32_t>(sp)));
-                    lv[sp] = dsmem_ld(dsmem_addr(l_base + 4u * r, static_cast<uint32_t>(sp)));
+                    const float2 ml = s_ml[tid * C + sp];
+                    mv[sp] = ml.x;
+                    lv[sp] = ml.y;
                 }
             }
             float M = -INFINITY;

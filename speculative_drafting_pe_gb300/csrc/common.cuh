@@ -378,6 +378,11 @@ __device__ __forceinline__ float2 dsmem_ld2(uint32_t addr) {
     asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
     return v;
 }
+// Store to the distributed shared memory of a CTA of this cluster (no
+// completion signal of its own: a cluster barrier publishes it).
+__device__ __forceinline__ void dsmem_st2(uint32_t addr, float a, float b) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
 
