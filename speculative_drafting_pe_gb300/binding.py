@@ -372,14 +372,36 @@ class StepGraph:
                         ("page_table", page_table), ("target_tokens", target_tokens)):
             _need(t, torch.int32, dev, name)
         _need(target_hidden, drafter.dtype, dev, "target_hidden")
-        z = lambda *s: torch.zeros(*s, dtype=torch.int32, device=dev)
         self.inputs = dict(last_token=last_token, target_hidden=target_hidden, positions=positions,
                            seq_lens=seq_lens, page_table=page_table, target_tokens=target_tokens,
                            k_cache=k_cache, v_cache=v_cache)
-        self.out = dict(drafts=z(B, K), draft_status=z(B), accepted=z(B), bonus=z(B), emitted=z(B, K + 1),
-                        slot_mapping=z(B, K), rollback_slots=z(B, K), status=z(B),
-                        positions=positions_out if positions_out is not None else z(B),
-                        seq_lens=seq_lens_out if seq_lens_out is not None else z(B))
+        # Every result the graph writes is a view into one int32 buffer
+        # (`out_packed`, each view 64-byte aligned), so that a caller can read
+        # all of a step's results back with a single copy.
+        shapes = dict(drafts=(B, K), draft_status=(B,), accepted=(B,), bonus=(B,), emitted=(B, K + 1),
+                      slot_mapping=(B, K), rollback_slots=(B, K), status=(B,))
+        if positions_out is None:
+            shapes["positions"] = (B,)
+        if seq_lens_out is None:
+            shapes["seq_lens"] = (B,)
+        offs, total = {}, 0
+        for name, shp in shapes.items():
+            offs[name] = total
+            n = 1
+            for d in shp:
+                n *= d
+            total += (n + 15) // 16 * 16
+        self.out_packed = torch.zeros(max(total, 16), dtype=torch.int32, device=dev)
+        self.out = {}
+        for name, shp in shapes.items():
+            n = 1
+            for d in shp:
+                n *= d
+            self.out[name] = self.out_packed.narrow(0, offs[name], n).view(*shp)
+        if positions_out is not None:
+            self.out["positions"] = positions_out
+        if seq_lens_out is not None:
+            self.out["seq_lens"] = seq_lens_out
         o = self.out
         g = _vp()
         _check(lib.pe_step_graph_create_ex(
