@@ -252,9 +252,11 @@ __device__ __forceinline__ void cluster_reduce(const GemmParams& p, float* stile
 // kind::f16 MMA share a type).
 
 // EG = 2 (bf16 weights, one CTA per SM): a second group of epilogue warps
-// 6..9; the two groups take a tile's 16-column chunks in turn.
-template <typename T, int EPI, bool W8, int EG>
-__global__ void __launch_bounds__(W8 || EG == 2 ? kThreadsW8 : kThreads, EG == 2 ? 1 : 2)
+// 6..9; the two groups take a tile's 16-column chunks in turn. ONE (FP8
+// weights): compiled for one CTA per SM, which gives the 320 threads up to
+// 168 registers instead of 96 (no split-K epilogue in local memory).
+template <typename T, int EPI, bool W8, int EG, bool ONE = false>
+__global__ void __launch_bounds__(W8 || EG == 2 ? kThreadsW8 : kThreads, EG == 2 || ONE ? 1 : 2)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
            const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -599,10 +601,10 @@ __global__ void __launch_bounds__(W8 || EG == 2 ? kThreadsW8 : kThreads, EG == 2
     }
 }
 
-template <typename T, int EPI, bool W8, int EG>
+template <typename T, int EPI, bool W8, int EG, bool ONE = false>
 int launch_typed(const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B, const GemmPlan& plan,
                  const GemmParams& p, cudaStream_t stream, bool pdl) {
-    auto kern = k_gemm<T, EPI, W8, EG>;
+    auto kern = k_gemm<T, EPI, W8, EG, ONE>;
     static size_t smem_set[64] = {};
     int dev = 0;
     PE_CUDA_TRY(cudaGetDevice(&dev));
@@ -651,6 +653,16 @@ int launch_dispatch(int epi, const CUtensorMap& A, const CUtensorMap& A2, const 
     if (plan.epi_groups != 1) {
         set_error("GEMM plan with two epilogue warp groups for FP8 or fp32 weights");
         return PE_ERR_ARG;
+    }
+    if constexpr (W8) {
+        if (plan.w8_one) {
+            switch (epi) {
+                case EPI_QKV: return launch_typed<T, EPI_QKV, W8, 1, true>(A, A2, B, plan, p, stream, pdl);
+                case EPI_RESID: return launch_typed<T, EPI_RESID, W8, 1, true>(A, A2, B, plan, p, stream, pdl);
+                case EPI_SWIGLU: return launch_typed<T, EPI_SWIGLU, W8, 1, true>(A, A2, B, plan, p, stream, pdl);
+                default: set_error("GEMM epilogue without a one-CTA-per-SM FP8 kernel"); return PE_ERR_ARG;
+            }
+        }
     }
     switch (epi) {
         case EPI_STORE: return launch_typed<T, EPI_STORE, W8, 1>(A, A2, B, plan, p, stream, pdl);
@@ -763,12 +775,19 @@ GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, b
         else if (epi == EPI_SWIGLU) big = N > 48 && N <= 128;
         else if (epi == EPI_RESID) big = N > 128 && N <= 256;
     }
-    const size_t budget = w8 ? (g.bn <= 64 ? 112 * 1024 : 215 * 1024) - fixed
+    // FP8 weights, one CTA per SM (compiled for up to 168 registers): gate/up
+    // always, QKV and O/down above 128 token rows; with fewer rows QKV and
+    // O/down measured faster at two CTAs per SM (96 registers), where they
+    // start streaming their weights beside the attention's CTAs
+    // (B=1, K=7: O and down 72/76 -> 98/108 us per step at one CTA per SM;
+    // B=128, K=11: O, down and QKV 394/463/402 -> 282/381/299)
+    g.w8_one = w8 && (epi == EPI_SWIGLU || ((epi == EPI_QKV || epi == EPI_RESID) && N > 128));
+    const size_t budget = w8 ? ((g.bn <= 64 && !g.w8_one) ? 112 * 1024 : 215 * 1024) - fixed
                              : ((g.bn <= 128 && !big) ? 100 * 1024 : 190 * 1024);
     int st = static_cast<int>(budget / stage);
     g.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
     g.smem_bytes = gemm_smem_bytes(g.stages, g.bn, inv_floats, w8, g.cstages);
-    const int ctas_per_sm = g.smem_bytes <= 113 * 1024 ? 2 : 1;
+    const int ctas_per_sm = g.w8_one ? 1 : (g.smem_bytes <= 113 * 1024 ? 2 : 1);
     int splits = 1;
     if (epi != EPI_ARGMAX) {
         if (cluster) {

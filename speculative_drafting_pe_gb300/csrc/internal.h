@@ -103,6 +103,7 @@ struct GemmPlan {
     bool persistent;    // grid < units: CTAs loop over tiles
     int grid;           // CTAs launched
     int epi_groups;     // groups of four epilogue warps (2: 320 threads, one CTA per SM)
+    bool w8_one;        // FP8 weights: the kernel compiled for one CTA per SM
 };
 
 GemmPlan plan_gemm(int M, int N, int Kd, int epi, int elem_bytes, int num_sms, bool cluster, bool w8 = false);
