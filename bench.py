@@ -51,6 +51,7 @@ def parse_args(argv=None):
     ap.add_argument("--fp8", action="store_true",
                     help="the main line with FP8 (E4M3) GEMM weights and per-row scales (bf16 activations and KV)")
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--worker-warmup", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
 
@@ -253,32 +254,39 @@ def oracle_worker(args):
              positions=inp.positions.numpy(), seq_lens=inp.seq_lens.numpy(), page_table=inp.page_table.numpy(),
              k_cache=inp.k_cache.float().numpy(), v_cache=inp.v_cache.float().numpy())
     K = wl.K
+
+    def step():
+        out = oracle.draft_pass(wl.shape, Wn, a["last_token"], a["target_hidden"], a["positions"], a["seq_lens"],
+                                a["page_table"], a["k_cache"], a["v_cache"], K)
+        g = synth.plant_targets(out["drafts"], inp.alpha, wl.shape.vocab, wl.seed)
+        acc, bonus = oracle.verify(out["drafts"], g)
+        oracle.rebuild_metadata(acc, K, a["seq_lens"], a["positions"], a["page_table"], inp.num_pages)
+
+    for _ in range(args.worker_warmup):   # untimed
+        step()
     times = []
     budget = args.cpu_seconds
     t_start = time.time()
     max_steps = args.steps
     while len(times) < max_steps:
         t0 = time.time()
-        out = oracle.draft_pass(wl.shape, Wn, a["last_token"], a["target_hidden"], a["positions"], a["seq_lens"],
-                                a["page_table"], a["k_cache"], a["v_cache"], K)
-        g = synth.plant_targets(out["drafts"], inp.alpha, wl.shape.vocab, wl.seed)
-        acc, bonus = oracle.verify(out["drafts"], g)
-        oracle.rebuild_metadata(acc, K, a["seq_lens"], a["positions"], a["page_table"], inp.num_pages)
+        step()
         times.append(time.time() - t0)
         if time.time() - t_start > budget:
             break
     print(json.dumps({"steps": len(times), "seconds": sum(times), "step_s": times,
-                      "cores": len(os.sched_getaffinity(0))}))
+                      "warmup": args.worker_warmup, "cores": len(os.sched_getaffinity(0))}))
 
 
-def run_oracle_subprocess(workload, seconds, max_steps, fp8=False):
+def run_oracle_subprocess(workload, seconds, max_steps, fp8=False, warmup=0):
     cores = len(os.sched_getaffinity(0))
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = str(cores)
     env["CUDA_VISIBLE_DEVICES"] = ""
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker", "--workload", workload,
-           "--cpu-seconds", str(seconds), "--steps", str(max_steps)] + (["--fp8"] if fp8 else [])
+           "--cpu-seconds", str(seconds), "--steps", str(max_steps),
+           "--worker-warmup", str(warmup)] + (["--fp8"] if fp8 else [])
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=seconds * 6 + 600)
     if r.returncode != 0:
         raise RuntimeError("oracle worker failed: " + r.stderr[-2000:])
@@ -765,7 +773,7 @@ def bench_reference(args):
         return
     from speculative_drafting_pe_gb300 import synth
     wl = synth.WORKLOADS[args.workload]
-    res = run_oracle_subprocess(args.workload, max(args.cpu_seconds, 60.0), args.steps)
+    res = run_oracle_subprocess(args.workload, max(args.cpu_seconds, 60.0), args.steps, warmup=args.warmup)
     value = res["steps"] / res["seconds"]
     base = cpu_baseline_obj(res, wl)
     line = {
@@ -776,7 +784,7 @@ def bench_reference(args):
         "n_gpus": world,
         "steps": res["steps"],
         "steps_requested": args.steps,
-        "warmup": 0,
+        "warmup": res["warmup"],
         "ms_per_step": 1e3 / value,
         "higher_is_better": True,
         "scaling": "weak",
